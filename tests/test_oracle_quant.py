@@ -1,0 +1,243 @@
+"""Pins for the oracle's quantisers, stochastic rounding and Philox (no GPU)."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from precision_moe_numerics_gb300 import workloads as W
+
+
+# Known-answer vectors published with Random123 (D. E. Shaw Research), the
+# reference distribution of Salmon et al., SC'11, for philox4x32 with 10 rounds.
+PHILOX_KAT = [
+    ([0, 0, 0, 0], [0, 0], [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]),
+    ([0xFFFFFFFF] * 4, [0xFFFFFFFF] * 2, [0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD]),
+    ([0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344], [0xA4093822, 0x299F31D0],
+     [0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1]),
+]
+
+
+@pytest.mark.parametrize("ctr,key,want", PHILOX_KAT)
+def test_philox_known_answers(ctr, key, want):
+    assert list(oracle.philox4x32_10(ctr, key)) == want
+
+
+def test_sr_bits_mapping():
+    seed, tag = 0x1234567890ABCDEF, 3
+    for i in [0, 1, 7, 8, 9, 12345, (1 << 33) + 5]:
+        j = i // 8
+        w = oracle.philox4x32_10([j & 0xFFFFFFFF, j >> 32, tag, 0], [seed & 0xFFFFFFFF, seed >> 32])
+        word = int(w[(i % 8) // 2])
+        want = (word >> 16) if i % 2 else (word & 0xFFFF)
+        assert oracle.sr_bits16(seed, tag, i) == want
+
+
+# ------------------------------------------------------------------ NVFP4 block
+def test_absmax_minus_54_example(golden):
+    ex = golden["absmax_block_example"]
+    rng = np.random.default_rng(0)
+    x = (rng.standard_normal(16) * 5).astype(np.float32)
+    x[3] = ex["absmax_value"]
+    codes, sbyte, _ = oracle.nvfp4_quantize_block(x, 1.0)
+    assert oracle.e4m3_value(sbyte) == ex["scale"]
+    assert oracle.e2m1_value(codes[3]) == ex["code_value"]
+
+
+def test_five_point_four_example_forward(golden):
+    ex = golden["transpose_sr_example"]
+    x = np.zeros(16, np.float32)
+    x[0] = -54.0
+    x[5] = ex["x"]
+    codes, sbyte, _ = oracle.nvfp4_quantize_block(x, 1.0)
+    assert oracle.e4m3_value(sbyte) == ex["forward_scale"]
+    assert oracle.e2m1_value(codes[5]) == ex["forward_code_value"]
+    deq = oracle.nvfp4_dequant_f32(np.array([[codes[0] | (codes[1] << 4), codes[2] | (codes[3] << 4),
+                                              codes[4] | (codes[5] << 4)] + [0] * 5], np.uint8),
+                                   np.array([[sbyte]], np.uint8), np.array([1.0], np.float32))
+    assert deq[0, 5] == ex["forward_dequant"]
+
+
+def _brute_nearest_code(p):
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    a = min(abs(float(p)), 6.0)
+    d = [abs(a - m) for m in mags]
+    best = min(range(8), key=lambda c: (d[c], c % 2))
+    return best | (8 if np.signbit(p) else 0)
+
+
+def test_block_codes_are_nearest_of_scaled_values():
+    """codes = nearest grid point of x * (1/(dec(S) g)) computed in binary32;
+    S = nearest E4M3 of amax / (6 g)."""
+    rng = np.random.default_rng(1)
+    for t in range(300):
+        x = (rng.standard_normal(16) * 10.0 ** rng.uniform(-3, 3)).astype(np.float32)
+        g = np.float32(10.0 ** rng.uniform(-4, 1))
+        codes, sbyte, m = oracle.nvfp4_quantize_block(x, g)
+        assert m == 6
+        amax = np.max(np.abs(x))
+        s = np.float32(amax / np.float32(np.float32(6.0) * g))
+        assert sbyte == oracle.e4m3_rne(s)
+        sd = np.float32(np.float32(oracle.e4m3_value(sbyte)) * g)
+        r = np.float32(1.0) / sd if sd != 0 else np.float32(0)
+        for i in range(16):
+            assert codes[i] == _brute_nearest_code(np.float32(x[i] * r)), (t, i)
+
+
+def test_four_over_six_picks_exact_candidate():
+    # values exactly on the grid for scale 1 with m = 4 (amax 4), not with m = 6
+    x = np.array([4, 3, 2, 1, -4, -3, -2, -1, 0.5, 1.5, 4, 3, 2, 1, 0, 0], np.float32)
+    codes, sbyte, m = oracle.nvfp4_quantize_block(x, 1.0, four_over_six=True)
+    assert m == 4 and oracle.e4m3_value(sbyte) == 1.0
+    assert np.array_equal([oracle.e2m1_value(c) for c in codes], x)
+    codes6, _, m6 = oracle.nvfp4_quantize_block(x, 1.0, four_over_six=False)
+    assert m6 == 6 and not np.array_equal([oracle.e2m1_value(c) for c in codes6], x)
+    # a block exact for m = 6: ties keep 6
+    y = np.array([6, 3, 1.5, -6, 0.5, 1, 2, 4] * 2, np.float32)
+    _, sb, m = oracle.nvfp4_quantize_block(y, 1.0, four_over_six=True)
+    assert m == 6 and oracle.e4m3_value(sb) == 1.0
+
+
+def _sse(x, codes, sbyte, g):
+    deq = np.array([np.float32(np.float32(oracle.e2m1_value(c) * oracle.e4m3_value(sbyte)) * g) for c in codes])
+    return float(np.sum((x.astype(np.float64) - deq) ** 2))
+
+
+def test_four_over_six_never_worse():
+    rng = np.random.default_rng(2)
+    better = 0
+    for _ in range(400):
+        x = (rng.standard_normal(16) * 3).astype(np.float32)
+        g = np.float32(np.max(np.abs(x)) / 1792.0)
+        c46, s46, m = oracle.nvfp4_quantize_block(x, g, True)
+        c6, s6, _ = oracle.nvfp4_quantize_block(x, g, False)
+        e46, e6 = _sse(x, c46, s46, g), _sse(x, c6, s6, g)
+        assert e46 <= e6 * (1 + 1e-5) + 1e-30
+        better += m == 4
+    assert 0 < better < 400
+
+
+def test_outer_scale_per_row_and_group():
+    rng = np.random.default_rng(4)
+    x = W.normal_bf16_host(rng, (40, 64))
+    xf = W.bf16_bits_to_f32(x)
+    _, _, g = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW)
+    assert np.array_equal(g, (np.abs(xf).max(1) / np.float32(2688.0)).astype(np.float32))
+    _, _, g46 = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW, four_over_six=True)
+    assert np.array_equal(g46, (np.abs(xf).max(1) / np.float32(1792.0)).astype(np.float32))
+    offs = [0, 16, 16, 40]
+    _, _, gg = oracle.nvfp4_quantize(x, oracle.OUTER_PER_GROUP, group_offsets=offs)
+    assert gg[0] == np.float32(np.abs(xf[:16]).max() / np.float32(2688.0))
+    assert gg[1] == 1.0
+    assert gg[2] == np.float32(np.abs(xf[16:]).max() / np.float32(2688.0))
+    # block scales always fit E4M3 without saturating
+    c, s, g = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW, four_over_six=True)
+    assert np.all(s != 0x7F) and np.all(s != 0xFF)
+
+
+def test_quantize_row_matches_blockwise_and_packing():
+    rng = np.random.default_rng(6)
+    x = W.normal_bf16_host(rng, (8, 48), 1.0, 0.05, 30.0)
+    codes, scales, g = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW, four_over_six=True)
+    xf = W.bf16_bits_to_f32(x)
+    for r in range(8):
+        for b in range(3):
+            cb, sb, _ = oracle.nvfp4_quantize_block(xf[r, b * 16:(b + 1) * 16], g[r], True)
+            packed = codes[r, b * 8:(b + 1) * 8]
+            assert np.array_equal(packed & 15, cb[0::2]) and np.array_equal(packed >> 4, cb[1::2])
+            assert scales[r, b] == sb
+
+
+def test_zero_rows_and_blocks():
+    x = np.zeros((3, 32), np.uint16)
+    x[1, 0] = 0x8000  # -0.0
+    codes, scales, g = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW, four_over_six=True)
+    assert np.all(g == 1.0) and np.all(scales == 0)
+    assert codes[1, 0] & 15 == 8 and np.all(codes[0] == 0)
+
+
+def test_dequant_error_bound():
+    """|x - deq| <= half the grid step at x's magnitude, plus the binary32 roundings."""
+    rng = np.random.default_rng(8)
+    x = W.normal_bf16_host(rng, (16, 256), 1.0, 0.01, 30.0)
+    c, s, g = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW)
+    deq = oracle.nvfp4_dequant_f32(c, s, g)
+    xf = W.bf16_bits_to_f32(x).astype(np.float64)
+    sd = np.array([[oracle.e4m3_value(b) for b in row] for row in s]) * g[:, None].astype(np.float64)
+    step = np.repeat(sd, 16, axis=1)
+    mag = np.abs(xf) / step
+    half = np.where(mag < 2, 0.25, np.where(mag < 4, 0.5, 1.0))
+    # saturation: a block scale rounded down can push |x|/sd above 6
+    bound = np.maximum(half, mag - 6.0) * step * (1 + 1e-5) + 1e-30
+    assert np.all(np.abs(xf - deq) <= bound)
+
+
+# ------------------------------------------------------------------ SR [SR]
+def test_sr_example_on_fp4_grid_exact(golden):
+    ex = golden["transpose_sr_example"]
+    y = ex["forward_dequant"] / ex["backward_scale"]
+    assert y == ex["backward_scaled"]
+    assert oracle.e2m1_value(oracle.e2m1_rne(y)) == ex["rn_value"]
+    counts = {}
+    for rb in range(65536):
+        v = oracle.e2m1_value(oracle.e2m1_sr(y, rb))
+        counts[v] = counts.get(v, 0) + 1
+    assert sorted(counts) == ex["sr_values"]
+    for v, p in zip(ex["sr_values"], ex["sr_probabilities"]):
+        assert Fraction(counts[v], 65536) == Fraction(p)
+    mean = sum(v * n for v, n in counts.items()) / 65536 * ex["backward_scale"]
+    assert mean == ex["expected_dequant"]
+
+
+def test_sr_example_statistics_with_philox(golden):
+    """10^6 draws with the Philox bit stream: frequency of 3 within 5 sigma of 1/4."""
+    ex = golden["transpose_sr_example"]
+    n = 1_000_000
+    # the 16-bit stream for indices 0..n-1 = the Philox words in order
+    words = np.empty((n // 8, 4), np.uint32)
+    for j in range(n // 8):
+        words[j] = oracle.philox4x32_10([int(j) & 0xFFFFFFFF, int(j) >> 32, 9, 0], [0, 0])
+    bits = np.stack([words & 0xFFFF, words >> 16], axis=2).reshape(-1)
+    up = bits < int(0.25 * 65536)
+    p = up.mean()
+    sigma = np.sqrt(0.25 * 0.75 / n)
+    assert abs(p - ex["sr_probabilities"][1]) < 5 * sigma
+    mean = (2.0 + up.astype(np.float64)).mean() * ex["backward_scale"]
+    assert abs(mean - ex["expected_dequant"]) < 5 * sigma * ex["backward_scale"]
+
+
+def test_sr_e4m3_analogue_and_unbiased():
+    # 2.0625 lies a quarter of the way from 2.0 to 2.25 on the E4M3 grid
+    ups = sum(oracle.e4m3_value(oracle.e4m3_sr(2.0625, rb)) == 2.25 for rb in range(65536))
+    assert ups == 16384
+    rng = np.random.default_rng(9)
+    for y in rng.uniform(-448, 448, 40).tolist() + [1e-5, -3e-3, 447.9]:
+        tot = Fraction(0)
+        vals = set()
+        for rb in range(0, 65536, 1):
+            v = oracle.e4m3_value(oracle.e4m3_sr(y, rb))
+            vals.add(v)
+            tot += Fraction(v)
+        mean = tot / 65536
+        lo, hi = min(vals), max(vals)
+        assert len(vals) <= 2
+        step = Fraction(hi) - Fraction(lo) if hi != lo else Fraction(0)
+        assert abs(mean - Fraction(y)) <= step / 65536
+
+
+def test_sr_on_grid_values_is_exact():
+    for b in range(0, 0x7F):
+        y = oracle.e4m3_value(b)
+        for rb in (0, 1, 12345, 65535):
+            assert oracle.e4m3_sr(y, rb) == b
+
+
+def test_e8m0_exponent_closed_forms():
+    f = oracle.e8m0_exponent
+    assert f(448.0) == 0 and f(449.0) == 1 and f(224.0) == -1 and f(224.5) == 0
+    assert f(0.0) == -127 and f(1e-45) == -127 and f(3e38) == 120
+    assert f(448.0 * 2.0 ** 40) == 40 and f(448.0 * 2.0 ** 40 * (1 + 2 ** -20)) == 41
+    assert f(127 / 64, 127 / 64) == 0 and f(2.0, 127 / 64) == 1 and f(127 / 128, 127 / 64) == -1
+    for a in np.random.default_rng(1).uniform(1e-6, 1e6, 200):
+        e = f(a)
+        assert a <= 448.0 * 2.0 ** e and a > 448.0 * 2.0 ** (e - 1)
