@@ -1,0 +1,233 @@
+/*
+ * pmn.h -- C ABI of the block-scaled MoE expert-layer numerics library
+ * (GB300, sm_103a).
+ *
+ * The operations follow the page "Thinking Machines ... Inkling 2 Small ...
+ * native 4-bit forward passes" (arex-research.com, 2026-11-14), cited by
+ * section:
+ *   [Bits]   "fewer bits, faster arithmetic" (更少的比特换更快的算术)
+ *   [Layers] "only the expert forward in 4-bit" (只把专家层的前向传播降到 4-bit)
+ *   [SR]     "transpose regroups, stochastic rounding keeps the expectation"
+ *            (转置打散分组,随机舍入保住期望值)
+ *   [NVLink] "NVLink becomes the bottleneck" (计算提速后,NVLink 通信成了新瓶颈)
+ *   [Cost]   "the recipe's costs" (配方的代价)
+ *
+ * Conventions for every call
+ *  - All tensor arguments are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or synchronises the device inside a call.  Work is
+ *    enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy
+ *    default stream) and returns immediately.
+ *  - Layouts are row-major and dense unless a leading dimension is given.
+ *    NVFP4 tensor [R, C]: codes uint8 [R, C/2] (element 2i in the low nibble,
+ *    2i+1 in the high nibble), scales uint8 [R, C/16] (E4M3), outer float32.
+ *    MXFP8 tensor [R, C]: values uint8 [R, C] (E4M3), scales uint8 [R, C/32]
+ *    (E8M0, value 2^(b-127)).  S2F6 tensor [R, C]: int8 [R, C] (k/64), scales
+ *    uint8 [R, C/32] (E8M0).  bf16 tensors are uint16 bit patterns.
+ *  - Pointers must be 16-byte aligned; sizes must satisfy the per-call rules
+ *    below.  Arguments are checked on the host before anything is enqueued;
+ *    a violation returns PMN_ERR_INVALID_ARG and enqueues nothing.
+ *  - A failed launch returns PMN_ERR_CUDA.  Kernels never trap: a bounded
+ *    device-side wait that runs out latches a bit in a device error word and
+ *    the kernel returns; pmn_get_device_error() reads and clears it.
+ *  - Every result is bit-reproducible run to run (no atomics in reductions
+ *    whose order could change a value).
+ */
+#ifndef PMN_H
+#define PMN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PMN_API __attribute__((visibility("default")))
+#else
+#define PMN_API
+#endif
+
+typedef int pmn_status;
+#define PMN_OK 0
+#define PMN_ERR_INVALID_ARG 1
+#define PMN_ERR_UNSUPPORTED 2
+#define PMN_ERR_CUDA 3
+#define PMN_ERR_TIMEOUT 4
+
+/* input modes of pmn_nvfp4_quantize */
+#define PMN_IN_BF16 0
+#define PMN_IN_BF16_SWIGLU 1
+/* outer-scale modes */
+#define PMN_OUTER_PER_ROW 0
+#define PMN_OUTER_PER_GROUP 1
+/* rounding of pmn_requant_transpose_sr_mxfp8 */
+#define PMN_ROUND_SR 0
+#define PMN_ROUND_RN 1
+/* GEMM outputs / epilogues */
+#define PMN_OUT_BF16 0
+#define PMN_OUT_F32 1
+#define PMN_OUT_RHT_S2F6 2
+/* grouping of pmn_gemm_mxfp8 */
+#define PMN_GROUP_M 0
+#define PMN_GROUP_K 1
+
+/* device error bits (pmn_get_device_error) */
+#define PMN_DEVERR_WAIT_TIMEOUT 1
+#define PMN_DEVERR_BAD_OFFSETS 2
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+PMN_API int pmn_version(void);
+
+/* Human-readable name of a status code (static string). */
+PMN_API const char *pmn_status_string(pmn_status s);
+
+/* Reads and clears the device error word; synchronises `stream` only.
+ * *err receives the PMN_DEVERR_* bits latched since the last call. */
+PMN_API pmn_status pmn_get_device_error(void *stream, int32_t *err);
+
+/*
+ * NVFP4 quantisation [SR] (16-value blocks, E4M3 block scale set from the
+ * block absmax, E2M1 codes by round-to-nearest-even) with a float32 outer
+ * scale per row or per group of rows [Cost] and the optional 4/6 choice
+ * between two candidate block scales [Cost].
+ *
+ *  x        bf16 [rows, ldx] (PMN_IN_BF16: the row's first `cols` values are
+ *           quantised) or bf16 [rows, ldx] holding gate | up halves of width
+ *           `cols` each (PMN_IN_BF16_SWIGLU: h = silu(gate) * up is formed in
+ *           float32, rounded to bf16, then quantised).
+ *  rows, cols  cols % 16 == 0, cols <= 8192 (one row lives in one CTA).
+ *  ldx      leading dimension of x in elements (>= cols, or >= 2*cols).
+ *  outer_mode  PMN_OUTER_PER_ROW: outer[rows], g = amax(row) / M.
+ *           PMN_OUTER_PER_GROUP: outer[rows / rows_per_group], g over each
+ *           block of rows_per_group consecutive rows (one expert's weight
+ *           matrix, or the whole tensor).  M = 6 * 448, or 4 * 448 with
+ *           four_over_six; g = 1 for an all-zero row/group.
+ *  rows_per_group  PER_GROUP only: rows % rows_per_group == 0.
+ *  four_over_six   0 or 1: keep, per block, the candidate scale amax/6 or
+ *           amax/4 with the smaller squared dequantisation error (ties: 6).
+ *  codes    out uint8 [rows, cols/2];  scales  out uint8 [rows, cols/16];
+ *  outer    out float32 (see outer_mode).
+ *  h_out    optional out bf16 [rows, cols]: the SwiGLU value that was
+ *           quantised (PMN_IN_BF16_SWIGLU only; NULL to skip).
+ * PER_GROUP enqueues a reduction pass, the quantisation pass and a finishing
+ * pass; `outer` holds intermediate values until the last pass completes.
+ */
+PMN_API pmn_status pmn_nvfp4_quantize(const void *x, int64_t rows, int64_t cols, int64_t ldx, int in_mode,
+                              int outer_mode, int64_t rows_per_group, int four_over_six,
+                              uint8_t *codes, uint8_t *scales, float *outer, void *h_out,
+                              void *stream);
+
+/*
+ * Dequantise -> transpose -> requantise to MXFP8 [SR]: the saved NVFP4 tensor
+ * is dequantised in float32, d = (code * scale) * g, transposed, and rounded
+ * to E4M3 with one E8M0 scale per 32 values along the ORIGINAL rows.  The
+ * scale exponent is the smallest e with amax <= 448 * 2^e (never clips), so
+ * stochastic rounding keeps E[result] = d ([SR]: E[w_q] = E[(w_q^T)^T]).
+ *
+ *  codes, scales  NVFP4 [batch, rows, cols] (batch = experts for weights, 1
+ *           for activations).
+ *  outer    float32: PMN_OUTER_PER_ROW -> [batch * rows] (tokens);
+ *           PMN_OUTER_PER_GROUP -> [batch] (one per expert).
+ *  rows     multiple of 32 (expert segments of activations must be padded
+ *           with zero rows to multiples of 32 so blocks never straddle).
+ *  cols     multiple of 64.
+ *  seed, tag  stochastic rounding bits: element i of the output (row-major
+ *           index over [batch, cols, rows]) takes 16 bits from Philox4x32-10
+ *           (Salmon et al., SC'11) with key (seed lo, seed hi) and counter
+ *           (i/8 lo, i/8 hi, tag, 0), word (i%8)/2, low half for even i; it
+ *           rounds away from zero iff bits < frac * 2^16.
+ *  rounding PMN_ROUND_SR or PMN_ROUND_RN (nearest even; bits unused).
+ *  out      uint8 [batch, cols, rows] (E4M3); out_scales uint8 [batch, cols,
+ *           rows/32] (E8M0).
+ */
+PMN_API pmn_status pmn_requant_transpose_sr_mxfp8(const uint8_t *codes, const uint8_t *scales,
+                                          const float *outer, int outer_mode, int64_t batch,
+                                          int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,
+                                          int rounding, uint8_t *out, uint8_t *out_scales,
+                                          void *stream);
+
+/*
+ * bf16 -> MXFP8 with round-to-nearest-even (the gradient dY; the pages ask
+ * for SR on the saved forward tensors only).  Same scale rule as above.
+ *  transpose 0: out [rows, cols], out_scales [rows, cols/32] (cols % 32 == 0)
+ *  transpose 1: out [cols, rows], out_scales [cols, rows/32] (rows % 32 == 0)
+ */
+PMN_API pmn_status pmn_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int transpose,
+                              uint8_t *out, uint8_t *out_scales, void *stream);
+
+/*
+ * Grouped NVFP4 expert GEMM for the forward pass [Layers], [Cost]:
+ *   Z[m, n] = (sum_k A[m, k] * B_e[n, k]) * a_outer[m] * b_outer[e]
+ * for the rows m of expert e, offsets[e] <= m < offsets[e+1].  A and B are
+ * NVFP4 with the contraction along their rows (K-major); the products are
+ * accumulated in float32 on the tensor cores (block-scaled MMA).
+ *
+ *  a_codes/a_scales  NVFP4 [total_rows, k]; a_outer float32 [total_rows].
+ *  b_codes/b_scales  NVFP4 [num_experts, n, k]; b_outer float32 [num_experts].
+ *  offsets  DEVICE int32 [num_experts + 1], non-decreasing, 0 <= offsets[e]
+ *           <= total_rows (any row counts, empty experts allowed).  They are
+ *           read and checked on the device: invalid offsets run nothing and
+ *           latch PMN_DEVERR_BAD_OFFSETS.  num_experts <= 1024.
+ *  n        multiple of 128;  k multiple of 256.
+ *  out_kind PMN_OUT_BF16 (bf16 [total_rows, n]) or PMN_OUT_F32.
+ */
+PMN_API pmn_status pmn_grouped_gemm_nvfp4(const uint8_t *a_codes, const uint8_t *a_scales,
+                                  const float *a_outer, const uint8_t *b_codes,
+                                  const uint8_t *b_scales, const float *b_outer,
+                                  const int32_t *offsets, int num_experts, int64_t total_rows,
+                                  int64_t n, int64_t k, int out_kind, void *out, void *stream);
+
+/*
+ * w2 GEMM with the combine quantisation fused into its epilogue [NVLink]:
+ * the grouped NVFP4 GEMM above, then for every 32 contiguous outputs of a row
+ *   z = RN(1/sqrt(32)) * FWHT32(sigma . x)   (float32 butterflies h=1..16)
+ *   e = smallest integer with amax(|z|) <= (127/64) * 2^e   (E8M0 byte e+127)
+ *   k = round-to-nearest-even(z * 2^(6-e))                   (S2F6 int8)
+ * sigma in {+-1}^32 is bit j of Philox4x32-10 word 0 at counter (0, 0, 5, 0)
+ * with key (seed lo, seed hi), bit set -> -1, the same for every block.
+ *  out      int8 [total_rows, n];  out_scales uint8 [total_rows, n/32].
+ * Other arguments as pmn_grouped_gemm_nvfp4.
+ */
+PMN_API pmn_status pmn_w2_gemm_rht_s2f6(const uint8_t *a_codes, const uint8_t *a_scales,
+                                const float *a_outer, const uint8_t *b_codes,
+                                const uint8_t *b_scales, const float *b_outer,
+                                const int32_t *offsets, int num_experts, int64_t total_rows,
+                                int64_t n, int64_t k, uint64_t seed, int8_t *out,
+                                uint8_t *out_scales, void *stream);
+
+/*
+ * The combine quantisation alone on a float32 tensor [NVLink] (the same
+ * epilogue arithmetic as pmn_w2_gemm_rht_s2f6, for unfused use):
+ *  x float32 [rows, cols], cols % 32 == 0 -> out int8 [rows, cols],
+ *  out_scales uint8 [rows, cols/32].
+ */
+PMN_API pmn_status pmn_rht_s2f6_quantize(const float *x, int64_t rows, int64_t cols, uint64_t seed,
+                                 int8_t *out, uint8_t *out_scales, void *stream);
+
+/*
+ * Grouped MXFP8 GEMM for the backward pass [SR] (E4M3 operands with E8M0
+ * scales per 32 along the contraction, float32 accumulation):
+ *   C[m, n] = sum_k A[m, k] * B[n, k]
+ * group_mode PMN_GROUP_M (dX = dY . W): A [m, k], B [num_groups, n, k];
+ *           rows of group g are offsets[g] <= row < offsets[g+1]; out [m, n].
+ * group_mode PMN_GROUP_K (dW = dY^T . X per expert): A [m, k], B [n, k] with k
+ *           the routed-row axis; group g contracts offsets[g] <= k <
+ *           offsets[g+1] (multiples of 32); out [num_groups, m, n].
+ *  offsets  DEVICE int32 [num_groups + 1], non-decreasing, within [0, m]
+ *           (GROUP_M) or [0, k] and multiples of 32 (GROUP_K); checked on the
+ *           device (invalid: nothing runs, PMN_DEVERR_BAD_OFFSETS latched).
+ *  scale tensors need a row pitch that is a multiple of 16 bytes: k % 512 == 0.
+ *  m        multiple of 128 for PMN_GROUP_K;  n multiple of 128;  k multiple
+ *           of 512.  num_groups <= 1024.
+ *  out_kind PMN_OUT_BF16 or PMN_OUT_F32.
+ */
+PMN_API pmn_status pmn_gemm_mxfp8(const uint8_t *a, const uint8_t *a_scales, const uint8_t *b,
+                          const uint8_t *b_scales, const int32_t *offsets, int num_groups,
+                          int group_mode, int64_t m, int64_t n, int64_t k, int out_kind, void *out,
+                          void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PMN_H */

@@ -1,0 +1,223 @@
+// numerics.cuh -- device-side format codecs, rounding and random bits for the
+// block-scaled MoE numerics (GB300, sm_103a).
+//
+// Formats (page "Thinking Machines ... Inkling 2 Small", arex-research.com):
+//   E2M1 codes {+-0, 0.5, 1, 1.5, 2, 3, 4, 6}       section [SR], first paragraph
+//   E4M3 block scales of NVFP4, E8M0 scales of MXFP8  section [SR] / [Bits]
+//   S2F6 combine format, int8 k = value * 64           section [NVLink]
+// E4M3 / E8M0 bit layouts follow the OCP Microscaling spec v1.0.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pmn {
+
+// ---------------------------------------------------------------- decoders
+// E2M1 magnitude code m (0..7): e = m >> 1, mantissa bit m & 1; e == 0 is the
+// subnormal 0 / 0.5, otherwise (1 + mant/2) * 2^(e-1).  Built as float bits.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t code)
+{
+    uint32_t m = code & 7u;
+    uint32_t bits = (m >= 2u) ? ((((m >> 1) + 126u) << 23) | ((m & 1u) << 22))
+                              : (m == 1u ? 0x3F000000u : 0u);
+    return __uint_as_float(bits | ((code & 8u) << 28));
+}
+
+// E4M3 (bias 7, subnormal m * 2^-9); NaN (S.1111.111) never reaches here.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b)
+{
+    uint32_t e = (b >> 3) & 15u, m = b & 7u;
+    float v = (e == 0u) ? (float)m * 0.001953125f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+    return (b & 0x80u) ? -v : v;
+}
+
+// 2^(b - 127) for an E8M0 byte b in [0, 254].
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b)
+{
+    return b == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+}
+
+// ---------------------------------------------------------------- hardware RN
+// Two binary32 values -> two E2M1 codes, round to nearest even, saturating;
+// `lo` lands in bits 3:0, `hi` in bits 7:4.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tcvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+// One binary32 value -> E4M3 byte, round to nearest even, saturating at 448.
+__device__ __forceinline__ uint32_t cvt_e4m3(float v)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(r) : "f"(v), "f"(0.0f));
+    return (uint32_t)r & 0xFFu;
+}
+
+// ---------------------------------------------------------------- E8M0 exponents
+// Smallest integer e with a <= 448 * 2^e (448 = 1.75 * 2^8), clamped to
+// [-127, 127]; -127 for a == 0.  a is a finite non-negative binary32.
+__device__ __forceinline__ int mx_exponent_448(float a)
+{
+    uint32_t bits = __float_as_uint(a);
+    uint32_t E = bits >> 23, m = bits & 0x7FFFFFu;
+    if (E == 0u) return -127;  // zero or subnormal: 2^-126 <= 448 * 2^-127
+    int e = (m <= 0x600000u) ? (int)E - 135 : (int)E - 134;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// Smallest integer e with a <= (127/64) * 2^e (127/64 = 1.984375), clamped.
+__device__ __forceinline__ int mx_exponent_s2f6(float a)
+{
+    uint32_t bits = __float_as_uint(a);
+    uint32_t E = bits >> 23, m = bits & 0x7FFFFFu;
+    if (E == 0u) return (m <= 0x7F0000u) ? -127 : -126;
+    int e = (m <= 0x7E0000u) ? (int)E - 127 : (int)E - 126;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// ---------------------------------------------------------------- E4M3 from d * 2^-e
+// Rounds y = d * 2^-e (|y| <= 448 by the exponent rule) onto the E4M3 grid by
+// integer arithmetic on the binary32 bits of d, so no intermediate is rounded:
+//   |d| = M * 2^ex,  L = floor(log2 |y|),  grid step 2^u with u = max(L,-6)-3,
+//   |y| / 2^u = n + F / 2^D  (n integer part, F the D discarded bits).
+// stochastic: away from zero iff rb16 < (F / 2^D) * 2^16;
+// otherwise    round to nearest, ties to even n.
+// The sign of d is kept (negative values that round to zero give 0x80).
+__device__ __forceinline__ uint32_t e4m3_round_scaled(float d, int e, uint32_t rb16, bool stochastic)
+{
+    uint32_t bits = __float_as_uint(d);
+    uint32_t sign = (bits >> 24) & 0x80u;
+    uint32_t a = bits & 0x7FFFFFFFu;
+    if (a == 0u) return sign;
+    uint32_t E = a >> 23;
+    uint32_t M = (E == 0u) ? a : ((a & 0x7FFFFFu) | 0x800000u);
+    int ex = (E == 0u) ? -149 : (int)E - 150;
+    int L = (31 - __clz(M)) + ex - e;
+    int u = (L < -6 ? -6 : L) - 3;
+    int s = ex - e - u;
+    uint32_t n;
+    bool up;
+    if (s >= 0) {
+        n = M << s;  // exact: |y| / 2^u < 2^18
+        up = false;
+    } else {
+        int D = -s;
+        uint64_t F;
+        if (D >= 32) {
+            n = 0u;
+            F = M;  // all bits fractional
+        } else {
+            n = M >> D;
+            F = M & ((1u << D) - 1u);
+        }
+        if (stochastic) {
+            if (D <= 16) up = rb16 < (uint32_t)(F << (16 - D));
+            else if (D - 16 >= 40) up = (rb16 == 0u) && (F != 0u);
+            else up = ((uint64_t)rb16 << (D - 16)) < F;
+        } else {
+            if (D >= 40) up = false;  // F < 2^24 < half
+            else {
+                uint64_t half = 1ull << (D - 1);
+                up = (F > half) || (F == half && (n & 1u));
+            }
+        }
+    }
+    uint32_t q = n + (up ? 1u : 0u);
+    uint32_t code;
+    if (q < 8u) code = q;                                        // subnormal (u == -9)
+    else if (q < 16u) code = ((uint32_t)(u + 10) << 3) | (q - 8u);
+    else code = (uint32_t)(u + 11) << 3;                         // carried into next binade
+    return sign | code;
+}
+
+// ---------------------------------------------------------------- Philox4x32-10
+// Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
+// SC'11: ten rounds of two 32x32->64 multiplies (multipliers 0xD2511F53,
+// 0xCD9E8D57) with the key added by xor and bumped by the Weyl constants
+// (0x9E3779B9, 0xBB67AE85) between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1)
+{
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// 16 random bits for elements 8j .. 8j+7 of a tensor (tag selects the
+// tensor): counter (j lo, j hi, tag, 0), key (seed lo, seed hi); element
+// 8j + t takes word t/2, low half for even t.
+struct SrBits8 {
+    uint4 w;
+    __device__ __forceinline__ uint32_t get(int t) const
+    {
+        uint32_t word = (t >> 1) == 0 ? w.x : (t >> 1) == 1 ? w.y : (t >> 1) == 2 ? w.z : w.w;
+        return (t & 1) ? (word >> 16) : (word & 0xFFFFu);
+    }
+};
+
+__device__ __forceinline__ SrBits8 sr_bits8(uint64_t seed, uint32_t tag, uint64_t j)
+{
+    SrBits8 b;
+    b.w = philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), tag, 0u), (uint32_t)seed,
+                        (uint32_t)(seed >> 32));
+    return b;
+}
+
+// ---------------------------------------------------------------- RHT + S2F6
+// In-register 32-point randomised Hadamard transform and S2F6 block
+// quantisation [NVLink]: v = sigma . x; butterflies (a, b) -> (a + b, a - b)
+// for strides 1, 2, 4, 8, 16; z = v * RN(1/sqrt(32)); e = smallest exponent
+// with amax <= (127/64) 2^e; k = rint(z * 2^(6 - e)).  Returns the E8M0 byte
+// and writes 32 int8 codes packed little-endian into q[8].
+__device__ __forceinline__ uint32_t rht32_s2f6(float (&v)[32], uint32_t sigma, uint32_t (&q)[8])
+{
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        if ((sigma >> j) & 1u) v[j] = -v[j];
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if ((i & h) == 0) {
+                float a = v[i], b = v[i + h];
+                v[i] = __fadd_rn(a, b);
+                v[i + h] = __fsub_rn(a, b);
+            }
+        }
+    }
+    const float rs = __uint_as_float(0x3E3504F3u);  // RN(1/sqrt(32))
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        v[j] = __fmul_rn(v[j], rs);
+        amax = fmaxf(amax, fabsf(v[j]));
+    }
+    int e = mx_exponent_s2f6(amax);
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        uint32_t packed = 0u;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            int k = __float2int_rn(ldexpf(v[4 * w + t], 6 - e));
+            k = k > 127 ? 127 : (k < -128 ? -128 : k);
+            packed |= ((uint32_t)k & 0xFFu) << (8 * t);
+        }
+        q[w] = packed;
+    }
+    return (uint32_t)(e + 127);
+}
+
+__device__ __forceinline__ uint32_t rht_sigma(uint64_t seed)
+{
+    return philox4x32_10(make_uint4(0u, 0u, 5u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32)).x;
+}
+
+}  // namespace pmn

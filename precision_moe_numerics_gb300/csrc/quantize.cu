@@ -1,0 +1,532 @@
+// quantize.cu -- HBM-bound quantisation kernels of the MoE expert-layer path:
+//   pmn_nvfp4_quantize              NVFP4 with outer scales and 4/6   [SR], [Cost]
+//   pmn_mxfp8_quantize              bf16 -> MXFP8 (RN), both orientations
+//   pmn_requant_transpose_sr_mxfp8  dequant -> transpose -> SR MXFP8  [SR]
+//   pmn_rht_s2f6_quantize           RHT-32 + S2F6 combine quantisation [NVLink]
+// Sections cited are those of the page "Thinking Machines ... Inkling 2
+// Small ... native 4-bit forward" (arex-research.com).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/pmn.h"
+#include "numerics.cuh"
+
+using namespace pmn;
+
+namespace {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline pmn_status launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? PMN_OK : PMN_ERR_CUDA;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// ------------------------------------------------------------------ NVFP4 block
+// One candidate block scale m (6, or 4 for the 4/6 choice) with outer scale g:
+//   s = amax / (m g); S = RN_E4M3(s); sd = dec(S) g; r = 1/sd (0 if sd == 0)
+//   c_i = RN_E2M1(x_i r)   (packed: element 2i low nibble)
+// Returns the summed squared dequantisation error (tree order i+8, +4, +2, +1)
+// when want_err is set.
+struct BlockQ {
+    uint32_t w0, w1;  // 8 code bytes
+    uint32_t sbyte;
+};
+
+__device__ __forceinline__ float quant_block_candidate(const float (&x)[16], float amax, float g, float m,
+                                                       bool want_err, BlockQ &out)
+{
+    float s = __fdiv_rn(amax, __fmul_rn(m, g));
+    uint32_t S = cvt_e4m3(s);
+    float dS = e4m3_to_f32(S);
+    float sd = __fmul_rn(dS, g);
+    float r = (sd == 0.0f) ? 0.0f : __fdiv_rn(1.0f, sd);
+    uint32_t c[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = cvt_e2m1x2(__fmul_rn(x[2 * i], r), __fmul_rn(x[2 * i + 1], r));
+    out.w0 = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+    out.w1 = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+    out.sbyte = S;
+    if (!want_err) return 0.0f;
+    float e[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        uint32_t code = (c[i >> 1] >> (4 * (i & 1))) & 15u;
+        float deq = __fmul_rn(__fmul_rn(e2m1_to_f32(code), dS), g);
+        float d = __fsub_rn(x[i], deq);
+        e[i] = __fmul_rn(d, d);
+    }
+#pragma unroll
+    for (int h = 8; h >= 1; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < h; ++i) e[i] = __fadd_rn(e[i], e[i + h]);
+    return e[0];
+}
+
+__device__ __forceinline__ BlockQ quant_block(const float (&x)[16], float g, bool four_over_six)
+{
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    BlockQ q6, q4;
+    float err6 = quant_block_candidate(x, amax, g, 6.0f, four_over_six, q6);
+    if (four_over_six) {
+        float err4 = quant_block_candidate(x, amax, g, 4.0f, true, q4);
+        if (err4 < err6) return q4;
+    }
+    return q6;
+}
+
+// outer scale g = amax / M (M = 6*448, or 4*448 with 4/6), 1 for a zero group
+__device__ __forceinline__ float outer_from_amax(float amax, bool four_over_six)
+{
+    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, four_over_six ? 1792.0f : 2688.0f);
+}
+
+// One warp per row; lane handles 16-blocks lane, lane+32, ...  NB = blocks per
+// lane (ceil(cols/16/32)).  The whole row stays in registers, so x is read
+// once.  SWIGLU: h = silu(gate) * up in binary32, rounded to bf16 first.
+template <int NB, bool SWIGLU>
+__global__ void __launch_bounds__(256) nvfp4_quant_rows_kernel(
+    const uint16_t *__restrict__ x, int64_t rows, int cols, int64_t ldx, int per_group,
+    int64_t rows_per_group, const uint32_t *__restrict__ group_amax, int four_over_six,
+    uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, float *__restrict__ outer,
+    uint16_t *__restrict__ h_out)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int nblk = cols >> 4;
+    const uint16_t *xr = x + row * ldx;
+    uint4 v[NB][2];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+        int b = lane + 32 * i;
+        if (b < nblk) {
+            if (!SWIGLU) {
+                const uint4 *p = reinterpret_cast<const uint4 *>(xr + b * 16);
+                v[i][0] = __ldg(p);
+                v[i][1] = __ldg(p + 1);
+            } else {
+                const uint4 *pg = reinterpret_cast<const uint4 *>(xr + b * 16);
+                const uint4 *pu = reinterpret_cast<const uint4 *>(xr + cols + b * 16);
+                uint4 gv[2] = {__ldg(pg), __ldg(pg + 1)};
+                uint4 uv[2] = {__ldg(pu), __ldg(pu + 1)};
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const uint32_t *gw = reinterpret_cast<const uint32_t *>(&gv[half]);
+                    const uint32_t *uw = reinterpret_cast<const uint32_t *>(&uv[half]);
+                    uint32_t hw[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        float a0 = bf16_lo(gw[t]), a1 = bf16_hi(gw[t]);
+                        float u0 = bf16_lo(uw[t]), u1 = bf16_hi(uw[t]);
+                        float h0 = __fmul_rn(__fdiv_rn(a0, __fadd_rn(1.0f, expf(-a0))), u0);
+                        float h1 = __fmul_rn(__fdiv_rn(a1, __fadd_rn(1.0f, expf(-a1))), u1);
+                        __nv_bfloat16 b0 = __float2bfloat16_rn(h0), b1 = __float2bfloat16_rn(h1);
+                        hw[t] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
+                    }
+                    v[i][half] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                }
+                if (h_out) {
+                    uint4 *ph = reinterpret_cast<uint4 *>(h_out + row * cols + b * 16);
+                    ph[0] = v[i][0];
+                    ph[1] = v[i][1];
+                }
+            }
+            const uint32_t *w = reinterpret_cast<const uint32_t *>(&v[i][0]);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[t])), fabsf(bf16_hi(w[t]))));
+        }
+    }
+    const bool fos = four_over_six != 0;
+    float g;
+    if (!per_group) {
+        amax = warp_max(amax);
+        g = outer_from_amax(amax, fos);
+        if (lane == 0) outer[row] = g;
+    } else {
+        g = outer_from_amax(__uint_as_float(group_amax[row / rows_per_group]), fos);
+    }
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+        int b = lane + 32 * i;
+        if (b < nblk) {
+            float xf[16];
+            const uint32_t *w = reinterpret_cast<const uint32_t *>(&v[i][0]);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                xf[2 * t] = bf16_lo(w[t]);
+                xf[2 * t + 1] = bf16_hi(w[t]);
+            }
+            BlockQ q = quant_block(xf, g, fos);
+            *reinterpret_cast<uint2 *>(codes + row * (cols >> 1) + b * 8) = make_uint2(q.w0, q.w1);
+            scales[row * nblk + b] = (uint8_t)q.sbyte;
+        }
+    }
+}
+
+// amax of each group of rows (contiguous: ldx == cols), as binary32 bits,
+// combined with atomicMax (order-independent, hence deterministic).
+__global__ void __launch_bounds__(256) group_amax_kernel(const uint16_t *__restrict__ x,
+                                                         int64_t elems_per_group, int64_t chunk,
+                                                         uint32_t *__restrict__ amax_bits)
+{
+    const int64_t grp = blockIdx.y;
+    const int64_t begin = (int64_t)blockIdx.x * chunk;
+    int64_t end = begin + chunk;
+    if (end > elems_per_group) end = elems_per_group;
+    const uint16_t *base = x + grp * elems_per_group;
+    uint32_t m = 0u;
+    for (int64_t i = begin + (int64_t)threadIdx.x * 8; i < end; i += (int64_t)blockDim.x * 8) {
+        uint4 q = __ldg(reinterpret_cast<const uint4 *>(base + i));
+        uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            m = max(m, w[t] & 0x7FFFu);
+            m = max(m, (w[t] >> 16) & 0x7FFFu);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    __shared__ uint32_t red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t r = red[0];
+        for (int i = 1; i < (int)(blockDim.x >> 5); ++i) r = max(r, red[i]);
+        atomicMax(amax_bits + grp, r << 16);
+    }
+}
+
+__global__ void group_outer_finish_kernel(float *outer, int64_t groups, int four_over_six)
+{
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < groups) outer[i] = outer_from_amax(outer[i], four_over_six != 0);
+}
+
+template <int NB>
+void launch_rows(bool swiglu, dim3 grid, dim3 block, cudaStream_t s, const uint16_t *x, int64_t rows,
+                 int cols, int64_t ldx, int per_group, int64_t rpg, const uint32_t *gam, int fos,
+                 uint8_t *codes, uint8_t *scales, float *outer, uint16_t *h_out)
+{
+    if (swiglu)
+        nvfp4_quant_rows_kernel<NB, true><<<grid, block, 0, s>>>(x, rows, cols, ldx, per_group, rpg, gam, fos,
+                                                                 codes, scales, outer, h_out);
+    else
+        nvfp4_quant_rows_kernel<NB, false><<<grid, block, 0, s>>>(x, rows, cols, ldx, per_group, rpg, gam, fos,
+                                                                  codes, scales, outer, h_out);
+}
+
+// ------------------------------------------------------------------ MXFP8 RN (dY)
+// rowwise: one thread per 32-block along the row.
+__global__ void __launch_bounds__(256) mxfp8_quant_rowwise_kernel(const uint16_t *__restrict__ x,
+                                                                  int64_t nblocks, int64_t bpr,
+                                                                  uint8_t *__restrict__ out,
+                                                                  uint8_t *__restrict__ out_sc)
+{
+    int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= nblocks) return;
+    const uint4 *p = reinterpret_cast<const uint4 *>(x + t * 32);
+    uint4 q[4] = {__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3)};
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(q);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+    int e = mx_exponent_448(amax);
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t b0 = e4m3_round_scaled(bf16_lo(w[2 * i]), e, 0u, false);
+        uint32_t b1 = e4m3_round_scaled(bf16_hi(w[2 * i]), e, 0u, false);
+        uint32_t b2 = e4m3_round_scaled(bf16_lo(w[2 * i + 1]), e, 0u, false);
+        uint32_t b3 = e4m3_round_scaled(bf16_hi(w[2 * i + 1]), e, 0u, false);
+        o[i] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    }
+    uint4 *po = reinterpret_cast<uint4 *>(out + t * 32);
+    po[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    po[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    out_sc[t] = (uint8_t)(e + 127);
+    (void)bpr;
+}
+
+// transposed: tile of 128 rows x 64 cols staged in shared memory; thread
+// (c, rb) quantises the 32 values of column c in row block rb.
+__global__ void __launch_bounds__(256) mxfp8_quant_transposed_kernel(const uint16_t *__restrict__ x,
+                                                                     int64_t rows, int64_t cols,
+                                                                     uint8_t *__restrict__ out,
+                                                                     uint8_t *__restrict__ out_sc)
+{
+    constexpr int TR = 128, TC = 64, PITCH = TC + 2;  // elements
+    __shared__ uint16_t tile[TR * PITCH];
+    const int64_t r0 = (int64_t)blockIdx.y * TR, c0 = (int64_t)blockIdx.x * TC;
+    // load: 128 rows x 128 bytes; thread t loads 16 bytes: row t/8 (+32k), segment t%8
+    for (int k = 0; k < 4; ++k) {
+        int rr = (threadIdx.x >> 3) + 32 * k;
+        int seg = threadIdx.x & 7;
+        uint4 q = make_uint4(0u, 0u, 0u, 0u);
+        if (r0 + rr < rows && c0 + seg * 8 < cols)
+            q = __ldg(reinterpret_cast<const uint4 *>(x + (r0 + rr) * cols + c0 + seg * 8));
+        uint32_t *dst = reinterpret_cast<uint32_t *>(tile + rr * PITCH + seg * 8);
+        dst[0] = q.x;
+        dst[1] = q.y;
+        dst[2] = q.z;
+        dst[3] = q.w;
+    }
+    __syncthreads();
+    const int c = threadIdx.x & 63, rb = threadIdx.x >> 6;
+    if (c0 + c >= cols || r0 + rb * 32 >= rows) return;
+    float v[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        v[j] = __uint_as_float((uint32_t)tile[(rb * 32 + j) * PITCH + c] << 16);
+        amax = fmaxf(amax, fabsf(v[j]));
+    }
+    int e = mx_exponent_448(amax);
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t p = 0u;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) p |= e4m3_round_scaled(v[4 * i + t], e, 0u, false) << (8 * t);
+        o[i] = p;
+    }
+    uint4 *po = reinterpret_cast<uint4 *>(out + (c0 + c) * rows + r0 + rb * 32);
+    po[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    po[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    out_sc[(c0 + c) * (rows / 32) + (r0 / 32) + rb] = (uint8_t)(e + 127);
+}
+
+// ------------------------------------------------------------------ requant [SR]
+// Tile of 128 input rows x 128 input cols.  Phase 1: dequantise
+// d = (dec(code) * dec(S)) * g in binary32 into shared memory, stored
+// transposed (row c of the output holds the 128 values d[r, c]).  Phase 2:
+// thread (c, rb) forms the 32-block of output row c, its E8M0 exponent and
+// the rounded E4M3 bytes, with 16 Philox bits per element.
+constexpr int RQ_T = 128;
+constexpr int RQ_PITCH = RQ_T + 1;
+
+__global__ void __launch_bounds__(256) requant_transpose_kernel(
+    const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, const float *__restrict__ outer,
+    int outer_per_row, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, int stochastic,
+    uint8_t *__restrict__ out, uint8_t *__restrict__ out_sc)
+{
+    extern __shared__ float dT[];  // [RQ_T (c)][RQ_PITCH (r)]
+    const int64_t b = blockIdx.z;
+    const int64_t r0 = (int64_t)blockIdx.y * RQ_T, c0 = (int64_t)blockIdx.x * RQ_T;
+    const int64_t cols2 = cols / 2, cols16 = cols / 16;
+    // phase 1: thread -> row r = t % 128, half h = t / 128 (64 columns each)
+    {
+        const int r = threadIdx.x & 127, h = threadIdx.x >> 7;
+        const int64_t src = b * rows + r0 + r;
+        const bool ok = (r0 + r < rows) && (c0 + h * 64 < cols);
+        float g = 0.0f;
+        uint4 q0 = make_uint4(0u, 0u, 0u, 0u), q1 = q0;
+        uint32_t sw = 0u;
+        if (ok) {
+            g = outer_per_row ? outer[src] : outer[b];
+            const uint8_t *pc = codes + src * cols2 + (c0 + h * 64) / 2;
+            q0 = __ldg(reinterpret_cast<const uint4 *>(pc));
+            q1 = __ldg(reinterpret_cast<const uint4 *>(pc + 16));
+            sw = __ldg(reinterpret_cast<const uint32_t *>(scales + src * cols16 + (c0 + h * 64) / 16));
+        }
+        const uint32_t cw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+            uint32_t code = (cw[j >> 3] >> (4 * (j & 7))) & 15u;
+            float dS = e4m3_to_f32((sw >> (8 * (j >> 4))) & 0xFFu);
+            float d = __fmul_rn(__fmul_rn(e2m1_to_f32(code), dS), g);
+            dT[(h * 64 + j) * RQ_PITCH + r] = ok ? d : 0.0f;
+        }
+    }
+    __syncthreads();
+    // phase 2: 128 output rows x 4 row-blocks = 512 tasks, 2 per thread
+    for (int task = threadIdx.x; task < RQ_T * 4; task += blockDim.x) {
+        const int c = task & 127, rb = task >> 7;
+        const int64_t oc = c0 + c, orow0 = r0 + rb * 32;
+        if (oc >= cols || orow0 >= rows) continue;
+        float v[32];
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            v[j] = dT[c * RQ_PITCH + rb * 32 + j];
+            amax = fmaxf(amax, fabsf(v[j]));
+        }
+        const int e = mx_exponent_448(amax);
+        const int64_t i0 = (b * cols + oc) * rows + orow0;  // output index, multiple of 32
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            SrBits8 rb8;
+            if (stochastic) rb8 = sr_bits8(seed, tag, (uint64_t)(i0 >> 3) + k);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t p = 0u;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int jj = 8 * k + 4 * h2 + t;
+                    const uint32_t bits = stochastic ? rb8.get(4 * h2 + t) : 0u;
+                    p |= e4m3_round_scaled(v[jj], e, bits, stochastic != 0) << (8 * t);
+                }
+                o[2 * k + h2] = p;
+            }
+        }
+        uint4 *po = reinterpret_cast<uint4 *>(out + i0);
+        po[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        po[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        out_sc[(b * cols + oc) * (rows / 32) + orow0 / 32] = (uint8_t)(e + 127);
+    }
+}
+
+// ------------------------------------------------------------------ RHT + S2F6
+__global__ void __launch_bounds__(256) rht_s2f6_kernel(const float *__restrict__ x, int64_t nblocks,
+                                                       uint64_t seed, int8_t *__restrict__ out,
+                                                       uint8_t *__restrict__ out_sc)
+{
+    int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= nblocks) return;
+    const uint32_t sigma = rht_sigma(seed);
+    float v[32];
+    const float4 *p = reinterpret_cast<const float4 *>(x + t * 32);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float4 f = __ldg(p + i);
+        v[4 * i] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+    }
+    uint32_t q[8];
+    uint32_t sb = rht32_s2f6(v, sigma, q);
+    uint4 *po = reinterpret_cast<uint4 *>(out + t * 32);
+    po[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    po[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    out_sc[t] = (uint8_t)sb;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" pmn_status pmn_nvfp4_quantize(const void *x, int64_t rows, int64_t cols, int64_t ldx, int in_mode,
+                                         int outer_mode, int64_t rows_per_group, int four_over_six,
+                                         uint8_t *codes, uint8_t *scales, float *outer, void *h_out,
+                                         void *stream)
+{
+    if (rows < 0 || cols <= 0 || cols % 16 != 0 || cols > 8192) return PMN_ERR_INVALID_ARG;
+    if (in_mode != PMN_IN_BF16 && in_mode != PMN_IN_BF16_SWIGLU) return PMN_ERR_INVALID_ARG;
+    if (outer_mode != PMN_OUTER_PER_ROW && outer_mode != PMN_OUTER_PER_GROUP) return PMN_ERR_INVALID_ARG;
+    if (four_over_six != 0 && four_over_six != 1) return PMN_ERR_INVALID_ARG;
+    const bool swiglu = in_mode == PMN_IN_BF16_SWIGLU;
+    if (ldx < (swiglu ? 2 * cols : cols) || ldx % 8 != 0) return PMN_ERR_INVALID_ARG;
+    if (!x || !codes || !scales || !outer) return PMN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(outer)) return PMN_ERR_INVALID_ARG;
+    if (h_out && (!swiglu || !aligned16(h_out))) return PMN_ERR_INVALID_ARG;
+    if (outer_mode == PMN_OUTER_PER_GROUP) {
+        if (swiglu || rows_per_group <= 0 || rows % rows_per_group != 0 || ldx != cols) return PMN_ERR_INVALID_ARG;
+    }
+    if (rows == 0) return PMN_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint16_t *xb = reinterpret_cast<const uint16_t *>(x);
+    const uint32_t *gam = nullptr;
+    int64_t groups = 0;
+    if (outer_mode == PMN_OUTER_PER_GROUP) {
+        groups = rows / rows_per_group;
+        const int64_t epg = rows_per_group * cols;
+        const int64_t chunk = 1 << 16;
+        if (cudaMemsetAsync(outer, 0, groups * sizeof(float), s) != cudaSuccess) return PMN_ERR_CUDA;
+        dim3 g((unsigned)((epg + chunk - 1) / chunk), (unsigned)groups);
+        group_amax_kernel<<<g, 256, 0, s>>>(xb, epg, chunk, reinterpret_cast<uint32_t *>(outer));
+        if (launch_status() != PMN_OK) return PMN_ERR_CUDA;
+        gam = reinterpret_cast<const uint32_t *>(outer);
+    }
+    const int nb = (int)((cols / 16 + 31) / 32);
+    dim3 block(256), grid((unsigned)((rows + 7) / 8));
+    const int pg = outer_mode == PMN_OUTER_PER_GROUP;
+    uint16_t *ho = reinterpret_cast<uint16_t *>(h_out);
+    if (nb <= 1) launch_rows<1>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, pg, rows_per_group, gam, four_over_six, codes, scales, outer, ho);
+    else if (nb <= 2) launch_rows<2>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, pg, rows_per_group, gam, four_over_six, codes, scales, outer, ho);
+    else if (nb <= 4) launch_rows<4>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, pg, rows_per_group, gam, four_over_six, codes, scales, outer, ho);
+    else if (nb <= 8) launch_rows<8>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, pg, rows_per_group, gam, four_over_six, codes, scales, outer, ho);
+    else launch_rows<16>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, pg, rows_per_group, gam, four_over_six, codes, scales, outer, ho);
+    if (launch_status() != PMN_OK) return PMN_ERR_CUDA;
+    if (outer_mode == PMN_OUTER_PER_GROUP) {
+        group_outer_finish_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, s>>>(outer, groups, four_over_six);
+        if (launch_status() != PMN_OK) return PMN_ERR_CUDA;
+    }
+    return PMN_OK;
+}
+
+extern "C" pmn_status pmn_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int transpose, uint8_t *out,
+                                         uint8_t *out_scales, void *stream)
+{
+    if (rows < 0 || cols < 0 || (transpose != 0 && transpose != 1)) return PMN_ERR_INVALID_ARG;
+    if (!x || !out || !out_scales || !aligned16(x) || !aligned16(out)) return PMN_ERR_INVALID_ARG;
+    if (transpose == 0 && cols % 32 != 0) return PMN_ERR_INVALID_ARG;
+    if (transpose == 1 && (rows % 32 != 0 || cols % 8 != 0)) return PMN_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return PMN_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint16_t *xb = reinterpret_cast<const uint16_t *>(x);
+    if (!transpose) {
+        const int64_t nblocks = rows * cols / 32;
+        mxfp8_quant_rowwise_kernel<<<(unsigned)((nblocks + 255) / 256), 256, 0, s>>>(xb, nblocks, cols / 32, out,
+                                                                                     out_scales);
+    } else {
+        dim3 grid((unsigned)((cols + 63) / 64), (unsigned)((rows + 127) / 128));
+        mxfp8_quant_transposed_kernel<<<grid, 256, 0, s>>>(xb, rows, cols, out, out_scales);
+    }
+    return launch_status();
+}
+
+extern "C" pmn_status pmn_requant_transpose_sr_mxfp8(const uint8_t *codes, const uint8_t *scales,
+                                                     const float *outer, int outer_mode, int64_t batch,
+                                                     int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,
+                                                     int rounding, uint8_t *out, uint8_t *out_scales,
+                                                     void *stream)
+{
+    if (batch < 0 || rows < 0 || cols < 0 || rows % 32 != 0 || cols % 32 != 0) return PMN_ERR_INVALID_ARG;
+    if (outer_mode != PMN_OUTER_PER_ROW && outer_mode != PMN_OUTER_PER_GROUP) return PMN_ERR_INVALID_ARG;
+    if (rounding != PMN_ROUND_SR && rounding != PMN_ROUND_RN) return PMN_ERR_INVALID_ARG;
+    if (!codes || !scales || !outer || !out || !out_scales) return PMN_ERR_INVALID_ARG;
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(out) || ((uintptr_t)outer & 3u)) return PMN_ERR_INVALID_ARG;
+    if (batch == 0 || rows == 0 || cols == 0) return PMN_OK;
+    if ((cols / 16) % 4 != 0) return PMN_ERR_INVALID_ARG;  // 4-byte scale words per 64 columns
+    static bool attr_done = false;
+    const int smem = RQ_T * RQ_PITCH * (int)sizeof(float);
+    if (!attr_done) {
+        if (cudaFuncSetAttribute(requant_transpose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return PMN_ERR_CUDA;
+        attr_done = true;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    dim3 grid((unsigned)((cols + RQ_T - 1) / RQ_T), (unsigned)((rows + RQ_T - 1) / RQ_T), (unsigned)batch);
+    requant_transpose_kernel<<<grid, 256, smem, s>>>(codes, scales, outer, outer_mode == PMN_OUTER_PER_ROW, rows,
+                                                     cols, seed, tag, rounding == PMN_ROUND_SR, out, out_scales);
+    return launch_status();
+}
+
+extern "C" pmn_status pmn_rht_s2f6_quantize(const float *x, int64_t rows, int64_t cols, uint64_t seed, int8_t *out,
+                                            uint8_t *out_scales, void *stream)
+{
+    if (rows < 0 || cols < 0 || cols % 32 != 0) return PMN_ERR_INVALID_ARG;
+    if (!x || !out || !out_scales || !aligned16(x) || !aligned16(out)) return PMN_ERR_INVALID_ARG;
+    const int64_t nblocks = rows * cols / 32;
+    if (nblocks == 0) return PMN_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    rht_s2f6_kernel<<<(unsigned)((nblocks + 255) / 256), 256, 0, s>>>(x, nblocks, seed, out, out_scales);
+    return launch_status();
+}

@@ -1,0 +1,71 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/pmn.h declares (no GPU needed: nothing is launched)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "pmn.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^PMN_API\s+[\w\s\*]*?\b(pmn_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from precision_moe_numerics_gb300 import build
+    return build.build()
+
+
+def test_header_declares_the_path():
+    syms = declared_symbols()
+    for name in ["pmn_nvfp4_quantize", "pmn_requant_transpose_sr_mxfp8", "pmn_grouped_gemm_nvfp4",
+                 "pmn_gemm_mxfp8", "pmn_w2_gemm_rht_s2f6", "pmn_mxfp8_quantize", "pmn_rht_s2f6_quantize",
+                 "pmn_get_device_error", "pmn_status_string", "pmn_version"]:
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(libpath):
+    L = ctypes.CDLL(libpath)
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+    from precision_moe_numerics_gb300 import pmn
+    assert set(pmn.SIGNATURES) == set(declared_symbols())
+    L.pmn_status_string.restype = ctypes.c_char_p
+    L.pmn_status_string.argtypes = [ctypes.c_int]
+    assert L.pmn_status_string(0) == b"ok"
+    assert L.pmn_version() >= 100
+
+
+def test_host_argument_checks_need_no_gpu(libpath):
+    """Invalid arguments are rejected on the host before any CUDA call."""
+    from precision_moe_numerics_gb300 import pmn
+    L = pmn.lib()
+    null = None
+    assert L.pmn_nvfp4_quantize(null, 4, 24, 24, 0, 0, 0, 0, null, null, null, null, null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_mxfp8_quantize(null, 40, 64, 1, null, null, null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_requant_transpose_sr_mxfp8(null, null, null, 0, 1, 32, 32, 0, 1, 0, null, null,
+                                            null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_grouped_gemm_nvfp4(null, null, null, null, null, null, null, 0, 0, 128, 256, 0, null,
+                                    null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_gemm_mxfp8(null, null, null, null, null, 1, 5, 128, 128, 512, 0, null, null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_rht_s2f6_quantize(null, 1, 31, 0, null, null, null) == pmn.ERR_INVALID_ARG
+
+
+def test_product_path_does_not_import_oracle():
+    """The library and its binding never reach the CPU oracle."""
+    pkg = os.path.join(ROOT, "precision_moe_numerics_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                with open(os.path.join(dirpath, fn)) as f:
+                    src = f.read()
+                assert "import oracle" not in src and "from oracle" not in src, fn
+                assert "pmn_oracle" not in src, fn

@@ -1,0 +1,192 @@
+"""GPU parity of the quantisation kernels against the CPU oracle (bit-exact).
+
+Inputs come from the seeded generators; the oracle sees the same bf16 bytes.
+Codes, scales, outer scales and MXFP8 / S2F6 bytes must match exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from precision_moe_numerics_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pmn():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from precision_moe_numerics_gb300 import build, pmn as P
+    build.build()
+    return P
+
+
+def to_dev_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def host(t):
+    if t.dtype == torch.bfloat16:
+        t = t.view(torch.int16)
+    return t.cpu().numpy()
+
+
+def assert_same(gpu, ref, what):
+    g = host(gpu) if isinstance(gpu, torch.Tensor) else gpu
+    if g.dtype == np.float32:
+        g, ref = g.view(np.uint32), np.asarray(ref, np.float32).view(np.uint32)
+    bad = np.argwhere(g != ref)
+    assert bad.size == 0, "%s: %d mismatches, first at %s: gpu %s oracle %s" % (
+        what, len(bad), bad[0], g[tuple(bad[0])], ref[tuple(bad[0])])
+
+
+@pytest.mark.parametrize("fos", [False, True])
+@pytest.mark.parametrize("shape", [(1, 16), (37, 48), (256, 256), (100, 1536), (64, 4096), (9, 8192)])
+def test_nvfp4_quantize_per_row(pmn, shape, fos):
+    rng = np.random.default_rng(hash(shape) % 1000)
+    x = W.normal_bf16_host(rng, shape, 1.0, 0.01, 30.0)
+    x[0, :16] = 0  # a zero block
+    if shape[0] > 2:
+        x[2] = 0  # a zero row
+    c, s, g = pmn.nvfp4_quantize(to_dev_bf16(x), four_over_six=fos)
+    rc, rs, rg = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW, four_over_six=fos)
+    assert_same(g, rg, "outer")
+    assert_same(s, rs, "scales")
+    assert_same(c, rc, "codes")
+
+
+def test_nvfp4_quantize_tiny_case_per_tensor(pmn):
+    d = W.tiny(0)
+    c, s, g = pmn.nvfp4_quantize(to_dev_bf16(d["x"]), outer_mode=pmn.OUTER_PER_GROUP, rows_per_group=256)
+    rc, rs, rg = oracle.nvfp4_quantize(d["x"], oracle.OUTER_PER_GROUP, group_offsets=[0, 256])
+    assert_same(g, rg, "outer")
+    assert_same(s, rs, "scales")
+    assert_same(c, rc, "codes")
+
+
+def test_nvfp4_quantize_per_expert_weights(pmn):
+    rng = np.random.default_rng(3)
+    E, N, K = 5, 96, 512
+    w = W.normal_bf16_host(rng, (E * N, K), 0.02)
+    w[N:2 * N] = 0  # an all-zero expert
+    c, s, g = pmn.nvfp4_quantize(to_dev_bf16(w), outer_mode=pmn.OUTER_PER_GROUP, rows_per_group=N)
+    rc, rs, rg = oracle.nvfp4_quantize(w, oracle.OUTER_PER_GROUP, group_offsets=np.arange(E + 1) * N)
+    assert_same(g, rg, "outer")
+    assert_same(s, rs, "scales")
+    assert_same(c, rc, "codes")
+
+
+def test_nvfp4_quantize_expert_case_activations(pmn):
+    d = W.expert(0, tokens=512)
+    c, s, g = pmn.nvfp4_quantize(to_dev_bf16(d["x"]), four_over_six=True)
+    rc, rs, rg = oracle.nvfp4_quantize(d["x"], oracle.OUTER_PER_ROW, four_over_six=True)
+    assert_same(g, rg, "outer")
+    assert_same(s, rs, "scales")
+    assert_same(c, rc, "codes")
+
+
+def test_nvfp4_quantize_swiglu(pmn):
+    """h = silu(gate) * up (glue between w1 and w2).  The GPU forms h with
+    expf in binary32; h must be within one bf16 step of the binary64 value,
+    and rows whose h equals the oracle's h bit for bit must quantise bit for bit."""
+    rng = np.random.default_rng(5)
+    rows, f = 64, 1536
+    y = W.normal_bf16_host(rng, (rows, 2 * f), 0.5)
+    c, s, g, h = pmn.nvfp4_quantize(to_dev_bf16(y), cols=f, swiglu=True, four_over_six=True, want_h=True)
+    rh = oracle.swiglu_bf16(y, f)
+    hg = host(h).view(np.uint16)
+    hf, rf = W.bf16_bits_to_f32(hg).astype(np.float64), W.bf16_bits_to_f32(rh).astype(np.float64)
+    assert np.all(np.abs(hf - rf) <= np.abs(rf) * 2.0 ** -7 + 1e-30)
+    rc, rs, rg = oracle.nvfp4_quantize(rh, oracle.OUTER_PER_ROW, four_over_six=True)
+    same = np.all(hg == rh, axis=1)
+    assert same.mean() > 0.5
+    assert_same(host(c)[same], rc[same], "codes")
+    assert_same(host(s)[same], rs[same], "scales")
+    assert_same(host(g)[same], rg[same], "outer")
+
+
+@pytest.mark.parametrize("shape", [(32, 32), (96, 256), (256, 4096), (4096, 64)])
+def test_mxfp8_quantize_rowwise(pmn, shape):
+    rng = np.random.default_rng(7)
+    x = W.normal_bf16_host(rng, shape, 1e-3, 0.01, 50.0)
+    x[0, :32] = 0
+    q, sc = pmn.mxfp8_quantize(to_dev_bf16(x), transpose=False)
+    rq, rsc = oracle.mxfp8_quantize(x, transpose=False)
+    assert_same(sc, rsc, "scales")
+    assert_same(q, rq, "values")
+
+
+@pytest.mark.parametrize("shape", [(32, 32), (96, 256), (256, 4096), (4096, 72)])
+def test_mxfp8_quantize_transposed(pmn, shape):
+    rng = np.random.default_rng(8)
+    x = W.normal_bf16_host(rng, shape, 1e-3, 0.01, 50.0)
+    q, sc = pmn.mxfp8_quantize(to_dev_bf16(x), transpose=True)
+    rq, rsc = oracle.mxfp8_quantize(x, transpose=True)
+    assert_same(sc, rsc, "scales")
+    assert_same(q, rq, "values")
+
+
+@pytest.mark.parametrize("stochastic", [True, False])
+@pytest.mark.parametrize("batch,rows,cols,per_row", [(1, 32, 64, True), (1, 256, 256, True), (1, 160, 1536, True),
+                                                     (3, 96, 128, False), (2, 512, 192, False)])
+def test_requant_transpose(pmn, batch, rows, cols, per_row, stochastic):
+    rng = np.random.default_rng(rows + cols)
+    x = W.normal_bf16_host(rng, (batch * rows, cols), 1.0, 0.02, 30.0)
+    x[:32] = 0  # a padding segment
+    if per_row:
+        c, s, g = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW, four_over_six=True)
+    else:
+        c, s, g = oracle.nvfp4_quantize(x, oracle.OUTER_PER_GROUP, group_offsets=np.arange(batch + 1) * rows)
+    seed, tag = 1234567, 2
+    dc, ds, dg = (torch.from_numpy(a).cuda() for a in (c, s, g))
+    q, qs = pmn.requant_transpose_sr_mxfp8(dc, ds, dg, per_row, batch, rows, cols, seed, tag, stochastic)
+    rq, rqs = oracle.requant_transpose_mxfp8(c, s, g, per_row, batch, rows, cols, seed, tag, stochastic)
+    assert_same(qs, rqs, "scales")
+    assert_same(q, rq, "values")
+
+
+def test_requant_gpu_chain_from_gpu_quantize(pmn):
+    """GPU quantise then GPU requant equals the oracle chain on the same input."""
+    d = W.tiny(0)
+    c, s, g = pmn.nvfp4_quantize(to_dev_bf16(d["x"]), outer_mode=pmn.OUTER_PER_GROUP, rows_per_group=256)
+    q, qs = pmn.requant_transpose_sr_mxfp8(c, s, g, False, 1, 256, 256, 0, 1)
+    rc, rs, rg = oracle.nvfp4_quantize(d["x"], oracle.OUTER_PER_GROUP, group_offsets=[0, 256])
+    rq, rqs = oracle.requant_transpose_mxfp8(rc, rs, rg, False, 1, 256, 256, 0, 1)
+    assert_same(qs, rqs, "scales")
+    assert_same(q, rq, "values")
+
+
+@pytest.mark.parametrize("shape", [(1, 32), (64, 256), (300, 4096)])
+def test_rht_s2f6_quantize(pmn, shape):
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal(shape) * 10.0 ** rng.uniform(-3, 2, (shape[0], 1))).astype(np.float32)
+    x[0, :32] = 0
+    for seed in (0, 99):
+        q, sc = pmn.rht_s2f6_quantize(torch.from_numpy(x).cuda(), seed)
+        rq, rsc = oracle.rht_s2f6(x, seed)
+        assert_same(sc, rsc, "scales")
+        assert_same(q, rq, "codes")
+
+
+def test_quantize_deterministic(pmn):
+    rng = np.random.default_rng(12)
+    x = to_dev_bf16(W.normal_bf16_host(rng, (512, 4096)))
+    a = [pmn.nvfp4_quantize(x, four_over_six=True) for _ in range(3)]
+    for t in a[1:]:
+        for u, v in zip(a[0], t):
+            assert torch.equal(u, v)
+
+
+def test_invalid_arguments_rejected(pmn):
+    x = torch.zeros((4, 24), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pmn.PmnError):
+        pmn.nvfp4_quantize(x)  # cols % 16 != 0
+    y = torch.zeros((40, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pmn.PmnError):
+        pmn.mxfp8_quantize(y, transpose=True)  # rows % 32 != 0
+    c = torch.zeros((32, 16), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((32, 2), dtype=torch.uint8, device="cuda")
+    g = torch.ones(32, dtype=torch.float32, device="cuda")
+    with pytest.raises(pmn.PmnError):
+        pmn.requant_transpose_sr_mxfp8(c, s, g, True, 1, 32, 32, 0, 1)  # cols % 64 != 0
