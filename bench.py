@@ -1,0 +1,424 @@
+"""Benchmark of the MoE expert layer's block-scaled numerics path on GB300.
+
+One step = one pass of the whole path over one batch: NVFP4 quantisation of
+the bf16 master weights (per expert) and of the routed activations (per token,
+4/6), the grouped NVFP4 w1 GEMM, SwiGLU + NVFP4 quantisation of h, the grouped
+NVFP4 w2 GEMM with the fused RHT-32 + S2F6 combine quantisation, the
+dequantise -> transpose -> SR -> MXFP8 requantisation of X, H, W1 and W2, the
+MXFP8 quantisation of dY and dY1 (both orientations) and the four grouped
+MXFP8 gradient GEMMs (dX, dW1, dH, dW2).  Workload: 384 experts, top-8 routing
+of 16384 tokens (131072 routed rows), d_model 4096, expert d_ff 1536, seeded
+synthetic data drawn on the device.
+
+value = expert-GEMM FLOPs of the step (forward NVFP4 + backward MXFP8, on the
+real routed rows) / step time.  Per-kernel throughput and roofline fractions
+are reported in `components`; the dominant kernel's in `roofline`.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own replica of the layer (no data
+path collective; weak scaling); rank 0 prints one JSON line.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 expert-GEMM TFLOPS (% FP4 peak); quant/requant GB/s (% HBM peak)"
+WORKLOAD = ("moe_expert_layer_step: 384 experts, top-8 of 16384 tokens (131072 routed rows, expert segments "
+            "padded to 32), d_model 4096, d_ff 1536; NVFP4 fwd + RHT/S2F6 combine + SR-MXFP8 bwd")
+NOMINAL_TC_RATIO = {"fp4": 13.5 / 2.25, "fp8": 4.5 / 2.25}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def traffic_table():
+    """DRAM bytes per launch from committed ncu summaries: lines
+    `<call-name> <bytes-per-launch> <sha256-prefix-of-source>`; an entry counts
+    only while the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    out = {}
+    if not os.path.exists(path):
+        return out
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            name, nbytes, sha = line.split()[:3]
+            out[name] = (float(nbytes), sha)
+    return out
+
+
+def source_sha(name):
+    src = "gemm.cu" if ("gemm" in name) else "quantize.cu"
+    h = hashlib.sha256()
+    for fn in (src, "numerics.cuh", "sm100.cuh"):
+        with open(os.path.join(ROOT, "precision_moe_numerics_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+# ---------------------------------------------------------------------- oracle sample
+def oracle_sample(inputs, experts, seed=0):
+    """Runs the CPU oracle over the step restricted to `experts` (host copies of
+    the same device inputs).  Returns (flops, seconds, threads)."""
+    import numpy as np
+    import oracle
+    import torch
+
+    r = inputs["routing"]
+    D, F = inputs["x"].shape[1], inputs["w2"].shape[2]
+    F2 = 2 * F
+    flops = 0.0
+    host = {}
+    for e in experts:
+        lo, hi = int(r.offsets[e]), int(r.offsets[e + 1])
+        n = hi - lo
+        if n == 0:
+            continue
+        hb = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+        host[e] = (hb(inputs["x"][lo:hi]), hb(inputs["w1"][e]), hb(inputs["w2"][e]), hb(inputs["dy"][lo:hi]),
+                   hb(inputs["dy1"][lo:hi]), int(r.counts[e]))
+    t0 = time.perf_counter()
+    for e, (x, w1, w2, dy, dy1, real) in host.items():
+        n = x.shape[0]
+        w1q = oracle.nvfp4_quantize(w1, oracle.OUTER_PER_GROUP, group_offsets=[0, F2])
+        w2q = oracle.nvfp4_quantize(w2, oracle.OUTER_PER_GROUP, group_offsets=[0, D])
+        xq = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW, four_over_six=True)
+        y = oracle.grouped_gemm_nvfp4(xq[0], xq[1], xq[2], w1q[0][None], w1q[1][None], w1q[2], [0, n])
+        h = oracle.swiglu_bf16(oracle.bf16_rne_array(y), F)
+        hq = oracle.nvfp4_quantize(h, oracle.OUTER_PER_ROW, four_over_six=True)
+        z = oracle.grouped_gemm_nvfp4(hq[0], hq[1], hq[2], w2q[0][None], w2q[1][None], w2q[2], [0, n])
+        oracle.rht_s2f6(z.astype(np.float32), seed)
+        xt = oracle.requant_transpose_mxfp8(xq[0], xq[1], xq[2], True, 1, n, D, seed, oracle.TAG_X)
+        ht = oracle.requant_transpose_mxfp8(hq[0], hq[1], hq[2], True, 1, n, F, seed, oracle.TAG_H)
+        w1t = oracle.requant_transpose_mxfp8(w1q[0], w1q[1], w1q[2], False, 1, F2, D, seed, oracle.TAG_W1)
+        w2t = oracle.requant_transpose_mxfp8(w2q[0], w2q[1], w2q[2], False, 1, D, F, seed, oracle.TAG_W2)
+        dyr, dyt = oracle.mxfp8_quantize(dy), oracle.mxfp8_quantize(dy, transpose=True)
+        dy1r, dy1t = oracle.mxfp8_quantize(dy1), oracle.mxfp8_quantize(dy1, transpose=True)
+        oracle.gemm_mxfp8_mgrouped(dyr[0], dyr[1], w2t[0], w2t[1], [0, n])
+        oracle.gemm_mxfp8_kgrouped(dyt[0], dyt[1], ht[0][0], ht[1][0], [0, n])
+        oracle.gemm_mxfp8_mgrouped(dy1r[0], dy1r[1], w1t[0], w1t[1], [0, n])
+        oracle.gemm_mxfp8_kgrouped(dy1t[0], dy1t[1], xt[0][0], xt[1][0], [0, n])
+        flops += 3 * (2.0 * real * D * F2 + 2.0 * real * F * D)
+    dt = time.perf_counter() - t0
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return flops, dt, threads
+
+
+def pick_sample_experts(r, k):
+    """k experts spread over the index range (deterministic)."""
+    import numpy as np
+    nz = [e for e in range(len(r.counts)) if r.counts[e] > 0]
+    idx = np.linspace(0, len(nz) - 1, k).round().astype(int)
+    return [nz[i] for i in sorted(set(idx.tolist()))]
+
+
+# ---------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_env()
+
+    import torch
+    import torch.distributed as dist
+
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from precision_moe_numerics_gb300 import build, layer, pmn
+    from precision_moe_numerics_gb300 import workloads as W
+    build.build()
+
+    inp = W.moe_device(args.seed + rank, device=dev)
+    r = inp["routing"]
+    offsets = torch.from_numpy(r.offsets.astype("int32")).to(dev)
+    L = layer.ExpertLayerStep(inp["x"], inp["w1"], inp["w2"], inp["dy"], inp["dy1"], offsets, r.real_rows,
+                              seed=args.seed)
+    calls = L.kernel_calls()
+    alg = layer.algorithmic(L.shape)
+    flops_step = sum(v[0] for v in alg.values())
+
+    for _ in range(args.warmup):
+        L.step()
+    torch.cuda.synchronize()
+    if pmn.get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for s in range(args.steps):
+            ev[s][0].record(stream)
+            for i, (_, f) in enumerate(calls):
+                f()
+                ev[s][i + 1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    if pmn.get_device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+    per_call_ms = {name: sum(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)) / args.steps
+                   for i, (name, _) in enumerate(calls)}
+    t = torch.tensor([ms_total], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_step = t.item() / args.steps
+    value = flops_step * world / (ms_step * 1e-3) / 1e12
+
+    # ------------------------------------------------------------ end to end
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(L, inp, args, dev, flops_step, world)
+
+    pk = peaks()
+    comps = {}
+    for name, (fl, by) in alg.items():
+        ms = per_call_ms[name]
+        c = {"ms": round(ms, 4), "GB/s": round(by / (ms * 1e-3) / 1e9, 1),
+             "hbm_frac": round(by / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3)}
+        if fl:
+            kind = "fp4" if "nvfp4" in name else "fp8"
+            tc_peak = pk["bf16_tflops_sustained"] * NOMINAL_TC_RATIO[kind]
+            c["TFLOP/s"] = round(fl / (ms * 1e-3) / 1e12, 1)
+            c["tc_frac"] = round(fl / (ms * 1e-3) / 1e12 / tc_peak, 3)
+        comps[name] = c
+    dom = max(per_call_ms, key=per_call_ms.get)
+    fl, by = alg[dom]
+    tr = traffic_table().get(dom)
+    traffic = tr[0] if tr and tr[1] == source_sha(dom) else None
+    if fl:
+        kind = "fp4" if "nvfp4" in dom else "fp8"
+        tc_peak = pk["bf16_tflops_sustained"] * NOMINAL_TC_RATIO[kind]
+        t_c, t_m = fl / tc_peak / 1e12, by / pk["hbm_gbs"] / 1e9
+    else:
+        t_c, t_m = 0.0, 1.0
+    ms = per_call_ms[dom]
+    if t_c > t_m:
+        roof = {"bound": "tensor", "achieved": round(fl / (ms * 1e-3) / 1e12, 1), "peak": round(tc_peak, 1),
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": round(by / (ms * 1e-3) / 1e9, 1), "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof.update({"frac": round(roof["achieved"] / roof["peak"], 3), "traffic": traffic, "kernel": dom,
+                 "algorithmic_bytes": by, "flops": fl, "ms": round(ms, 4), "peak_source": pk["source"],
+                 "share_of_step": round(ms / ms_step, 3)})
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, args)
+
+    clocks = clk.summary()
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4+mxfp8",
+                "data": "synthetic", "config": {
+                    "workload": WORKLOAD, "routed_rows": r.real_rows, "padded_rows": r.rows,
+                    "experts": L.shape.experts, "d_model": L.shape.d_model, "d_ff": L.shape.d_ff,
+                    "flops_per_step": flops_step, "l2": "inputs larger than L2 (no flush needed)",
+                    "parallelism": "replicas" if world > 1 else "single-gpu"},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": layer.launches_per_step() * args.steps, "clocks": clocks,
+                "components": comps}
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(L, inp, args, dev, flops_step, world):
+    """Same step through the binding with host buffers: every step copies the
+    batch inputs (routed X, dY, dY1) from pinned host memory and reads back the
+    forward result (S2F6 combine payload + scales) and dX."""
+    import torch
+    pins = {k: torch.empty_like(inp[k], device="cpu").pin_memory() for k in ("x", "dy", "dy1")}
+    for k in pins:
+        pins[k].copy_(inp[k])
+    outs = [torch.empty_like(L.z[0], device="cpu").pin_memory(), torch.empty_like(L.z[1], device="cpu").pin_memory(),
+            torch.empty_like(L.dx, device="cpu").pin_memory()]
+    stream = torch.cuda.current_stream()
+    bi = sum(p.numel() * p.element_size() for p in pins.values())
+    bo = sum(o.numel() * o.element_size() for o in outs)
+
+    def one():
+        L.x.copy_(pins["x"], non_blocking=True)
+        L.dy.copy_(pins["dy"], non_blocking=True)
+        L.dy1.copy_(pins["dy1"], non_blocking=True)
+        L.step()
+        outs[0].copy_(L.z[0], non_blocking=True)
+        outs[1].copy_(L.z[1], non_blocking=True)
+        outs[2].copy_(L.dx, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = t.item()
+    return {"value": round(flops_step * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+def cpu_baseline(inp, args, budget_s=12.0):
+    r = inp["routing"]
+    k = 1
+    flops, dt, threads = oracle_sample(inp, pick_sample_experts(r, 1), args.seed)
+    # grow the sample to about `budget_s` of CPU work
+    per = dt
+    k = max(1, min(48, int(budget_s / max(per, 1e-3))))
+    experts = pick_sample_experts(r, k)
+    flops, dt, threads = oracle_sample(inp, experts, args.seed)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "the full step (quantise, GEMMs in binary64, SwiGLU, RHT+S2F6, SR requant, dY quant, "
+                      "gradient GEMMs) for %d of 384 experts (%d routed rows), %.1f s" % (
+                          len(experts), int(sum(r.counts[e] for e in experts)), dt)}
+
+
+def run_reference(args):
+    """The oracle timed as the reference arm: each step is the oracle's pass
+    over a bounded sample of experts of the same workload (host inputs drawn
+    with the same seeded generator on the host)."""
+    import numpy as np
+    import torch
+    from precision_moe_numerics_gb300 import workloads as W
+    r = W.moe_routing(args.seed)
+    k = 2
+    experts = pick_sample_experts(r, k)
+    rng_dev = "cpu"
+    gen = torch.Generator(device=rng_dev)
+    gen.manual_seed(args.seed + 100)
+    D, F = W.D_MODEL, W.D_FF
+    inputs = {"routing": r}
+    rows = r.rows
+    x = torch.zeros((rows, D), dtype=torch.bfloat16)
+    dy = torch.zeros((rows, D), dtype=torch.bfloat16)
+    dy1 = torch.zeros((rows, 2 * F), dtype=torch.bfloat16)
+    w1 = torch.zeros((r.counts.size, 2 * F, D), dtype=torch.bfloat16)
+    w2 = torch.zeros((r.counts.size, D, F), dtype=torch.bfloat16)
+    for e in experts:
+        lo, hi = int(r.offsets[e]), int(r.offsets[e + 1])
+        real = int(r.counts[e])
+        x[lo:lo + real] = W.normal_bf16_device(gen, (real, D), 1.0, 0.001, 30.0, device=rng_dev)
+        dy[lo:lo + real] = W.normal_bf16_device(gen, (real, D), 1e-3, device=rng_dev)
+        dy1[lo:lo + real] = W.normal_bf16_device(gen, (real, 2 * F), 1e-3, device=rng_dev)
+        w1[e] = W.normal_bf16_device(gen, (2 * F, D), 0.02, device=rng_dev)
+        w2[e] = W.normal_bf16_device(gen, (D, F), 0.02, device=rng_dev)
+    inputs.update({"x": x, "dy": dy, "dy1": dy1, "w1": w1, "w2": w2})
+    for _ in range(args.warmup):
+        oracle_sample(inputs, experts, args.seed)
+    tot_f, tot_t, threads = 0.0, 0.0, 1
+    for _ in range(args.steps):
+        f, t, threads = oracle_sample(inputs, experts, args.seed)
+        tot_f += f
+        tot_t += t
+    value = tot_f / tot_t / 1e12
+    sample = "the full step for %d of 384 experts (%d routed rows) per step" % (
+        len(experts), int(sum(r.counts[e] for e in experts)))
+    line = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 GEMMs, f32 quantisers",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "sample_experts": experts},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

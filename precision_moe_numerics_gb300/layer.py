@@ -1,0 +1,178 @@
+"""One pass of the MoE expert layer's block-scaled numerics path on one GPU.
+
+Forward (page "Thinking Machines ... Inkling 2 Small", sections [Layers],
+[Cost], [NVLink]):
+  W1, W2 (bf16 master weights)  -> NVFP4, outer scale per expert
+  X (routed rows, bf16)         -> NVFP4, outer scale per token, 4/6
+  Y  = X . W1^T                 grouped NVFP4 GEMM -> bf16
+  H  = silu(Y_gate) * Y_up      -> NVFP4, per token, 4/6 (one kernel)
+  Z  = H . W2^T                 grouped NVFP4 GEMM with the RHT-32 + S2F6
+                                combine quantisation in its epilogue
+Backward (section [SR]):
+  saved X, H, W1, W2 (NVFP4)    -> dequantise, transpose, SR -> MXFP8
+  dY, dY1 (bf16)                -> MXFP8 (RN), rowwise and transposed
+  dH  = dY  . W2                M-grouped MXFP8 GEMM -> bf16
+  dW2 = dY^T . H  per expert    K-grouped MXFP8 GEMM -> fp32
+  dX  = dY1 . W1                M-grouped MXFP8 GEMM -> bf16
+  dW1 = dY1^T . X per expert    K-grouped MXFP8 GEMM -> fp32
+
+All buffers are allocated once (torch, device memory); step() only enqueues
+the library's kernels on the current stream.
+"""
+from dataclasses import dataclass
+
+import torch
+
+from . import pmn
+
+ALIGN_ROWS = 512  # routed-row buffers are padded so MXFP8 scale rows are 16-byte pitched
+
+
+@dataclass
+class LayerShape:
+    experts: int
+    d_model: int
+    d_ff: int
+    rows: int        # allocated routed rows (multiple of ALIGN_ROWS)
+    real_rows: int   # routed (token, expert) pairs
+
+
+def flops_forward(s: LayerShape):
+    return 2.0 * s.real_rows * s.d_model * (2 * s.d_ff) + 2.0 * s.real_rows * s.d_ff * s.d_model
+
+
+def flops_backward(s: LayerShape):
+    # dX, dW1 (w1 layer) and dH, dW2 (w2 layer): two GEMMs of each forward shape
+    return 2.0 * flops_forward(s)
+
+
+class ExpertLayerStep:
+    def __init__(self, x, w1, w2, dy, dy1, offsets, real_rows, seed=0, device="cuda"):
+        E, F2, D = w1.shape
+        F = F2 // 2
+        T = x.shape[0]
+        assert T % ALIGN_ROWS == 0 and w2.shape == (E, D, F)
+        self.shape = LayerShape(E, D, F, T, real_rows)
+        self.x, self.w1, self.w2, self.dy, self.dy1 = x, w1, w2, dy, dy1
+        self.offsets = offsets
+        self.seed = seed
+        u8, f32, bf16 = torch.uint8, torch.float32, torch.bfloat16
+
+        def e(*shape, dtype=u8):
+            return torch.empty(shape, dtype=dtype, device=device)
+
+        # forward operands
+        self.w1q = (e(E * F2, D // 2), e(E * F2, D // 16), e(E, dtype=f32))
+        self.w2q = (e(E * D, F // 2), e(E * D, F // 16), e(E, dtype=f32))
+        self.xq = (e(T, D // 2), e(T, D // 16), e(T, dtype=f32))
+        self.y = e(T, F2, dtype=bf16)
+        self.hq = (e(T, F // 2), e(T, F // 16), e(T, dtype=f32))
+        self.z = (e(T, D, dtype=torch.int8), e(T, D // 32))
+        # backward operands
+        self.xt = (e(1, D, T), e(1, D, T // 32))
+        self.ht = (e(1, F, T), e(1, F, T // 32))
+        self.w1t = (e(E, D, F2), e(E, D, F2 // 32))
+        self.w2t = (e(E, F, D), e(E, F, D // 32))
+        self.dy_r = (e(T, D), e(T, D // 32))
+        self.dy_t = (e(D, T), e(D, T // 32))
+        self.dy1_r = (e(T, F2), e(T, F2 // 32))
+        self.dy1_t = (e(F2, T), e(F2, T // 32))
+        self.dh = e(T, F, dtype=bf16)
+        self.dx = e(T, D, dtype=bf16)
+        self.dw1 = e(E, F2, D, dtype=f32)
+        self.dw2 = e(E, D, F, dtype=f32)
+
+    def w1q3(self):
+        E, F2, D = self.w1.shape
+        c, s, g = self.w1q
+        return c.view(E, F2, D // 2), s.view(E, F2, D // 16), g
+
+    def w2q3(self):
+        E, D, F = self.w2.shape
+        c, s, g = self.w2q
+        return c.view(E, D, F // 2), s.view(E, D, F // 16), g
+
+    def kernel_calls(self):
+        """(name, callable) pairs in step order; each call enqueues library kernels."""
+        s = self.shape
+        E, D, F, T = s.experts, s.d_model, s.d_ff, s.rows
+        F2 = 2 * F
+        P = pmn
+        return [
+            ("quant_w1", lambda: P.nvfp4_quantize(self.w1.view(E * F2, D), outer_mode=P.OUTER_PER_GROUP,
+                                                  rows_per_group=F2, out=self.w1q)),
+            ("quant_w2", lambda: P.nvfp4_quantize(self.w2.view(E * D, F), outer_mode=P.OUTER_PER_GROUP,
+                                                  rows_per_group=D, out=self.w2q)),
+            ("quant_x", lambda: P.nvfp4_quantize(self.x, four_over_six=True, out=self.xq)),
+            ("gemm1_nvfp4", lambda: P.grouped_gemm_nvfp4(self.xq, self.w1q3(), self.offsets, out=self.y)),
+            ("swiglu_quant_h", lambda: P.nvfp4_quantize(self.y, cols=F, swiglu=True, four_over_six=True,
+                                                        out=self.hq)),
+            ("gemm2_nvfp4_rht_s2f6", lambda: P.w2_gemm_rht_s2f6(self.hq, self.w2q3(), self.offsets, self.seed,
+                                                                out=self.z)),
+            ("requant_x", lambda: P.requant_transpose_sr_mxfp8(*self.xq, True, 1, T, D, self.seed, P.TAG_X,
+                                                               out=self.xt)),
+            ("requant_h", lambda: P.requant_transpose_sr_mxfp8(*self.hq, True, 1, T, F, self.seed, P.TAG_H,
+                                                               out=self.ht)),
+            ("requant_w1", lambda: P.requant_transpose_sr_mxfp8(*self.w1q, False, E, F2, D, self.seed, P.TAG_W1,
+                                                                out=self.w1t)),
+            ("requant_w2", lambda: P.requant_transpose_sr_mxfp8(*self.w2q, False, E, D, F, self.seed, P.TAG_W2,
+                                                                out=self.w2t)),
+            ("quant_dy_rows", lambda: P.mxfp8_quantize(self.dy, False, out=self.dy_r)),
+            ("quant_dy_cols", lambda: P.mxfp8_quantize(self.dy, True, out=self.dy_t)),
+            ("quant_dy1_rows", lambda: P.mxfp8_quantize(self.dy1, False, out=self.dy1_r)),
+            ("quant_dy1_cols", lambda: P.mxfp8_quantize(self.dy1, True, out=self.dy1_t)),
+            ("gemm_dh_mxfp8", lambda: P.gemm_mxfp8(self.dy_r[0], self.dy_r[1], self.w2t[0], self.w2t[1],
+                                                   self.offsets, P.GROUP_M, torch.bfloat16, out=self.dh)),
+            ("gemm_dw2_mxfp8", lambda: P.gemm_mxfp8(self.dy_t[0], self.dy_t[1], self.ht[0][0], self.ht[1][0],
+                                                    self.offsets, P.GROUP_K, torch.float32, out=self.dw2)),
+            ("gemm_dx_mxfp8", lambda: P.gemm_mxfp8(self.dy1_r[0], self.dy1_r[1], self.w1t[0], self.w1t[1],
+                                                   self.offsets, P.GROUP_M, torch.bfloat16, out=self.dx)),
+            ("gemm_dw1_mxfp8", lambda: P.gemm_mxfp8(self.dy1_t[0], self.dy1_t[1], self.xt[0][0], self.xt[1][0],
+                                                    self.offsets, P.GROUP_K, torch.float32, out=self.dw1)),
+        ]
+
+    def step(self):
+        for _, f in self.kernel_calls():
+            f()
+
+
+# launches of library kernels per call name (for the launch count)
+LAUNCHES = {"quant_w1": 3, "quant_w2": 3}
+
+
+def launches_per_step():
+    names = ["quant_w1", "quant_w2", "quant_x", "gemm1_nvfp4", "swiglu_quant_h", "gemm2_nvfp4_rht_s2f6",
+             "requant_x", "requant_h", "requant_w1", "requant_w2", "quant_dy_rows", "quant_dy_cols",
+             "quant_dy1_rows", "quant_dy1_cols", "gemm_dh_mxfp8", "gemm_dw2_mxfp8", "gemm_dx_mxfp8",
+             "gemm_dw1_mxfp8"]
+    return sum(LAUNCHES.get(n, 1) for n in names)
+
+
+def algorithmic(shape: LayerShape):
+    """Per call: (flops, algorithmic HBM bytes) on real rows (padding excluded)."""
+    E, D, F, R = shape.experts, shape.d_model, shape.d_ff, shape.real_rows
+    F2 = 2 * F
+    nv = 0.5 + 1 / 16      # NVFP4 bytes per element (codes + E4M3 scales)
+    mx = 1 + 1 / 32        # MXFP8 / S2F6 bytes per element (values + E8M0 scales)
+    w1n, w2n = E * F2 * D, E * D * F
+    out = {
+        "quant_w1": (0, w1n * (2 + nv)),
+        "quant_w2": (0, w2n * (2 + nv)),
+        "quant_x": (0, R * D * (2 + nv)),
+        "gemm1_nvfp4": (2.0 * R * F2 * D, (R * D + w1n) * nv + R * F2 * 2),
+        "swiglu_quant_h": (0, R * F2 * 2 + R * F * nv),
+        "gemm2_nvfp4_rht_s2f6": (2.0 * R * D * F, (R * F + w2n) * nv + R * D * mx),
+        "requant_x": (0, R * D * (nv + mx)),
+        "requant_h": (0, R * F * (nv + mx)),
+        "requant_w1": (0, w1n * (nv + mx)),
+        "requant_w2": (0, w2n * (nv + mx)),
+        "quant_dy_rows": (0, R * D * (2 + mx)),
+        "quant_dy_cols": (0, R * D * (2 + mx)),
+        "quant_dy1_rows": (0, R * F2 * (2 + mx)),
+        "quant_dy1_cols": (0, R * F2 * (2 + mx)),
+        "gemm_dh_mxfp8": (2.0 * R * D * F, (R * D + w2n) * mx + R * F * 2),
+        "gemm_dw2_mxfp8": (2.0 * R * D * F, (R * D + R * F) * mx + w2n * 4),
+        "gemm_dx_mxfp8": (2.0 * R * F2 * D, (R * F2 + w1n) * mx + R * D * 2),
+        "gemm_dw1_mxfp8": (2.0 * R * F2 * D, (R * F2 + R * D) * mx + w1n * 4),
+    }
+    return out

@@ -157,14 +157,18 @@ def small_moe(seed=0, tokens=256, experts=8, k=2, d=256, f=128, pad=PAD):
 
 # ------------------------------------------------------------------ device cases
 def moe_device(seed=0, device="cuda", with_backward=True, experts=N_EXPERTS, tokens=MOE_TOKENS,
-               d=D_MODEL, f=D_FF):
-    """Full-size MoE layer inputs drawn on the device (bf16 tensors)."""
+               d=D_MODEL, f=D_FF, align_rows=512):
+    """Full-size MoE layer inputs drawn on the device (bf16 tensors).  Row
+    buffers hold `rows_alloc` rows (the routed rows rounded up to
+    `align_rows`); rows past the last expert segment are zero."""
     r = moe_routing(seed, tokens, experts)
+    rows_alloc = ((r.rows + align_rows - 1) // align_rows) * align_rows
     gen = torch.Generator(device=device)
     gen.manual_seed(seed + 100)
     xt = normal_bf16_device(gen, (tokens, d), 1.0, 0.001, 30.0, device)
-    rt = torch.from_numpy(r.row_token).to(device)
-    x = torch.zeros((r.rows, d), dtype=torch.bfloat16, device=device)
+    rt = torch.full((rows_alloc,), -1, dtype=torch.int64, device=device)
+    rt[:r.rows] = torch.from_numpy(r.row_token).to(device)
+    x = torch.zeros((rows_alloc, d), dtype=torch.bfloat16, device=device)
     m = rt >= 0
     x[m] = xt[rt[m]]
     del xt
@@ -173,11 +177,11 @@ def moe_device(seed=0, device="cuda", with_backward=True, experts=N_EXPERTS, tok
     for e in range(experts):
         normal_bf16_device(gen, (2 * f, d), 0.02, device=device, out=w1[e])
         normal_bf16_device(gen, (d, f), 0.02, device=device, out=w2[e])
-    out = {"routing": r, "x": x, "w1": w1, "w2": w2}
+    out = {"routing": r, "x": x, "w1": w1, "w2": w2, "rows_alloc": rows_alloc}
     if with_backward:
-        dy = normal_bf16_device(gen, (r.rows, d), 1e-3, device=device)
+        dy = normal_bf16_device(gen, (rows_alloc, d), 1e-3, device=device)
         dy[~m] = 0
-        dy1 = normal_bf16_device(gen, (r.rows, 2 * f), 1e-3, device=device)
+        dy1 = normal_bf16_device(gen, (rows_alloc, 2 * f), 1e-3, device=device)
         dy1[~m] = 0
         out["dy"] = dy
         out["dy1"] = dy1
