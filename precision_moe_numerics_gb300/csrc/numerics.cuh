@@ -78,59 +78,30 @@ __device__ __forceinline__ int mx_exponent_s2f6(float a)
     return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
-// ---------------------------------------------------------------- E4M3 from d * 2^-e
-// Rounds y = d * 2^-e (|y| <= 448 by the exponent rule) onto the E4M3 grid by
-// integer arithmetic on the binary32 bits of d, so no intermediate is rounded:
-//   |d| = M * 2^ex,  L = floor(log2 |y|),  grid step 2^u with u = max(L,-6)-3,
-//   |y| / 2^u = n + F / 2^D  (n integer part, F the D discarded bits).
-// stochastic: away from zero iff rb16 < (F / 2^D) * 2^16;
-// otherwise    round to nearest, ties to even n.
-// The sign of d is kept (negative values that round to zero give 0x80).
-__device__ __forceinline__ uint32_t e4m3_round_scaled(float d, int e, uint32_t rb16, bool stochastic)
+// ---------------------------------------------------------------- E4M3 from y = d * 2^-e
+// 2^-e as binary32 for the MX exponents that finite inputs produce (e <= 120).
+__device__ __forceinline__ float exp2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
+
+// Two binary32 values -> two E4M3 bytes (lo in byte 0), nearest even, saturating.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_rn(float lo, float hi)
 {
-    uint32_t bits = __float_as_uint(d);
-    uint32_t sign = (bits >> 24) & 0x80u;
-    uint32_t a = bits & 0x7FFFFFFFu;
-    if (a == 0u) return sign;
-    uint32_t E = a >> 23;
-    uint32_t M = (E == 0u) ? a : ((a & 0x7FFFFFu) | 0x800000u);
-    int ex = (E == 0u) ? -149 : (int)E - 150;
-    int L = (31 - __clz(M)) + ex - e;
-    int u = (L < -6 ? -6 : L) - 3;
-    int s = ex - e - u;
-    uint32_t n;
-    bool up;
-    if (s >= 0) {
-        n = M << s;  // exact: |y| / 2^u < 2^18
-        up = false;
-    } else {
-        int D = -s;
-        uint64_t F;
-        if (D >= 32) {
-            n = 0u;
-            F = M;  // all bits fractional
-        } else {
-            n = M >> D;
-            F = M & ((1u << D) - 1u);
-        }
-        if (stochastic) {
-            if (D <= 16) up = rb16 < (uint32_t)(F << (16 - D));
-            else if (D - 16 >= 40) up = (rb16 == 0u) && (F != 0u);
-            else up = ((uint64_t)rb16 << (D - 16)) < F;
-        } else {
-            if (D >= 40) up = false;  // F < 2^24 < half
-            else {
-                uint64_t half = 1ull << (D - 1);
-                up = (F > half) || (F == half && (n & 1u));
-            }
-        }
-    }
-    uint32_t q = n + (up ? 1u : 0u);
-    uint32_t code;
-    if (q < 8u) code = q;                                        // subnormal (u == -9)
-    else if (q < 16u) code = ((uint32_t)(u + 10) << 3) | (q - 8u);
-    else code = (uint32_t)(u + 11) << 3;                         // carried into next binade
-    return sign | code;
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(r) : "f"(lo), "f"(hi));
+    return (uint32_t)r;
+}
+
+// Four binary32 values -> four E4M3 bytes (element k in byte k) by the
+// hardware's stochastic rounding: each element adds a 16-bit random value to
+// the leading 16 bits of its discarded fraction and rounds away from zero on
+// carry.  Elements 0 / 1 take rbits[15:0] / the same bits reversed, elements
+// 2 / 3 take rbits[31:16] / reversed.  The sign is kept.
+__device__ __forceinline__ uint32_t cvt_e4m3x4_rs(float e0, float e1, float e2, float e3, uint32_t rbits)
+{
+    uint32_t r;
+    asm("cvt.rs.satfinite.e4m3x4.f32 %0, {%1, %2, %3, %4}, %5;"
+        : "=r"(r)
+        : "f"(e3), "f"(e2), "f"(e1), "f"(e0), "r"(rbits));
+    return r;
 }
 
 // ---------------------------------------------------------------- Philox4x32-10
@@ -142,33 +113,22 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-        uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0);
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
     }
     return c;
 }
 
-// 16 random bits for elements 8j .. 8j+7 of a tensor (tag selects the
-// tensor): counter (j lo, j hi, tag, 0), key (seed lo, seed hi); element
-// 8j + t takes word t/2, low half for even t.
-struct SrBits8 {
-    uint4 w;
-    __device__ __forceinline__ uint32_t get(int t) const
-    {
-        uint32_t word = (t >> 1) == 0 ? w.x : (t >> 1) == 1 ? w.y : (t >> 1) == 2 ? w.z : w.w;
-        return (t & 1) ? (word >> 16) : (word & 0xFFFFu);
-    }
-};
-
-__device__ __forceinline__ SrBits8 sr_bits8(uint64_t seed, uint32_t tag, uint64_t j)
+// The 4 random words for output elements 16j .. 16j+15 of a tensor (tag
+// selects the tensor): counter (j lo, j hi, tag, 0), key (seed lo, seed hi);
+// word k serves elements 16j + 4k .. 16j + 4k + 3.
+__device__ __forceinline__ uint4 sr_words16(uint64_t seed, uint32_t tag, uint64_t j)
 {
-    SrBits8 b;
-    b.w = philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), tag, 0u), (uint32_t)seed,
-                        (uint32_t)(seed >> 32));
-    return b;
+    return philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), tag, 0u), (uint32_t)seed,
+                         (uint32_t)(seed >> 32));
 }
 
 // ---------------------------------------------------------------- RHT + S2F6

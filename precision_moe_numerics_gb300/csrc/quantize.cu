@@ -246,15 +246,14 @@ __global__ void __launch_bounds__(256) mxfp8_quant_rowwise_kernel(const uint16_t
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
-    int e = mx_exponent_448(amax);
+    const int e = mx_exponent_448(amax);
+    const float sc = exp2_neg(e);  // y = x * 2^-e is exact
     uint32_t o[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        uint32_t b0 = e4m3_round_scaled(bf16_lo(w[2 * i]), e, 0u, false);
-        uint32_t b1 = e4m3_round_scaled(bf16_hi(w[2 * i]), e, 0u, false);
-        uint32_t b2 = e4m3_round_scaled(bf16_lo(w[2 * i + 1]), e, 0u, false);
-        uint32_t b3 = e4m3_round_scaled(bf16_hi(w[2 * i + 1]), e, 0u, false);
-        o[i] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        const uint32_t lo = cvt_e4m3x2_rn(__fmul_rn(bf16_lo(w[2 * i]), sc), __fmul_rn(bf16_hi(w[2 * i]), sc));
+        const uint32_t hi = cvt_e4m3x2_rn(__fmul_rn(bf16_lo(w[2 * i + 1]), sc), __fmul_rn(bf16_hi(w[2 * i + 1]), sc));
+        o[i] = lo | (hi << 16);
     }
     uint4 *po = reinterpret_cast<uint4 *>(out + t * 32);
     po[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -296,14 +295,14 @@ __global__ void __launch_bounds__(256) mxfp8_quant_transposed_kernel(const uint1
         v[j] = __uint_as_float((uint32_t)tile[(rb * 32 + j) * PITCH + c] << 16);
         amax = fmaxf(amax, fabsf(v[j]));
     }
-    int e = mx_exponent_448(amax);
+    const int e = mx_exponent_448(amax);
+    const float sc = exp2_neg(e);
     uint32_t o[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        uint32_t p = 0u;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) p |= e4m3_round_scaled(v[4 * i + t], e, 0u, false) << (8 * t);
-        o[i] = p;
+        const uint32_t lo = cvt_e4m3x2_rn(__fmul_rn(v[4 * i], sc), __fmul_rn(v[4 * i + 1], sc));
+        const uint32_t hi = cvt_e4m3x2_rn(__fmul_rn(v[4 * i + 2], sc), __fmul_rn(v[4 * i + 3], sc));
+        o[i] = lo | (hi << 16);
     }
     uint4 *po = reinterpret_cast<uint4 *>(out + (c0 + c) * rows + r0 + rb * 32);
     po[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -314,11 +313,13 @@ __global__ void __launch_bounds__(256) mxfp8_quant_transposed_kernel(const uint1
 // ------------------------------------------------------------------ requant [SR]
 // Tile of 128 input rows x 128 input cols.  Phase 1: dequantise
 // d = (dec(code) * dec(S)) * g in binary32 into shared memory, stored
-// transposed (row c of the output holds the 128 values d[r, c]).  Phase 2:
-// thread (c, rb) forms the 32-block of output row c, its E8M0 exponent and
-// the rounded E4M3 bytes, with 16 Philox bits per element.
+// transposed (row c of the tile holds d[r, c] for its 128 rows r).  Phase 2:
+// thread (c, rb) forms the 32-block of output row c, its E8M0 exponent e,
+// y = d * 2^-e (exact) and the E4M3 bytes: stochastic rounding by the
+// hardware convert fed with Philox words (one Philox call per 16 elements),
+// or round-to-nearest-even.
 constexpr int RQ_T = 128;
-constexpr int RQ_PITCH = RQ_T + 1;
+constexpr int RQ_PITCH = RQ_T + 4;  // rows stay 16-byte aligned; column writes and 128-bit row reads are conflict-free
 
 __global__ void __launch_bounds__(256) requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, const float *__restrict__ outer,
@@ -345,45 +346,53 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
             sw = __ldg(reinterpret_cast<const uint32_t *>(scales + src * cols16 + (c0 + h * 64) / 16));
         }
         const uint32_t cw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        float *dst = dT + (h * 64) * RQ_PITCH + r;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-            uint32_t code = (cw[j >> 3] >> (4 * (j & 7))) & 15u;
-            float dS = e4m3_to_f32((sw >> (8 * (j >> 4))) & 0xFFu);
-            float d = __fmul_rn(__fmul_rn(e2m1_to_f32(code), dS), g);
-            dT[(h * 64 + j) * RQ_PITCH + r] = ok ? d : 0.0f;
+        for (int blk = 0; blk < 4; ++blk) {
+            const float dS = e4m3_to_f32((sw >> (8 * blk)) & 0xFFu);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int jj = blk * 16 + j;
+                const uint32_t code = (cw[jj >> 3] >> (4 * (jj & 7))) & 15u;
+                dst[jj * RQ_PITCH] = __fmul_rn(__fmul_rn(e2m1_to_f32(code), dS), g);
+            }
         }
     }
     __syncthreads();
     // phase 2: 128 output rows x 4 row-blocks = 512 tasks, 2 per thread
+#pragma unroll 1
     for (int task = threadIdx.x; task < RQ_T * 4; task += blockDim.x) {
         const int c = task & 127, rb = task >> 7;
         const int64_t oc = c0 + c, orow0 = r0 + rb * 32;
         if (oc >= cols || orow0 >= rows) continue;
         float v[32];
+        const float4 *src = reinterpret_cast<const float4 *>(dT + c * RQ_PITCH + rb * 32);
         float amax = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            v[j] = dT[c * RQ_PITCH + rb * 32 + j];
-            amax = fmaxf(amax, fabsf(v[j]));
+        for (int k = 0; k < 8; ++k) {
+            const float4 f = src[k];
+            v[4 * k] = f.x;
+            v[4 * k + 1] = f.y;
+            v[4 * k + 2] = f.z;
+            v[4 * k + 3] = f.w;
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
         }
         const int e = mx_exponent_448(amax);
-        const int64_t i0 = (b * cols + oc) * rows + orow0;  // output index, multiple of 32
+        const float sc = exp2_neg(e);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(v[j], sc);  // exact scaling
+        const int64_t i0 = (b * cols + oc) * rows + orow0;      // output index, multiple of 32
         uint32_t o[8];
+        if (stochastic) {
+            const uint4 wa = sr_words16(seed, tag, (uint64_t)i0 >> 4);
+            const uint4 wb = sr_words16(seed, tag, ((uint64_t)i0 >> 4) + 1);
+            const uint32_t wd[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            SrBits8 rb8;
-            if (stochastic) rb8 = sr_bits8(seed, tag, (uint64_t)(i0 >> 3) + k);
+            for (int k = 0; k < 8; ++k) o[k] = cvt_e4m3x4_rs(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], wd[k]);
+        } else {
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                uint32_t p = 0u;
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int jj = 8 * k + 4 * h2 + t;
-                    const uint32_t bits = stochastic ? rb8.get(4 * h2 + t) : 0u;
-                    p |= e4m3_round_scaled(v[jj], e, bits, stochastic != 0) << (8 * t);
-                }
-                o[2 * k + h2] = p;
-            }
+            for (int k = 0; k < 8; ++k)
+                o[k] = cvt_e4m3x2_rn(v[4 * k], v[4 * k + 1]) | (cvt_e4m3x2_rn(v[4 * k + 2], v[4 * k + 3]) << 16);
         }
         uint4 *po = reinterpret_cast<uint4 *>(out + i0);
         po[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -504,14 +513,10 @@ extern "C" pmn_status pmn_requant_transpose_sr_mxfp8(const uint8_t *codes, const
     if (!aligned16(codes) || !aligned16(scales) || !aligned16(out) || ((uintptr_t)outer & 3u)) return PMN_ERR_INVALID_ARG;
     if (batch == 0 || rows == 0 || cols == 0) return PMN_OK;
     if ((cols / 16) % 4 != 0) return PMN_ERR_INVALID_ARG;  // 4-byte scale words per 64 columns
-    static bool attr_done = false;
     const int smem = RQ_T * RQ_PITCH * (int)sizeof(float);
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(requant_transpose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
-            return PMN_ERR_CUDA;
-        attr_done = true;
-    }
+    if (cudaFuncSetAttribute(requant_transpose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return PMN_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     dim3 grid((unsigned)((cols + RQ_T - 1) / RQ_T), (unsigned)((rows + RQ_T - 1) / RQ_T), (unsigned)batch);
     requant_transpose_kernel<<<grid, 256, smem, s>>>(codes, scales, outer, outer_mode == PMN_OUTER_PER_ROW, rows,
