@@ -189,6 +189,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=None, help="smaller layer for profiling (default 384)")
+    ap.add_argument("--tokens", type=int, default=None, help="tokens routed (default 16384)")
+    ap.add_argument("--only", default=None, help="time only this call of the step (profiling)")
     args = ap.parse_args()
     rank, world, local = dist_env()
 
@@ -209,17 +212,30 @@ def main():
     from precision_moe_numerics_gb300 import workloads as W
     build.build()
 
-    inp = W.moe_device(args.seed + rank, device=dev)
+    kw = {}
+    if args.experts:
+        kw["experts"] = args.experts
+    if args.tokens:
+        kw["tokens"] = args.tokens
+    inp = W.moe_device(args.seed + rank, device=dev, **kw)
     r = inp["routing"]
     offsets = torch.from_numpy(r.offsets.astype("int32")).to(dev)
     L = layer.ExpertLayerStep(inp["x"], inp["w1"], inp["w2"], inp["dy"], inp["dy1"], offsets, r.real_rows,
                               seed=args.seed)
     calls = L.kernel_calls()
     alg = layer.algorithmic(L.shape)
+    if args.only:
+        for name, f in calls:  # the step once, so every operand of the chosen call exists
+            f()
+        calls = [(n, f) for n, f in calls if n == args.only]
+        if not calls:
+            raise SystemExit("unknown call " + args.only)
+        alg = {args.only: alg[args.only]}
     flops_step = sum(v[0] for v in alg.values())
 
     for _ in range(args.warmup):
-        L.step()
+        for _, f in calls:
+            f()
     torch.cuda.synchronize()
     if pmn.get_device_error() != 0:
         raise RuntimeError("device error during warm-up")
@@ -255,7 +271,7 @@ def main():
 
     # ------------------------------------------------------------ end to end
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.only:
         e2e = run_e2e(L, inp, args, dev, flops_step, world)
 
     pk = peaks()
@@ -291,7 +307,7 @@ def main():
                  "share_of_step": round(ms / ms_step, 3)})
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.only:
         cpu = cpu_baseline(inp, args)
 
     clocks = clk.summary()
@@ -305,7 +321,8 @@ def main():
                     "flops_per_step": flops_step, "l2": "inputs larger than L2 (no flush needed)",
                     "parallelism": "replicas" if world > 1 else "single-gpu"},
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": layer.launches_per_step() * args.steps, "clocks": clocks,
+                "gpu_launches": (layer.launches_per_step() if not args.only else
+                                 layer.LAUNCHES.get(args.only, 1)) * args.steps, "clocks": clocks,
                 "components": comps}
         print(json.dumps(line))
     if world > 1:

@@ -161,7 +161,7 @@ def moe_device(seed=0, device="cuda", with_backward=True, experts=N_EXPERTS, tok
     """Full-size MoE layer inputs drawn on the device (bf16 tensors).  Row
     buffers hold `rows_alloc` rows (the routed rows rounded up to
     `align_rows`); rows past the last expert segment are zero."""
-    r = moe_routing(seed, tokens, experts)
+    r = moe_routing(seed, tokens, experts, k=min(TOP_K, experts))
     rows_alloc = ((r.rows + align_rows - 1) // align_rows) * align_rows
     gen = torch.Generator(device=device)
     gen.manual_seed(seed + 100)
