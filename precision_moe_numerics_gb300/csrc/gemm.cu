@@ -8,12 +8,13 @@
 //
 // One persistent kernel per call, one CTA per SM, 8 warps:
 //   warp 0      TMA producer: code tiles (128 rows x 128 bytes, 128-byte
-//               swizzle) and raw scale tiles into a 5-stage ring
+//               swizzle) and raw scale tiles into a 4-stage ring
 //   warp 1      re-lays the stage's scale factors into the 32x128-bit form
 //               tcgen05.cp expects, copies them to TMEM and issues the MMAs
 //               (one elected lane), committing to the stage's empty barrier
 //   warps 4..7  epilogue: TMEM -> registers (one row per thread), outer
-//               scales, bf16/fp32 stores or RHT + S2F6
+//               scales, bf16/fp32 or RHT + S2F6, staged in shared memory and
+//               written by TMA tensor stores in full 128-byte lines
 // Tiles are 128 x 128 with two TMEM accumulators, so the epilogue of one
 // tile overlaps the main loop of the next.  Every wait is bounded: on timeout
 // a device error bit is latched and the CTA winds down (no trap).
@@ -37,7 +38,8 @@ namespace {
 
 constexpr int KIND_NVFP4 = 0, KIND_MXFP8 = 1;
 constexpr int BM = 128, BN = 128;
-constexpr int STAGES = 5;
+constexpr int STAGES = 4;
+constexpr int STAGE_OUT_BYTES = 32 * 128;  // one epilogue staging buffer: 32 rows x 128 bytes
 constexpr int TILE_BYTES = 128 * 128;  // one operand tile: 128 rows x 128 bytes
 constexpr int MAX_GROUPS = 1024;
 constexpr int NUM_THREADS = 256;
@@ -55,7 +57,8 @@ struct Cfg {
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES + 2 * RAW_BYTES + 2 * SFT_BYTES;
     static constexpr uint32_t TX_BYTES = 2 * TILE_BYTES + 2 * RAW_BYTES;
     static constexpr uint32_t SF_COLS_STAGE = 2 * 4 * SFT_CHUNKS;  // A and B, 4 columns per chunk
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 1024 + 2 * (MAX_GROUPS + 1) * 4;
+    static constexpr int SMEM_BYTES =
+        1024 + STAGES * STAGE_BYTES + 4 * 2 * STAGE_OUT_BYTES + 1024 + 2 * (MAX_GROUPS + 1) * 4;
 };
 static_assert(Cfg<KIND_NVFP4>::STAGE_BYTES % 1024 == 0, "stage alignment");
 static_assert(Cfg<KIND_MXFP8>::STAGE_BYTES % 1024 == 0, "stage alignment");
@@ -145,13 +148,14 @@ template <int KIND, int OUT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                             const GemmArgs p)
+                             const __grid_constant__ CUtensorMap tmO, const GemmArgs p)
 {
     using C = Cfg<KIND>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * C::STAGE_BYTES);
+    uint8_t *staging = smem + STAGES * C::STAGE_BYTES;  // epilogue: 4 warps x 2 x 4 KB
+    uint64_t *bars = reinterpret_cast<uint64_t *>(staging + 4 * 2 * STAGE_OUT_BYTES);
     // barrier slots: full[S], empty[S], acc_full[2], acc_empty[2], drain
     const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + 8 * STAGES;
     const uint32_t bar_acc_full = bar_empty + 8 * STAGES, bar_acc_empty = bar_acc_full + 16;
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
     int *s_abort = reinterpret_cast<int *>(tmem_slot + 1);
     int *s_total = s_abort + 1;
-    int *s_off = reinterpret_cast<int *>(smem + STAGES * C::STAGE_BYTES + 1024);
+    int *s_off = reinterpret_cast<int *>(staging + 4 * 2 * STAGE_OUT_BYTES + 1024);
     int *s_cum = s_off + (MAX_GROUPS + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -180,6 +184,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmSA);
         tma_prefetch_desc(&tmSB);
+        tma_prefetch_desc(&tmO);
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -372,7 +377,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     } else if (warp >= 4) {
         // ---------------------------------------------------- epilogue
+        // Warp q owns accumulator lanes (rows) 32q .. 32q+31.  A slice whose
+        // 32 rows are all valid is staged in shared memory (32 rows x 128 B,
+        // 128-byte swizzle, two buffers) and written by a TMA tensor store in
+        // full 128-byte lines; a slice cut by an expert boundary is written
+        // row by row with predicated stores.
         const int q = warp & 3;
+        uint8_t *stg = staging + q * 2 * STAGE_OUT_BYTES;
+        constexpr int CH_PER_STORE = OUT == PMN_OUT_F32 ? 1 : (OUT == PMN_OUT_BF16 ? 2 : 4);
+        uint32_t nstore = 0;
         uint32_t abuf = 0, aphase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const Tile ti = get_tile<KIND>(t, p, s_off, s_cum);
@@ -397,11 +410,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             }
             tc_fence_after();
+            const bool slice_any = ti.m0 + 32 * q < ti.row_end;
+            const bool slice_full = ti.m0 + 32 * q + 32 <= ti.row_end;
             float scale = 1.0f;
             if (KIND == KIND_NVFP4 && valid) scale = p.a_outer[row];
             const float gb = KIND == KIND_NVFP4 ? p.b_outer[ti.g] : 1.0f;
             const uint32_t sigma = OUT == PMN_OUT_RHT_S2F6 ? rht_sigma(p.seed) : 0u;
-            const int64_t orow = p.group_k ? ((int64_t)ti.g * p.m + row) : row;
+            const int64_t obase = p.group_k ? (int64_t)ti.g * p.m : 0;
+            const int64_t orow = obase + row;
+            uint32_t sc_word = 0u;
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + abuf * BN + 32 * c, r);
@@ -411,18 +428,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_acc_empty + 8 * abuf);
                 }
-                if (!valid) continue;
+                if (!slice_any) continue;
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     v[j] = __uint_as_float(r[j]);
                     if (KIND == KIND_NVFP4) v[j] = __fmul_rn(__fmul_rn(v[j], scale), gb);
                 }
-                const int64_t col = ti.n0 + 32 * c;
+                // the 16-byte chunks this 32-column piece contributes to a 128-byte row
+                uint4 chunk[8];
+                int nch;
                 if (OUT == PMN_OUT_F32) {
-                    float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + orow * p.n + col);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    for (int j = 0; j < 8; ++j)
+                        chunk[j] = make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                                              __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+                    nch = 8;
                 } else if (OUT == PMN_OUT_BF16) {
                     uint32_t w[16];
 #pragma unroll
@@ -430,23 +451,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
                         w[j] = *reinterpret_cast<uint32_t *>(&b2);
                     }
-                    uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out) + orow * p.n + col);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) o[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    for (int j = 0; j < 4; ++j) chunk[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    nch = 4;
                 } else {
                     uint32_t qv[8];
                     const uint32_t sb = rht32_s2f6(v, sigma, qv);
-                    uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<int8_t *>(p.out) + orow * p.n + col);
-                    o[0] = make_uint4(qv[0], qv[1], qv[2], qv[3]);
-                    o[1] = make_uint4(qv[4], qv[5], qv[6], qv[7]);
-                    p.out_sc[orow * (p.n / 32) + col / 32] = (uint8_t)sb;
+                    chunk[0] = make_uint4(qv[0], qv[1], qv[2], qv[3]);
+                    chunk[1] = make_uint4(qv[4], qv[5], qv[6], qv[7]);
+                    nch = 2;
+                    sc_word |= sb << (8 * c);
+                }
+                const int part = c % CH_PER_STORE;
+                if (slice_full) {
+                    uint8_t *buf = stg + (nstore & 1u) * STAGE_OUT_BYTES;
+                    if (part == 0) {
+                        if (lane == 0) bulk_wait_group_read<1>();  // the older store has left this buffer
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (j < nch) {
+                            const int ci = part * nch + j;
+                            *reinterpret_cast<uint4 *>(buf + lane * 128 + ((ci ^ (lane & 7)) << 4)) = chunk[j];
+                        }
+                    if (part == CH_PER_STORE - 1) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int32_t x = (int32_t)(ti.n0 + 32 * (c - part));
+                            tma_store_2d(&tmO, smem_u32(buf), x, (int32_t)(obase + ti.m0 + 32 * q));
+                            bulk_commit_group();
+                        }
+                        ++nstore;
+                    }
+                } else if (valid) {
+                    const int64_t col = ti.n0 + 32 * c;
+                    uint8_t *o;
+                    if (OUT == PMN_OUT_F32) o = reinterpret_cast<uint8_t *>(reinterpret_cast<float *>(p.out) + orow * p.n + col);
+                    else if (OUT == PMN_OUT_BF16) o = reinterpret_cast<uint8_t *>(reinterpret_cast<uint16_t *>(p.out) + orow * p.n + col);
+                    else o = reinterpret_cast<uint8_t *>(p.out) + orow * p.n + col;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (j < nch) reinterpret_cast<uint4 *>(o)[j] = chunk[j];
                 }
             }
+            if (OUT == PMN_OUT_RHT_S2F6 && valid)
+                *reinterpret_cast<uint32_t *>(p.out_sc + orow * (p.n / 32) + ti.n0 / 32) = sc_word;
             if (++abuf == 2) {
                 abuf = 0;
                 aphase ^= 1;
             }
         }
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -493,6 +551,25 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t width_bytes, uint64_t r
     return r == CUDA_SUCCESS;
 }
 
+// Output tensor [rows, n] of element size esize for the epilogue's TMA
+// stores: box = 128 bytes x 32 rows, 128-byte swizzle.
+bool make_out_map(CUtensorMap *m, void *base, int out_kind, uint64_t n, uint64_t rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const CUtensorMapDataType dt = out_kind == PMN_OUT_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : out_kind == PMN_OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const uint64_t es = out_kind == PMN_OUT_F32 ? 4 : (out_kind == PMN_OUT_BF16 ? 2 : 1);
+    cuuint64_t dims[2] = {n, rows};
+    cuuint64_t strides[1] = {n * es};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / es), 32};
+    cuuint32_t elem[2] = {1, 1};
+    CUresult r = fn(m, dt, 2, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int num_sms()
@@ -505,7 +582,7 @@ int num_sms()
 
 template <int KIND, int OUT>
 pmn_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &sa, const CUtensorMap &sb,
-                       const GemmArgs &args, cudaStream_t s)
+                       const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
 {
     auto kern = block_scaled_gemm_kernel<KIND, OUT>;
     const int smem = Cfg<KIND>::SMEM_BYTES;
@@ -513,7 +590,7 @@ pmn_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
         return PMN_ERR_CUDA;
     const int sms = num_sms();
     if (sms <= 0) return PMN_ERR_CUDA;
-    kern<<<sms, NUM_THREADS, smem, s>>>(a, b, sa, sb, args);
+    kern<<<sms, NUM_THREADS, smem, s>>>(a, b, sa, sb, o, args);
     return cudaGetLastError() == cudaSuccess ? PMN_OK : PMN_ERR_CUDA;
 }
 
@@ -531,8 +608,9 @@ pmn_status nvfp4_common(const uint8_t *a_codes, const uint8_t *a_scales, const f
         return PMN_ERR_INVALID_ARG;
     if (out_kind == PMN_OUT_RHT_S2F6 && !out_sc) return PMN_ERR_INVALID_ARG;
     if (total_rows == 0) return PMN_OK;
-    CUtensorMap ma, mb, msa, msb;
+    CUtensorMap ma, mb, msa, msb, mo;
     const uint64_t brows = (uint64_t)num_experts * (uint64_t)n;
+    if (!make_out_map(&mo, out, out_kind, n, total_rows)) return PMN_ERR_CUDA;
     if (!make_map(&ma, a_codes, k / 2, total_rows, k / 2, 128, true) ||
         !make_map(&mb, b_codes, k / 2, brows, k / 2, 128, true) ||
         !make_map(&msa, a_scales, k / 16, total_rows, k / 16, 16, false) ||
@@ -553,9 +631,9 @@ pmn_status nvfp4_common(const uint8_t *a_codes, const uint8_t *a_scales, const f
     args.seed = seed;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (out_kind) {
-        case PMN_OUT_BF16: return launch_gemm<KIND_NVFP4, PMN_OUT_BF16>(ma, mb, msa, msb, args, s);
-        case PMN_OUT_F32: return launch_gemm<KIND_NVFP4, PMN_OUT_F32>(ma, mb, msa, msb, args, s);
-        case PMN_OUT_RHT_S2F6: return launch_gemm<KIND_NVFP4, PMN_OUT_RHT_S2F6>(ma, mb, msa, msb, args, s);
+        case PMN_OUT_BF16: return launch_gemm<KIND_NVFP4, PMN_OUT_BF16>(ma, mb, msa, msb, mo, args, s);
+        case PMN_OUT_F32: return launch_gemm<KIND_NVFP4, PMN_OUT_F32>(ma, mb, msa, msb, mo, args, s);
+        case PMN_OUT_RHT_S2F6: return launch_gemm<KIND_NVFP4, PMN_OUT_RHT_S2F6>(ma, mb, msa, msb, mo, args, s);
         default: return PMN_ERR_INVALID_ARG;
     }
 }
@@ -633,8 +711,10 @@ extern "C" pmn_status pmn_gemm_mxfp8(const uint8_t *a, const uint8_t *a_scales, 
     if (m == 0) return PMN_OK;
     if (group_mode == PMN_GROUP_M && k == 0) return PMN_ERR_INVALID_ARG;
     const uint64_t brows = group_mode == PMN_GROUP_M ? (uint64_t)num_groups * (uint64_t)n : (uint64_t)n;
-    CUtensorMap ma, mb, msa, msb;
+    CUtensorMap ma, mb, msa, msb, mo;
     if (k == 0) return PMN_ERR_INVALID_ARG;
+    const uint64_t orows = group_mode == PMN_GROUP_M ? (uint64_t)m : (uint64_t)num_groups * (uint64_t)m;
+    if (!make_out_map(&mo, out, out_kind, n, orows)) return PMN_ERR_CUDA;
     if (!make_map(&ma, a, k, m, k, 128, true) || !make_map(&mb, b, k, brows, k, 128, true) ||
         !make_map(&msa, a_scales, k / 32, m, k / 32, 32, false) ||
         !make_map(&msb, b_scales, k / 32, brows, k / 32, 32, false))
@@ -649,6 +729,6 @@ extern "C" pmn_status pmn_gemm_mxfp8(const uint8_t *a, const uint8_t *a_scales, 
     args.k = k;
     args.out = out;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (out_kind == PMN_OUT_BF16) return launch_gemm<KIND_MXFP8, PMN_OUT_BF16>(ma, mb, msa, msb, args, s);
-    return launch_gemm<KIND_MXFP8, PMN_OUT_F32>(ma, mb, msa, msb, args, s);
+    if (out_kind == PMN_OUT_BF16) return launch_gemm<KIND_MXFP8, PMN_OUT_BF16>(ma, mb, msa, msb, mo, args, s);
+    return launch_gemm<KIND_MXFP8, PMN_OUT_F32>(ma, mb, msa, msb, mo, args, s);
 }
