@@ -9,9 +9,10 @@
 // One persistent kernel per call, one CTA per SM, 8 warps:
 //   warp 0      TMA producer: code tiles (128 rows x 128 bytes, 128-byte
 //               swizzle) and raw scale tiles into a 4-stage ring
-//   warp 1      re-lays the stage's scale factors into the 32x128-bit form
-//               tcgen05.cp expects, copies them to TMEM and issues the MMAs
-//               (one elected lane), committing to the stage's empty barrier
+//   warp 2      re-lays each stage's scale factors into the 32x128-bit form
+//               tcgen05.cp expects (runs ahead of the MMA issuer)
+//   warp 1      copies the scale factors to TMEM and issues the MMAs (one
+//               elected lane), committing to the stage's empty barrier
 //   warps 4..7  epilogue: TMEM -> registers (one row per thread), outer
 //               scales, bf16/fp32 or RHT + S2F6, staged in shared memory and
 //               written by TMA tensor stores in full 128-byte lines
@@ -156,11 +157,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t *stages = smem;
     uint8_t *staging = smem + STAGES * C::STAGE_BYTES;  // epilogue: 4 warps x 2 x 4 KB
     uint64_t *bars = reinterpret_cast<uint64_t *>(staging + 4 * 2 * STAGE_OUT_BYTES);
-    // barrier slots: full[S], empty[S], acc_full[2], acc_empty[2], drain
+    // barrier slots: full[S], empty[S], sf_ready[S], acc_full[2], acc_empty[2], drain
     const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + 8 * STAGES;
-    const uint32_t bar_acc_full = bar_empty + 8 * STAGES, bar_acc_empty = bar_acc_full + 16;
+    const uint32_t bar_sfr = bar_empty + 8 * STAGES;  // scale factors re-laid for the stage
+    const uint32_t bar_acc_full = bar_sfr + 8 * STAGES, bar_acc_empty = bar_acc_full + 16;
     const uint32_t bar_drain = bar_acc_empty + 16;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 5);
     int *s_abort = reinterpret_cast<int *>(tmem_slot + 1);
     int *s_total = s_abort + 1;
     int *s_off = reinterpret_cast<int *>(staging + 4 * 2 * STAGE_OUT_BYTES + 1024);
@@ -172,6 +174,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_sfr + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_acc_full + 8 * b, 1);
@@ -264,6 +267,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int s = 0; s < STAGES; ++s)
                 if (issued & (1u << s)) (void)mbar_wait(bar_full + 8 * s, (last_parity >> s) & 1u, 1000000000ull);
         }
+    } else if (warp == 2) {
+        // ---------------------------------------------------- scale-factor re-lay
+        // Waits for a stage's TMA data, re-lays its scale factors into the
+        // 32 x 128-bit chunks tcgen05.cp expects (chunk s, 16-byte line r0 =
+        // the scale words of rows r0, r0+32, r0+64, r0+96) and signals
+        // sf_ready; it runs up to STAGES stages ahead of the MMA issuer.
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile ti = get_tile<KIND>(t, p, s_off, s_cum);
+            for (int ks = 0; ks < ti.nks; ++ks) {
+                ok = warp_wait(bar_full + 8 * stage, phase);
+                if (!ok || __any_sync(0xFFFFFFFFu, *(volatile int *)s_abort != 0)) {
+                    if (!ok && lane == 0) {
+                        *(volatile int *)s_abort = 1;
+                        latch_error(PMN_DEVERR_WAIT_TIMEOUT);
+                    }
+                    ok = false;
+                    break;
+                }
+                uint8_t *st = stages + stage * C::STAGE_BYTES;
+                const uint8_t *rawA = st + 2 * TILE_BYTES, *rawB = rawA + C::RAW_BYTES;
+                uint8_t *sftA = st + 2 * TILE_BYTES + 2 * C::RAW_BYTES, *sftB = sftA + C::SFT_BYTES;
+                if (KIND == KIND_NVFP4) {
+#pragma unroll
+                    for (int op = 0; op < 2; ++op) {
+                        const uint8_t *raw = op ? rawB : rawA;
+                        uint8_t *sft = op ? sftB : sftA;
+                        uint4 w[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * 16);
+                        *reinterpret_cast<uint4 *>(sft + 0 * 512 + lane * 16) = make_uint4(w[0].x, w[1].x, w[2].x, w[3].x);
+                        *reinterpret_cast<uint4 *>(sft + 1 * 512 + lane * 16) = make_uint4(w[0].y, w[1].y, w[2].y, w[3].y);
+                        *reinterpret_cast<uint4 *>(sft + 2 * 512 + lane * 16) = make_uint4(w[0].z, w[1].z, w[2].z, w[3].z);
+                        *reinterpret_cast<uint4 *>(sft + 3 * 512 + lane * 16) = make_uint4(w[0].w, w[1].w, w[2].w, w[3].w);
+                    }
+                } else {
+                    const int64_t k0 = ti.kb + (int64_t)ks * 128;
+                    const int rem = (int)((k0 / 32) & 15);  // byte offset of this stage's 4 scales in the raw row
+                    const int wsel = rem >> 2, sh = (rem & 3) * 8;  // warp-uniform
+#pragma unroll
+                    for (int op = 0; op < 2; ++op) {
+                        const uint8_t *raw = op ? rawB : rawA;
+                        uint8_t *sft = op ? sftB : sftA;
+                        uint32_t v[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint4 *rw = reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * 32);
+                            const uint4 a0 = rw[0], a1 = rw[1];
+                            uint32_t lo, hi;
+                            switch (wsel) {
+                                case 0: lo = a0.x; hi = a0.y; break;
+                                case 1: lo = a0.y; hi = a0.z; break;
+                                case 2: lo = a0.z; hi = a0.w; break;
+                                default: lo = a0.w; hi = a1.x; break;
+                            }
+                            v[j] = sh ? __funnelshift_r(lo, hi, sh) : lo;
+                        }
+                        *reinterpret_cast<uint4 *>(sft + lane * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_sfr + 8 * stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer
         uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
@@ -282,7 +355,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const uint32_t d_tmem = tmem + abuf * BN;
             for (int ks = 0; ks < ti.nks; ++ks) {
-                ok = warp_wait(bar_full + 8 * stage, phase);
+                ok = warp_wait(bar_sfr + 8 * stage, phase);
                 if (!ok) {
                     if (lane == 0) {
                         *(volatile int *)s_abort = 1;
@@ -291,43 +364,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 uint8_t *st = stages + stage * C::STAGE_BYTES;
-                const uint8_t *rawA = st + 2 * TILE_BYTES, *rawB = rawA + C::RAW_BYTES;
                 uint8_t *sftA = st + 2 * TILE_BYTES + 2 * C::RAW_BYTES, *sftB = sftA + C::SFT_BYTES;
-                // Re-lay scale factors: chunk s, 16-byte line r0 holds the
-                // scale words of rows r0, r0+32, r0+64, r0+96.
-                if (KIND == KIND_NVFP4) {
-#pragma unroll
-                    for (int op = 0; op < 2; ++op) {
-                        const uint8_t *raw = op ? rawB : rawA;
-                        uint8_t *sft = op ? sftB : sftA;
-                        uint4 w[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * 16);
-                        *reinterpret_cast<uint4 *>(sft + 0 * 512 + lane * 16) = make_uint4(w[0].x, w[1].x, w[2].x, w[3].x);
-                        *reinterpret_cast<uint4 *>(sft + 1 * 512 + lane * 16) = make_uint4(w[0].y, w[1].y, w[2].y, w[3].y);
-                        *reinterpret_cast<uint4 *>(sft + 2 * 512 + lane * 16) = make_uint4(w[0].z, w[1].z, w[2].z, w[3].z);
-                        *reinterpret_cast<uint4 *>(sft + 3 * 512 + lane * 16) = make_uint4(w[0].w, w[1].w, w[2].w, w[3].w);
-                    }
-                } else {
-                    const int64_t k0 = ti.kb + (int64_t)ks * 128;
-                    const int rem = (int)((k0 / 32) & 15);  // byte offset of this stage's 4 scales
-                    const int wsel = rem >> 2, sh = (rem & 3) * 8;
-#pragma unroll
-                    for (int op = 0; op < 2; ++op) {
-                        const uint8_t *raw = op ? rawB : rawA;
-                        uint8_t *sft = op ? sftB : sftA;
-                        uint32_t v[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t *rw = reinterpret_cast<const uint32_t *>(raw + (lane + 32 * j) * 32);
-                            const uint32_t lo = rw[wsel], hi = rw[wsel + 1];
-                            v[j] = sh ? __funnelshift_r(lo, hi, sh) : lo;
-                        }
-                        *reinterpret_cast<uint4 *>(sft + lane * 16) = make_uint4(v[0], v[1], v[2], v[3]);
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
                 if (lane == 0) {
                     tc_fence_after();
                     const uint32_t sfa = tmem + SF_COL0 + stage * C::SF_COLS_STAGE;

@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "../../include/pmn.h"
@@ -179,6 +180,31 @@ __global__ void __launch_bounds__(256) nvfp4_quant_rows_kernel(
     }
 }
 
+// PER_GROUP quantisation once the group amax is known: every 16-block is
+// independent, so one thread per block streams x (32 bytes in, 9 bytes out).
+__global__ void __launch_bounds__(256) nvfp4_quant_blocks_kernel(const uint16_t *__restrict__ x, int64_t nblocks,
+                                                                 int64_t blocks_per_group,
+                                                                 const uint32_t *__restrict__ group_amax,
+                                                                 int four_over_six, uint8_t *__restrict__ codes,
+                                                                 uint8_t *__restrict__ scales)
+{
+    const int64_t bi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (bi >= nblocks) return;
+    const uint4 *p = reinterpret_cast<const uint4 *>(x + bi * 16);
+    const uint4 v0 = __ldg(p), v1 = __ldg(p + 1);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float xf[16];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        xf[2 * t] = bf16_lo(w[t]);
+        xf[2 * t + 1] = bf16_hi(w[t]);
+    }
+    const float g = outer_from_amax(__uint_as_float(__ldg(group_amax + bi / blocks_per_group)), four_over_six != 0);
+    const BlockQ q = quant_block(xf, g, four_over_six != 0);
+    *reinterpret_cast<uint2 *>(codes + bi * 8) = make_uint2(q.w0, q.w1);
+    scales[bi] = (uint8_t)q.sbyte;
+}
+
 // amax of each group of rows (contiguous: ldx == cols), as binary32 bits,
 // combined with atomicMax (order-independent, hence deterministic).
 __global__ void __launch_bounds__(256) group_amax_kernel(const uint16_t *__restrict__ x,
@@ -311,93 +337,141 @@ __global__ void __launch_bounds__(256) mxfp8_quant_transposed_kernel(const uint1
 }
 
 // ------------------------------------------------------------------ requant [SR]
-// Tile of 128 input rows x 128 input cols.  Phase 1: dequantise
-// d = (dec(code) * dec(S)) * g in binary32 into shared memory, stored
-// transposed (row c of the tile holds d[r, c] for its 128 rows r).  Phase 2:
-// thread (c, rb) forms the 32-block of output row c, its E8M0 exponent e,
-// y = d * 2^-e (exact) and the E4M3 bytes: stochastic rounding by the
-// hardware convert fed with Philox words (one Philox call per 16 elements),
-// or round-to-nearest-even.
+// Persistent kernel over tiles of 128 input rows x 128 input cols.  Phase 1:
+// dequantise d = (dec(code) * dec(S)) * g in binary32 into shared memory,
+// stored transposed (output row c holds d[r, c] for the tile's 128 rows r, in
+// four 32-blocks each padded to 36 floats so both phases are conflict-free).
+// Phase 2: task (c, rb) forms the 32-block of output row c, its E8M0 exponent
+// e, y = d * 2^-e (exact) and the E4M3 bytes -- stochastic rounding by the
+// hardware convert fed with Philox words (one Philox call per 16 elements) or
+// round-to-nearest-even.  Four consecutive lanes write one 128-byte line.
+// The next tile's codes are loaded into registers before phase 2 so its HBM
+// latency overlaps the current tile's arithmetic.
 constexpr int RQ_T = 128;
-constexpr int RQ_PITCH = RQ_T + 4;  // rows stay 16-byte aligned; column writes and 128-bit row reads are conflict-free
+constexpr int RQ_BLK = 36;                // padded 32-block (floats)
+constexpr int RQ_ROW = 4 * RQ_BLK;        // one output row of the tile (floats)
 
-__global__ void __launch_bounds__(256) requant_transpose_kernel(
+struct RqRegs {
+    uint4 q0, q1;
+    uint32_t sw;
+    float g;
+    bool ok;
+};
+
+__device__ __forceinline__ RqRegs requant_load(const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales,
+                                               const float *__restrict__ outer, int outer_per_row, int64_t rows,
+                                               int64_t cols, int64_t b, int64_t r0, int64_t c0, int r, int h)
+{
+    RqRegs x;
+    const int64_t src = b * rows + r0 + r;
+    x.ok = (r0 + r < rows) && (c0 + h * 64 < cols);
+    x.q0 = make_uint4(0u, 0u, 0u, 0u);
+    x.q1 = x.q0;
+    x.sw = 0u;
+    x.g = 0.0f;
+    if (x.ok) {
+        x.g = outer_per_row ? __ldg(outer + src) : __ldg(outer + b);
+        const uint8_t *pc = codes + src * (cols / 2) + (c0 + h * 64) / 2;
+        x.q0 = __ldg(reinterpret_cast<const uint4 *>(pc));
+        x.q1 = __ldg(reinterpret_cast<const uint4 *>(pc + 16));
+        x.sw = __ldg(reinterpret_cast<const uint32_t *>(scales + src * (cols / 16) + (c0 + h * 64) / 16));
+    }
+    return x;
+}
+
+__global__ void __launch_bounds__(256, 3) requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, const float *__restrict__ outer,
-    int outer_per_row, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, int stochastic,
+    int outer_per_row, int64_t batch, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, int stochastic,
     uint8_t *__restrict__ out, uint8_t *__restrict__ out_sc)
 {
-    extern __shared__ float dT[];  // [RQ_T (c)][RQ_PITCH (r)]
-    const int64_t b = blockIdx.z;
-    const int64_t r0 = (int64_t)blockIdx.y * RQ_T, c0 = (int64_t)blockIdx.x * RQ_T;
-    const int64_t cols2 = cols / 2, cols16 = cols / 16;
-    // phase 1: thread -> row r = t % 128, half h = t / 128 (64 columns each)
-    {
-        const int r = threadIdx.x & 127, h = threadIdx.x >> 7;
-        const int64_t src = b * rows + r0 + r;
-        const bool ok = (r0 + r < rows) && (c0 + h * 64 < cols);
-        float g = 0.0f;
-        uint4 q0 = make_uint4(0u, 0u, 0u, 0u), q1 = q0;
-        uint32_t sw = 0u;
-        if (ok) {
-            g = outer_per_row ? outer[src] : outer[b];
-            const uint8_t *pc = codes + src * cols2 + (c0 + h * 64) / 2;
-            q0 = __ldg(reinterpret_cast<const uint4 *>(pc));
-            q1 = __ldg(reinterpret_cast<const uint4 *>(pc + 16));
-            sw = __ldg(reinterpret_cast<const uint32_t *>(scales + src * cols16 + (c0 + h * 64) / 16));
-        }
-        const uint32_t cw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        float *dst = dT + (h * 64) * RQ_PITCH + r;
+    extern __shared__ float dT[];  // [RQ_T (c)][4 blocks][RQ_BLK]
+    const int64_t tiles_c = (cols + RQ_T - 1) / RQ_T, tiles_r = (rows + RQ_T - 1) / RQ_T;
+    const int64_t ntiles = batch * tiles_r * tiles_c;
+    const int r = threadIdx.x & 127, h = threadIdx.x >> 7;
+    auto coords = [&](int64_t t, int64_t &b, int64_t &r0, int64_t &c0) {
+        c0 = (t % tiles_c) * RQ_T;
+        const int64_t u = t / tiles_c;
+        r0 = (u % tiles_r) * RQ_T;
+        b = u / tiles_r;
+    };
+    int64_t t = blockIdx.x;
+    if (t >= ntiles) return;
+    int64_t b, r0, c0;
+    coords(t, b, r0, c0);
+    RqRegs cur = requant_load(codes, scales, outer, outer_per_row, rows, cols, b, r0, c0, r, h);
+    for (; t < ntiles; t += gridDim.x) {
+        // phase 1: row r of the tile, 64 columns (half h)
+        {
+            const uint32_t cw[8] = {cur.q0.x, cur.q0.y, cur.q0.z, cur.q0.w, cur.q1.x, cur.q1.y, cur.q1.z, cur.q1.w};
+            float *dst = dT + (h * 64) * RQ_ROW + (r >> 5) * RQ_BLK + (r & 31);
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-            const float dS = e4m3_to_f32((sw >> (8 * blk)) & 0xFFu);
+            for (int blk = 0; blk < 4; ++blk) {
+                const uint32_t dS2 = e4m3_to_h2((cur.sw >> (8 * blk)) & 0xFFu);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int jj = blk * 16 + j;
-                const uint32_t code = (cw[jj >> 3] >> (4 * (jj & 7))) & 15u;
-                dst[jj * RQ_PITCH] = __fmul_rn(__fmul_rn(e2m1_to_f32(code), dS), g);
+                for (int j = 0; j < 16; j += 2) {
+                    const int jj = blk * 16 + j;
+                    const uint32_t byte = (cw[jj >> 3] >> (4 * (jj & 7))) & 0xFFu;
+                    const float2 cs = e2m1x2_mul_scale(byte, dS2);  // exact code * scale
+                    dst[jj * RQ_ROW] = cur.ok ? __fmul_rn(cs.x, cur.g) : 0.0f;
+                    dst[(jj + 1) * RQ_ROW] = cur.ok ? __fmul_rn(cs.y, cur.g) : 0.0f;
+                }
             }
         }
-    }
-    __syncthreads();
-    // phase 2: 128 output rows x 4 row-blocks = 512 tasks, 2 per thread
+        __syncthreads();
+        // prefetch the next tile while this one is rounded
+        int64_t nb = 0, nr0 = 0, nc0 = 0;
+        const int64_t tn = t + gridDim.x;
+        RqRegs nxt;
+        nxt.ok = false;
+        if (tn < ntiles) {
+            coords(tn, nb, nr0, nc0);
+            nxt = requant_load(codes, scales, outer, outer_per_row, rows, cols, nb, nr0, nc0, r, h);
+        }
+        // phase 2: 128 output rows x 4 row-blocks = 512 tasks, 2 per thread
 #pragma unroll 1
-    for (int task = threadIdx.x; task < RQ_T * 4; task += blockDim.x) {
-        const int c = task & 127, rb = task >> 7;
-        const int64_t oc = c0 + c, orow0 = r0 + rb * 32;
-        if (oc >= cols || orow0 >= rows) continue;
-        float v[32];
-        const float4 *src = reinterpret_cast<const float4 *>(dT + c * RQ_PITCH + rb * 32);
-        float amax = 0.0f;
+        for (int task = threadIdx.x; task < RQ_T * 4; task += blockDim.x) {
+            const int c = task >> 2, rb = task & 3;
+            const int64_t oc = c0 + c, orow0 = r0 + rb * 32;
+            if (oc >= cols || orow0 >= rows) continue;
+            float v[32];
+            const float4 *src = reinterpret_cast<const float4 *>(dT + c * RQ_ROW + rb * RQ_BLK);
+            float amax = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float4 f = src[k];
-            v[4 * k] = f.x;
-            v[4 * k + 1] = f.y;
-            v[4 * k + 2] = f.z;
-            v[4 * k + 3] = f.w;
-            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+            for (int k = 0; k < 8; ++k) {
+                const float4 f = src[k];
+                v[4 * k] = f.x;
+                v[4 * k + 1] = f.y;
+                v[4 * k + 2] = f.z;
+                v[4 * k + 3] = f.w;
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+            }
+            const int e = mx_exponent_448(amax);
+            const float sc = exp2_neg(e);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(v[j], sc);  // exact scaling
+            const int64_t i0 = (b * cols + oc) * rows + orow0;      // output index, multiple of 32
+            uint32_t o[8];
+            if (stochastic) {
+                const uint4 wa = sr_words16(seed, tag, (uint64_t)i0 >> 4);
+                const uint4 wb = sr_words16(seed, tag, ((uint64_t)i0 >> 4) + 1);
+                const uint32_t wd[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) o[k] = cvt_e4m3x4_rs(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], wd[k]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    o[k] = cvt_e4m3x2_rn(v[4 * k], v[4 * k + 1]) | (cvt_e4m3x2_rn(v[4 * k + 2], v[4 * k + 3]) << 16);
+            }
+            uint4 *po = reinterpret_cast<uint4 *>(out + i0);
+            po[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            po[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            out_sc[(b * cols + oc) * (rows / 32) + orow0 / 32] = (uint8_t)(e + 127);
         }
-        const int e = mx_exponent_448(amax);
-        const float sc = exp2_neg(e);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(v[j], sc);  // exact scaling
-        const int64_t i0 = (b * cols + oc) * rows + orow0;      // output index, multiple of 32
-        uint32_t o[8];
-        if (stochastic) {
-            const uint4 wa = sr_words16(seed, tag, (uint64_t)i0 >> 4);
-            const uint4 wb = sr_words16(seed, tag, ((uint64_t)i0 >> 4) + 1);
-            const uint32_t wd[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-            for (int k = 0; k < 8; ++k) o[k] = cvt_e4m3x4_rs(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], wd[k]);
-        } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                o[k] = cvt_e4m3x2_rn(v[4 * k], v[4 * k + 1]) | (cvt_e4m3x2_rn(v[4 * k + 2], v[4 * k + 3]) << 16);
-        }
-        uint4 *po = reinterpret_cast<uint4 *>(out + i0);
-        po[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        po[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        out_sc[(b * cols + oc) * (rows / 32) + orow0 / 32] = (uint8_t)(e + 127);
+        __syncthreads();
+        cur = nxt;
+        b = nb;
+        r0 = nr0;
+        c0 = nc0;
     }
 }
 
@@ -462,6 +536,14 @@ extern "C" pmn_status pmn_nvfp4_quantize(const void *x, int64_t rows, int64_t co
         if (launch_status() != PMN_OK) return PMN_ERR_CUDA;
         gam = reinterpret_cast<const uint32_t *>(outer);
     }
+    if (outer_mode == PMN_OUTER_PER_GROUP) {
+        const int64_t nblocks = rows * (cols / 16);
+        nvfp4_quant_blocks_kernel<<<(unsigned)((nblocks + 255) / 256), 256, 0, s>>>(
+            xb, nblocks, rows_per_group * (cols / 16), gam, four_over_six, codes, scales);
+        if (launch_status() != PMN_OK) return PMN_ERR_CUDA;
+        group_outer_finish_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, s>>>(outer, groups, four_over_six);
+        return launch_status();
+    }
     const int nb = (int)((cols / 16 + 31) / 32);
     dim3 block(256), grid((unsigned)((rows + 7) / 8));
     const int pg = outer_mode == PMN_OUTER_PER_GROUP;
@@ -513,14 +595,20 @@ extern "C" pmn_status pmn_requant_transpose_sr_mxfp8(const uint8_t *codes, const
     if (!aligned16(codes) || !aligned16(scales) || !aligned16(out) || ((uintptr_t)outer & 3u)) return PMN_ERR_INVALID_ARG;
     if (batch == 0 || rows == 0 || cols == 0) return PMN_OK;
     if ((cols / 16) % 4 != 0) return PMN_ERR_INVALID_ARG;  // 4-byte scale words per 64 columns
-    const int smem = RQ_T * RQ_PITCH * (int)sizeof(float);
+    const int smem = RQ_T * RQ_ROW * (int)sizeof(float);
     if (cudaFuncSetAttribute(requant_transpose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
         return PMN_ERR_CUDA;
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_transpose_kernel, 256, smem) != cudaSuccess)
+        return PMN_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    dim3 grid((unsigned)((cols + RQ_T - 1) / RQ_T), (unsigned)((rows + RQ_T - 1) / RQ_T), (unsigned)batch);
-    requant_transpose_kernel<<<grid, 256, smem, s>>>(codes, scales, outer, outer_mode == PMN_OUTER_PER_ROW, rows,
-                                                     cols, seed, tag, rounding == PMN_ROUND_SR, out, out_scales);
+    const int64_t ntiles = batch * ((rows + RQ_T - 1) / RQ_T) * ((cols + RQ_T - 1) / RQ_T);
+    const int64_t grid = std::min<int64_t>(ntiles, (int64_t)sms * std::max(per_sm, 1));
+    requant_transpose_kernel<<<(unsigned)grid, 256, smem, s>>>(codes, scales, outer, outer_mode == PMN_OUTER_PER_ROW,
+                                                               batch, rows, cols, seed, tag, rounding == PMN_ROUND_SR,
+                                                               out, out_scales);
     return launch_status();
 }
 
