@@ -66,6 +66,8 @@ def lib():
         L.orc_e8m0_exponent.argtypes = [ctypes.c_double, ctypes.c_double]
         L.orc_e8m0_exponent.restype = i32
         L.orc_requant_transpose_mxfp8.argtypes = [P, P, P, i32, i64, i64, i64, u64, u32, i32, P, P]
+        L.orc_requant_transpose_mxfp8_window.argtypes = [P, P, P, i32, i64, i64, i64, u64, u32, i32, P, P,
+                                                         i64, i64, i64]
         L.orc_mxfp8_quantize.argtypes = [P, i64, i64, i32, P, P]
         L.orc_mxfp8_dequant_f64.argtypes = [P, P, i64, i64, P]
         L.orc_rht_sign_word.argtypes = [u64]
@@ -223,17 +225,21 @@ def nvfp4_dequant_f64(codes, scales):
 
 # ---------------------------------------------------------------- MXFP8 [SR]
 def requant_transpose_mxfp8(codes, scales, outer, outer_per_row, batch, rows, cols, seed, tag,
-                            stochastic=True):
-    """NVFP4 [batch, rows, cols] -> dequant -> transpose -> MXFP8 [batch, cols, rows]."""
+                            stochastic=True, b_begin=0, rows_total=None, r_begin=0):
+    """NVFP4 [batch, rows, cols] -> dequant -> transpose -> MXFP8 [batch, cols, rows].
+
+    With b_begin / rows_total / r_begin the inputs are a window of a larger
+    tensor and the random bits follow the element's index in the full output."""
     codes = _c(codes, np.uint8).reshape(batch * rows, cols // 2)
     scales = _c(scales, np.uint8).reshape(batch * rows, cols // 16)
     outer = _c(outer, np.float32)
-    assert rows % 32 == 0
+    assert rows % 32 == 0 and r_begin % 32 == 0
     out = np.zeros((batch, cols, rows), np.uint8)
     out_sc = np.zeros((batch, cols, rows // 32), np.uint8)
-    lib().orc_requant_transpose_mxfp8(_p(codes), _p(scales), _p(outer), 0 if outer_per_row else 1,
-                                      batch, rows, cols, seed, tag, 0 if stochastic else 1,
-                                      _p(out), _p(out_sc))
+    lib().orc_requant_transpose_mxfp8_window(_p(codes), _p(scales), _p(outer), 0 if outer_per_row else 1,
+                                             batch, rows, cols, seed, tag, 0 if stochastic else 1,
+                                             _p(out), _p(out_sc), b_begin, rows if rows_total is None else rows_total,
+                                             r_begin)
     return out, out_sc
 
 

@@ -412,10 +412,31 @@ ORC_API int orc_e8m0_exponent(double amax, double top)
  * [batch, cols, rows/32]; 32-blocks run along the original rows.  rounding 0:
  * stochastic with orc_sr_bits16(seed, tag, i), i the row-major output index;
  * rounding 1: nearest even. */
+ORC_API void orc_requant_transpose_mxfp8_window(const uint8_t *codes, const uint8_t *scales,
+                                                const float *outer, int outer_mode, int64_t batch,
+                                                int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,
+                                                int rounding, uint8_t *out, uint8_t *out_sc,
+                                                int64_t b_begin, int64_t rows_total, int64_t r_begin);
+
 ORC_API void orc_requant_transpose_mxfp8(const uint8_t *codes, const uint8_t *scales,
                                          const float *outer, int outer_mode, int64_t batch,
                                          int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,
                                          int rounding, uint8_t *out, uint8_t *out_sc)
+{
+    orc_requant_transpose_mxfp8_window(codes, scales, outer, outer_mode, batch, rows, cols, seed, tag,
+                                       rounding, out, out_sc, 0, rows, 0);
+}
+
+/* The same computation for a window of a larger tensor (sampled checks at
+ * full size): the inputs hold batch entries b_begin .. b_begin+batch-1 and,
+ * of each, rows r_begin .. r_begin+rows-1 of rows_total (r_begin and rows
+ * multiples of 32).  The random bits use the element's index in the FULL
+ * output [*, cols, rows_total].  Output: [batch, cols, rows] (+ scales). */
+ORC_API void orc_requant_transpose_mxfp8_window(const uint8_t *codes, const uint8_t *scales,
+                                                const float *outer, int outer_mode, int64_t batch,
+                                                int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,
+                                                int rounding, uint8_t *out, uint8_t *out_sc,
+                                                int64_t b_begin, int64_t rows_total, int64_t r_begin)
 {
     #pragma omp parallel for collapse(2) schedule(static)
     for (int64_t b = 0; b < batch; ++b)
@@ -434,14 +455,16 @@ ORC_API void orc_requant_transpose_mxfp8(const uint8_t *codes, const uint8_t *sc
                 }
                 int e = orc_e8m0_exponent(amax, 448.0);
                 int64_t orow = (b * cols + c) * rows;
+                int64_t grow = ((b_begin + b) * cols + c) * rows_total + r_begin;
                 for (int j = 0; j < 32; ++j) {
                     int64_t i = orow + rb * 32 + j;
+                    int64_t gi = grow + rb * 32 + j;
                     double y = ldexp((double)d[j], -e); /* exact */
                     uint32_t q;
-                    if (rounding == 0) q = orc_e4m3_sr(y, orc_sr_bits16(seed, tag, (uint64_t)i));
+                    if (rounding == 0) q = orc_e4m3_sr(y, orc_sr_bits16(seed, tag, (uint64_t)gi));
                     else {
-                        uint32_t s = signbit(y) ? 0x80u : 0u;
-                        q = s | e4m3_encode_mag(rne_grid(fabs(y), 3, -6, 448.0));
+                        uint32_t sg = signbit(y) ? 0x80u : 0u;
+                        q = sg | e4m3_encode_mag(rne_grid(fabs(y), 3, -6, 448.0));
                     }
                     out[i] = (uint8_t)q;
                 }

@@ -264,3 +264,26 @@ def test_swiglu_vs_torch_silu():
     got = torch.from_numpy(W.bf16_bits_to_f32(h).astype(np.float64))
     ulp = torch.clamp(ref.abs(), min=1e-30) * 2.0 ** -8
     assert torch.all((got - ref).abs() <= ulp)
+
+
+def test_requant_window_equals_slice_of_full():
+    """The windowed form (used for sampled checks at full size) equals the
+    matching slice of the whole-tensor computation, random bits included."""
+    rng = np.random.default_rng(31)
+    batch, rows, cols = 3, 128, 64
+    x = W.normal_bf16_host(rng, (batch * rows, cols))
+    c, s, g = oracle.nvfp4_quantize(x, oracle.OUTER_PER_GROUP, group_offsets=np.arange(batch + 1) * rows)
+    full, full_sc = oracle.requant_transpose_mxfp8(c, s, g, False, batch, rows, cols, 5, 3)
+    b0, r0, nr = 1, 64, 32
+    cw = c.reshape(batch, rows, -1)[b0:b0 + 1, r0:r0 + nr]
+    sw = s.reshape(batch, rows, -1)[b0:b0 + 1, r0:r0 + nr]
+    win, win_sc = oracle.requant_transpose_mxfp8(cw, sw, g[b0:b0 + 1], False, 1, nr, cols, 5, 3,
+                                                 b_begin=b0, rows_total=rows, r_begin=r0)
+    assert np.array_equal(win[0], full[b0][:, r0:r0 + nr])
+    assert np.array_equal(win_sc[0], full_sc[b0][:, r0 // 32:(r0 + nr) // 32])
+    # per-row outer scales (activations)
+    c2, s2, g2 = oracle.nvfp4_quantize(x[:rows], oracle.OUTER_PER_ROW)
+    f2, f2s = oracle.requant_transpose_mxfp8(c2, s2, g2, True, 1, rows, cols, 9, 1)
+    w2, w2s = oracle.requant_transpose_mxfp8(c2[r0:r0 + nr], s2[r0:r0 + nr], g2[r0:r0 + nr], True, 1, nr, cols,
+                                             9, 1, rows_total=rows, r_begin=r0)
+    assert np.array_equal(w2[0], f2[0][:, r0:r0 + nr]) and np.array_equal(w2s[0], f2s[0][:, r0 // 32:(r0 + nr) // 32])
