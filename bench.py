@@ -227,10 +227,11 @@ def main():
     if args.only:
         for name, f in calls:  # the step once, so every operand of the chosen call exists
             f()
-        calls = [(n, f) for n, f in calls if n == args.only]
-        if not calls:
-            raise SystemExit("unknown call " + args.only)
-        alg = {args.only: alg[args.only]}
+        only = args.only.split(",")
+        calls = [(n, f) for n, f in calls if n in only]
+        if len(calls) != len(only):
+            raise SystemExit("unknown call in " + args.only)
+        alg = {n: alg[n] for n in only}
     flops_step = sum(v[0] for v in alg.values())
 
     for _ in range(args.warmup):
@@ -322,7 +323,8 @@ def main():
                     "parallelism": "replicas" if world > 1 else "single-gpu"},
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": (layer.launches_per_step() if not args.only else
-                                 layer.LAUNCHES.get(args.only, 1)) * args.steps, "clocks": clocks,
+                                 sum(layer.LAUNCHES.get(n, 1) for n in args.only.split(","))) * args.steps,
+                "clocks": clocks,
                 "components": comps}
         print(json.dumps(line))
     if world > 1:

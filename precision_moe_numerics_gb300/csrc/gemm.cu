@@ -9,10 +9,10 @@
 // One persistent kernel per call, one CTA per SM, 8 warps:
 //   warp 0      TMA producer: code tiles (128 rows x 128 bytes, 128-byte
 //               swizzle) and raw scale tiles into a 4-stage ring
-//   warp 2      re-lays each stage's scale factors into the 32x128-bit form
-//               tcgen05.cp expects (runs ahead of the MMA issuer)
-//   warp 1      copies the scale factors to TMEM and issues the MMAs (one
-//               elected lane), committing to the stage's empty barrier
+//   warps 2, 3  re-lay each stage's scale factors into the 32x128-bit form
+//               tcgen05.cp expects (even / odd stage slots, ahead of the MMAs)
+//   warp 1      one lane copies the scale factors to TMEM (one stage ahead)
+//               and issues the MMAs, committing to the stage's empty barrier
 //   warps 4..7  epilogue: TMEM -> registers (one row per thread), outer
 //               scales, bf16/fp32 or RHT + S2F6, staged in shared memory and
 //               written by TMA tensor stores in full 128-byte lines
@@ -35,35 +35,68 @@ using namespace pmn::sm100;
 
 __device__ int g_pmn_device_error = 0;
 
+// Pipeline trace points for profiling builds (-DPMN_TRACE): CTA 0 records
+// clock64() at each hand-off; compiled out otherwise.
+#ifdef PMN_TRACE
+__device__ long long g_pmn_trace[8][256];
+extern "C" __attribute__((visibility("default"))) int pmn_trace_copy(long long *host)
+{
+    return cudaMemcpyFromSymbol(host, g_pmn_trace, sizeof(g_pmn_trace)) == cudaSuccess ? 0 : 1;
+}
+#define PMN_TRACE_POINT(slot, idx)                                            \
+    do {                                                                      \
+        if (blockIdx.x == 0 && (idx) < 256) g_pmn_trace[slot][idx] = clock64(); \
+    } while (0)
+#else
+#define PMN_TRACE_POINT(slot, idx) \
+    do {                           \
+    } while (0)
+#endif
+
 namespace {
 
 constexpr int KIND_NVFP4 = 0, KIND_MXFP8 = 1;
-constexpr int BM = 128, BN = 128;
-constexpr int STAGES = 4;
+constexpr int BM = 128;
+constexpr int BN_MIN = 128;  // N-tiles are 128 or 256 columns
+#ifndef PMN_GEMM_STAGES
+#define PMN_GEMM_STAGES 4
+#endif
+#ifndef PMN_EPI_BUFS
+#define PMN_EPI_BUFS 2
+#endif
+#ifndef PMN_MAX_GROUPS
+#define PMN_MAX_GROUPS 1024
+#endif
+constexpr int EPI_BUFS = PMN_EPI_BUFS;      // epilogue staging buffers per warp
 constexpr int STAGE_OUT_BYTES = 32 * 128;  // one epilogue staging buffer: 32 rows x 128 bytes
-constexpr int TILE_BYTES = 128 * 128;  // one operand tile: 128 rows x 128 bytes
-constexpr int MAX_GROUPS = 1024;
+constexpr int A_TILE_BYTES = BM * 128;     // A stage tile: 128 rows x 128 bytes of K
+constexpr int MAX_GROUPS = PMN_MAX_GROUPS;
 constexpr int NUM_THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t SF_COL0 = 2 * BN;  // scale factors live after the two accumulators
 
-template <int KIND>
+// Per (format, N-tile width) layout.  TBN = 256 tiles hold a single TMEM
+// accumulator (two of 256 columns would leave no room for scale factors) and
+// three stages; TBN = 128 tiles double-buffer the accumulator.
+template <int KIND, int TBN>
 struct Cfg {
-    // raw scale tile per operand: 128 rows x RAW_W bytes (TMA, no swizzle)
-    static constexpr int RAW_W = KIND == KIND_NVFP4 ? 16 : 32;
-    static constexpr int RAW_BYTES = 128 * RAW_W;
-    // re-laid scale chunks per operand: one 512-byte chunk per tcgen05.cp
-    static constexpr int SFT_CHUNKS = KIND == KIND_NVFP4 ? 4 : 1;
-    static constexpr int SFT_BYTES = 512 * SFT_CHUNKS;
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES + 2 * RAW_BYTES + 2 * SFT_BYTES;
-    static constexpr uint32_t TX_BYTES = 2 * TILE_BYTES + 2 * RAW_BYTES;
-    static constexpr uint32_t SF_COLS_STAGE = 2 * 4 * SFT_CHUNKS;  // A and B, 4 columns per chunk
+    static constexpr int RB = TBN / 128;                                         // 128-row blocks of B
+    static constexpr int RAW_W = (KIND == KIND_NVFP4 || TBN == 256) ? 16 : 32;   // raw scale bytes per row
+    static constexpr int B_TILE_BYTES = TBN * 128;
+    static constexpr int RAW_A = 128 * RAW_W, RAW_B = TBN * RAW_W;
+    static constexpr int SFT_CHUNKS = KIND == KIND_NVFP4 ? 4 : 1;  // K-step chunks per stage
+    static constexpr int SFT_A = 512 * SFT_CHUNKS, SFT_B = 512 * SFT_CHUNKS * RB;
+    static constexpr int STAGE_RAW = A_TILE_BYTES + B_TILE_BYTES + RAW_A + RAW_B + SFT_A + SFT_B;
+    static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
+    static constexpr int STAGES = TBN == 256 ? 3 : PMN_GEMM_STAGES;
+    static constexpr int ACC = TBN == 256 ? 1 : 2;
+    static constexpr uint32_t SF_COL0 = ACC * TBN;  // scale factors live after the accumulators
+    static constexpr uint32_t SFA_COLS = 4 * SFT_CHUNKS, SFB_COLS = 4 * SFT_CHUNKS * RB;
+    static constexpr uint32_t SF_COLS_STAGE = SFA_COLS + SFB_COLS;
     static constexpr int SMEM_BYTES =
-        1024 + STAGES * STAGE_BYTES + 4 * 2 * STAGE_OUT_BYTES + 1024 + 2 * (MAX_GROUPS + 1) * 4;
+        1024 + STAGES * STAGE_BYTES + 4 * EPI_BUFS * STAGE_OUT_BYTES + 1024 + 2 * (MAX_GROUPS + 1) * 4;
+    static_assert(SF_COL0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
-static_assert(Cfg<KIND_NVFP4>::STAGE_BYTES % 1024 == 0, "stage alignment");
-static_assert(Cfg<KIND_MXFP8>::STAGE_BYTES % 1024 == 0, "stage alignment");
-static_assert(SF_COL0 + STAGES * Cfg<KIND_NVFP4>::SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
 
 struct GemmArgs {
     const int32_t *offsets;  // device [groups + 1]
@@ -87,20 +120,20 @@ struct Tile {
     int nks;  // k-stages (128 bytes of K per stage)
 };
 
-// Instruction descriptor of the block-scaled MMA (M = 128, N = 128, both
+// Instruction descriptor of the block-scaled MMA (M = 128, N = TBN, both
 // operands K-major): operand formats in bits 7..9 / 10..12, N >> 3 in
 // 17..22, scale format in 23 (0 = E4M3, 1 = E8M0), M >> 4 in 24..28, scale
 // factor byte ids for B in 4..5 and A in 29..30.
-template <int KIND>
+template <int KIND, int TBN>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id)
 {
     const uint32_t fmt = KIND == KIND_NVFP4 ? 1u : 0u;  // E2M1 (mxf4nvf4) / E4M3 (mxf8f6f4)
     const uint32_t sfmt = KIND == KIND_NVFP4 ? 0u : 1u;
-    return (sf_id << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(BN >> 3) << 17) | (sfmt << 23) |
+    return (sf_id << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(TBN >> 3) << 17) | (sfmt << 23) |
            ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
 }
 
-template <int KIND>
+template <int KIND, int TBN>
 __device__ __forceinline__ Tile get_tile(int t, const GemmArgs &p, const int *s_off, const int *s_cum)
 {
     int lo = 0, hi = p.groups;
@@ -113,19 +146,18 @@ __device__ __forceinline__ Tile get_tile(int t, const GemmArgs &p, const int *s_
     ti.g = lo;
     const int local = t - s_cum[lo];
     if (!p.group_k) {
-        const int rows = s_off[lo + 1] - s_off[lo];
-        const int mt = (rows + BM - 1) / BM;
-        const int ni = local / mt, mi = local - ni * mt;
+        const int nt = (int)(p.n / TBN);
+        const int mi = local / nt, ni = local - mi * nt;  // consecutive tiles: adjacent N-tiles (cluster peers)
         ti.m0 = s_off[lo] + (int64_t)mi * BM;
-        ti.n0 = (int64_t)ni * BN;
+        ti.n0 = (int64_t)ni * TBN;
         ti.row_end = s_off[lo + 1];
         ti.kb = 0;
         ti.ke = p.k;
     } else {
-        const int nt = (int)(p.n / BN);
+        const int nt = (int)(p.n / TBN);
         const int mi = local / nt, ni = local - mi * nt;
         ti.m0 = (int64_t)mi * BM;
-        ti.n0 = (int64_t)ni * BN;
+        ti.n0 = (int64_t)ni * TBN;
         ti.row_end = p.m;
         ti.kb = s_off[lo];
         ti.ke = s_off[lo + 1];
@@ -145,18 +177,19 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity)
     return __all_sync(0xFFFFFFFFu, ok) != 0;
 }
 
-template <int KIND, int OUT>
+template <int KIND, int OUT, int CS, int TBN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                              const __grid_constant__ CUtensorMap tmO, const GemmArgs p)
 {
-    using C = Cfg<KIND>;
+    using C = Cfg<KIND, TBN>;
+    constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
-    uint8_t *staging = smem + STAGES * C::STAGE_BYTES;  // epilogue: 4 warps x 2 x 4 KB
-    uint64_t *bars = reinterpret_cast<uint64_t *>(staging + 4 * 2 * STAGE_OUT_BYTES);
+    uint8_t *staging = smem + STAGES * C::STAGE_BYTES;  // epilogue: 4 warps x EPI_BUFS x 4 KB
+    uint64_t *bars = reinterpret_cast<uint64_t *>(staging + 4 * EPI_BUFS * STAGE_OUT_BYTES);
     // barrier slots: full[S], empty[S], sf_ready[S], acc_full[2], acc_empty[2], drain
     const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + 8 * STAGES;
     const uint32_t bar_sfr = bar_empty + 8 * STAGES;  // scale factors re-laid for the stage
@@ -165,15 +198,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 5);
     int *s_abort = reinterpret_cast<int *>(tmem_slot + 1);
     int *s_total = s_abort + 1;
-    int *s_off = reinterpret_cast<int *>(staging + 4 * 2 * STAGE_OUT_BYTES + 1024);
+    int *s_off = reinterpret_cast<int *>(staging + 4 * EPI_BUFS * STAGE_OUT_BYTES + 1024);
     int *s_cum = s_off + (MAX_GROUPS + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Cluster of CS CTAs along N: consecutive tiles (same expert and M-tile,
+    // adjacent N-tiles); CTA `rank` multicasts rows [rank*128/CS, +128/CS) of
+    // the shared A tile to every peer, and a stage is free only when every
+    // peer's MMAs have consumed it.
+    const uint32_t rank = CS > 1 ? cluster_ctarank() : 0u;
+    const uint16_t cl_mask = (uint16_t)((1u << CS) - 1u);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, CS);
             mbar_init(bar_sfr + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -210,9 +249,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             s_cum[gi] = cum;
             if (!p.group_k) {
                 int rows = s_off[gi + 1] - s_off[gi];
-                cum += ((rows + BM - 1) / BM) * (int)(p.n / BN);
+                cum += ((rows + BM - 1) / BM) * (int)(p.n / TBN);
             } else {
-                cum += (int)(p.m / BM) * (int)(p.n / BN);
+                cum += (int)(p.m / BM) * (int)(p.n / TBN);
             }
         }
         s_cum[p.groups] = cum;
@@ -221,6 +260,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (CS > 1) cluster_sync();  // peers' barriers are initialised before any multicast
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int total = *s_total;
@@ -230,8 +270,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // ------------------------------------------------ TMA producer
             uint32_t stage = 0, phase = 0;
             uint32_t issued = 0, last_parity = 0;
+            int n_issued = 0;
             for (int t = blockIdx.x; t < total && !*(volatile int *)s_abort; t += gridDim.x) {
-                const Tile ti = get_tile<KIND>(t, p, s_off, s_cum);
+                const Tile ti = get_tile<KIND, TBN>(t, p, s_off, s_cum);
                 const int64_t brow = p.group_k ? ti.n0 : (int64_t)ti.g * p.n + ti.n0;
                 for (int ks = 0; ks < ti.nks; ++ks) {
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1)) {
@@ -239,9 +280,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         latch_error(PMN_DEVERR_WAIT_TIMEOUT);
                         break;
                     }
+                    PMN_TRACE_POINT(0, n_issued);
+                    ++n_issued;
                     uint8_t *st = stages + stage * C::STAGE_BYTES;
                     const uint32_t fb = bar_full + 8 * stage;
-                    mbar_arrive_expect_tx(fb, C::TX_BYTES);
+                    const uint32_t raw_w = (KIND == KIND_NVFP4 || TBN == 256 || !p.group_k) ? 16u : 32u;
+                    mbar_arrive_expect_tx(fb, A_TILE_BYTES + C::B_TILE_BYTES + (128u + TBN) * raw_w);
                     int32_t xk, xs;
                     if (KIND == KIND_NVFP4) {
                         xk = ks * 128;  // 256 fp4 values per stage
@@ -251,10 +295,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         xk = (int32_t)k0;
                         xs = (int32_t)((k0 / 32) & ~int64_t(15));  // 16-byte aligned start
                     }
-                    tma_load_2d(smem_u32(st), &tmA, fb, xk, (int32_t)ti.m0);
-                    tma_load_2d(smem_u32(st + TILE_BYTES), &tmB, fb, xk, (int32_t)brow);
-                    tma_load_2d(smem_u32(st + 2 * TILE_BYTES), &tmSA, fb, xs, (int32_t)ti.m0);
-                    tma_load_2d(smem_u32(st + 2 * TILE_BYTES + C::RAW_BYTES), &tmSB, fb, xs, (int32_t)brow);
+                    if (CS > 1)
+                        tma_load_2d_mc(smem_u32(st) + rank * (BM / CS) * 128, &tmA, fb, xk,
+                                       (int32_t)(ti.m0 + rank * (BM / CS)), cl_mask);
+                    else
+                        tma_load_2d(smem_u32(st), &tmA, fb, xk, (int32_t)ti.m0);
+                    tma_load_2d(smem_u32(st + A_TILE_BYTES), &tmB, fb, xk, (int32_t)brow);
+                    tma_load_2d(smem_u32(st + A_TILE_BYTES + C::B_TILE_BYTES), &tmSA, fb, xs, (int32_t)ti.m0);
+                    tma_load_2d(smem_u32(st + A_TILE_BYTES + C::B_TILE_BYTES + C::RAW_A), &tmSB, fb, xs, (int32_t)brow);
                     issued |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -267,17 +315,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int s = 0; s < STAGES; ++s)
                 if (issued & (1u << s)) (void)mbar_wait(bar_full + 8 * s, (last_parity >> s) & 1u, 1000000000ull);
         }
-    } else if (warp == 2) {
+    } else if (warp == 2 || warp == 3) {
         // ---------------------------------------------------- scale-factor re-lay
         // Waits for a stage's TMA data, re-lays its scale factors into the
         // 32 x 128-bit chunks tcgen05.cp expects (chunk s, 16-byte line r0 =
         // the scale words of rows r0, r0+32, r0+64, r0+96) and signals
         // sf_ready; it runs up to STAGES stages ahead of the MMA issuer.
+        // Warp 2 owns the even stage slots, warp 3 the odd ones.
+        const uint32_t mine = (uint32_t)(warp - 2);
+        const int raw_w = (KIND == KIND_NVFP4 || TBN == 256 || !p.group_k) ? 16 : 32;
         uint32_t stage = 0, phase = 0;
         bool ok = true;
+        int n_seq = 0;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const Tile ti = get_tile<KIND>(t, p, s_off, s_cum);
+            const Tile ti = get_tile<KIND, TBN>(t, p, s_off, s_cum);
             for (int ks = 0; ks < ti.nks; ++ks) {
+                const int seq = n_seq++;
+                if ((stage & 1u) != mine) {
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                    continue;
+                }
                 ok = warp_wait(bar_full + 8 * stage, phase);
                 if (!ok || __any_sync(0xFFFFFFFFu, *(volatile int *)s_abort != 0)) {
                     if (!ok && lane == 0) {
@@ -287,35 +347,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ok = false;
                     break;
                 }
+                if (lane == 0) PMN_TRACE_POINT(1, seq);
                 uint8_t *st = stages + stage * C::STAGE_BYTES;
-                const uint8_t *rawA = st + 2 * TILE_BYTES, *rawB = rawA + C::RAW_BYTES;
-                uint8_t *sftA = st + 2 * TILE_BYTES + 2 * C::RAW_BYTES, *sftB = sftA + C::SFT_BYTES;
-                if (KIND == KIND_NVFP4) {
+                const uint8_t *rawA = st + A_TILE_BYTES + C::B_TILE_BYTES, *rawB = rawA + C::RAW_A;
+                uint8_t *sftA = st + A_TILE_BYTES + C::B_TILE_BYTES + C::RAW_A + C::RAW_B, *sftB = sftA + C::SFT_A;
+                // operand op, 128-row block h: chunks at sft + (c * blocks + h) * 512
 #pragma unroll
-                    for (int op = 0; op < 2; ++op) {
-                        const uint8_t *raw = op ? rawB : rawA;
-                        uint8_t *sft = op ? sftB : sftA;
+                for (int blk = 0; blk < 1 + C::RB; ++blk) {
+                    const int op = blk == 0 ? 0 : 1, h = blk == 0 ? 0 : blk - 1;
+                    const uint8_t *raw = (op ? rawB : rawA) + h * 128 * raw_w;
+                    uint8_t *sft = (op ? sftB : sftA) + h * 512;
+                    const int cstride = (op ? C::RB : 1) * 512;
+                    if (KIND == KIND_NVFP4) {
                         uint4 w[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * 16);
-                        *reinterpret_cast<uint4 *>(sft + 0 * 512 + lane * 16) = make_uint4(w[0].x, w[1].x, w[2].x, w[3].x);
-                        *reinterpret_cast<uint4 *>(sft + 1 * 512 + lane * 16) = make_uint4(w[0].y, w[1].y, w[2].y, w[3].y);
-                        *reinterpret_cast<uint4 *>(sft + 2 * 512 + lane * 16) = make_uint4(w[0].z, w[1].z, w[2].z, w[3].z);
-                        *reinterpret_cast<uint4 *>(sft + 3 * 512 + lane * 16) = make_uint4(w[0].w, w[1].w, w[2].w, w[3].w);
-                    }
-                } else {
-                    const int64_t k0 = ti.kb + (int64_t)ks * 128;
-                    const int rem = (int)((k0 / 32) & 15);  // byte offset of this stage's 4 scales in the raw row
-                    const int wsel = rem >> 2, sh = (rem & 3) * 8;  // warp-uniform
-#pragma unroll
-                    for (int op = 0; op < 2; ++op) {
-                        const uint8_t *raw = op ? rawB : rawA;
-                        uint8_t *sft = op ? sftB : sftA;
+                        *reinterpret_cast<uint4 *>(sft + 0 * cstride + lane * 16) = make_uint4(w[0].x, w[1].x, w[2].x, w[3].x);
+                        *reinterpret_cast<uint4 *>(sft + 1 * cstride + lane * 16) = make_uint4(w[0].y, w[1].y, w[2].y, w[3].y);
+                        *reinterpret_cast<uint4 *>(sft + 2 * cstride + lane * 16) = make_uint4(w[0].z, w[1].z, w[2].z, w[3].z);
+                        *reinterpret_cast<uint4 *>(sft + 3 * cstride + lane * 16) = make_uint4(w[0].w, w[1].w, w[2].w, w[3].w);
+                    } else {
+                        const int64_t k0 = ti.kb + (int64_t)ks * 128;
+                        const int rem = (int)((k0 / 32) & 15);  // byte offset of this stage's 4 scales in the raw row
+                        const int wsel = rem >> 2, sh = (rem & 3) * 8;  // warp-uniform
                         uint32_t v[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const uint4 *rw = reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * 32);
-                            const uint4 a0 = rw[0], a1 = rw[1];
+                            const uint4 *rw = reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * raw_w);
+                            const uint4 a0 = rw[0], a1 = raw_w == 32 ? rw[1] : a0;
                             uint32_t lo, hi;
                             switch (wsel) {
                                 case 0: lo = a0.x; hi = a0.y; break;
@@ -330,7 +389,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_sfr + 8 * stage);
+                if (lane == 0) {
+                    PMN_TRACE_POINT(2, seq);
+                    mbar_arrive(bar_sfr + 8 * stage);
+                }
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1;
@@ -339,42 +401,65 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer
-        uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const Tile ti = get_tile<KIND>(t, p, s_off, s_cum);
-            if (ti.nks == 0) continue;
-            bool ok = warp_wait(bar_acc_empty + 8 * abuf, aphase ^ 1);
-            const bool aborted = __any_sync(0xFFFFFFFFu, *(volatile int *)s_abort != 0);
-            if (!ok || aborted) {
-                if (!ok && lane == 0) {
-                    *(volatile int *)s_abort = 1;
-                    latch_error(PMN_DEVERR_WAIT_TIMEOUT);
+        // One lane issues everything.  Each stage's scale factors are copied
+        // into TMEM one stage ahead (right after the previous stage's MMAs),
+        // so the copy latency hides behind tensor-core work; the TMEM slot of
+        // a stage is only rewritten after that stage's earlier MMAs completed
+        // (the producer refilled it after their commit).
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
+            bool ok = true;
+            int n_mma = 0;
+            auto next_tile = [&](int t0) {
+                for (int tt = t0; tt < total; tt += gridDim.x)
+                    if (get_tile<KIND, TBN>(tt, p, s_off, s_cum).nks > 0) return tt;
+                return total;
+            };
+            auto copy_sf = [&](uint32_t stg) {
+                uint8_t *st = stages + stg * C::STAGE_BYTES;
+                const uint8_t *sftA = st + A_TILE_BYTES + C::B_TILE_BYTES + C::RAW_A + C::RAW_B;
+                const uint8_t *sftB = sftA + C::SFT_A;
+                const uint32_t sfa = tmem + C::SF_COL0 + stg * C::SF_COLS_STAGE;
+                const uint32_t sfb = sfa + C::SFA_COLS;
+#pragma unroll
+                for (int c = 0; c < C::SFT_CHUNKS; ++c) {
+                    tc_cp_32x128b_warpx4(sfa + 4 * c, smem_desc(smem_u32(sftA + 512 * c), 0, 128, 0));
+#pragma unroll
+                    for (int h = 0; h < C::RB; ++h)
+                        tc_cp_32x128b_warpx4(sfb + 4 * (c * C::RB + h),
+                                             smem_desc(smem_u32(sftB + 512 * (c * C::RB + h)), 0, 128, 0));
                 }
-                break;
+            };
+            auto fail = [&]() {
+                *(volatile int *)s_abort = 1;
+                latch_error(PMN_DEVERR_WAIT_TIMEOUT);
+                ok = false;
+            };
+            int t = next_tile(blockIdx.x);
+            if (t < total) {
+                if (mbar_wait(bar_sfr + 8 * stage, phase)) {
+                    tc_fence_after();
+                    copy_sf(stage);
+                } else {
+                    fail();
+                }
             }
-            tc_fence_after();
-            const uint32_t d_tmem = tmem + abuf * BN;
-            for (int ks = 0; ks < ti.nks; ++ks) {
-                ok = warp_wait(bar_sfr + 8 * stage, phase);
-                if (!ok) {
-                    if (lane == 0) {
-                        *(volatile int *)s_abort = 1;
-                        latch_error(PMN_DEVERR_WAIT_TIMEOUT);
-                    }
+            while (ok && t < total) {
+                const Tile ti = get_tile<KIND, TBN>(t, p, s_off, s_cum);
+                if (!mbar_wait(bar_acc_empty + 8 * abuf, aphase ^ 1) || *(volatile int *)s_abort) {
+                    if (!*(volatile int *)s_abort) fail();
+                    ok = false;
                     break;
                 }
-                uint8_t *st = stages + stage * C::STAGE_BYTES;
-                uint8_t *sftA = st + 2 * TILE_BYTES + 2 * C::RAW_BYTES, *sftB = sftA + C::SFT_BYTES;
-                if (lane == 0) {
-                    tc_fence_after();
-                    const uint32_t sfa = tmem + SF_COL0 + stage * C::SF_COLS_STAGE;
-                    const uint32_t sfb = sfa + 4 * C::SFT_CHUNKS;
-                    const uint32_t a_addr = smem_u32(st), b_addr = smem_u32(st + TILE_BYTES);
-#pragma unroll
-                    for (int c = 0; c < C::SFT_CHUNKS; ++c) {
-                        tc_cp_32x128b_warpx4(sfa + 4 * c, smem_desc(smem_u32(sftA + 512 * c), 0, 128, 0));
-                        tc_cp_32x128b_warpx4(sfb + 4 * c, smem_desc(smem_u32(sftB + 512 * c), 0, 128, 0));
-                    }
+                tc_fence_after();
+                const int tn = next_tile(t + gridDim.x);
+                const uint32_t d_tmem = tmem + abuf * TBN;
+                for (int ks = 0; ks < ti.nks; ++ks) {
+                    PMN_TRACE_POINT(3, n_mma);
+                    uint8_t *st = stages + stage * C::STAGE_BYTES;
+                    const uint32_t sfa = tmem + C::SF_COL0 + stage * C::SF_COLS_STAGE;
+                    const uint32_t sfb = sfa + C::SFA_COLS;
+                    const uint32_t a_addr = smem_u32(st), b_addr = smem_u32(st + A_TILE_BYTES);
                     int nk = 4;
                     if (KIND == KIND_MXFP8) {
                         const int64_t left = ti.ke - (ti.kb + (int64_t)ks * 128);
@@ -386,28 +471,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t bd = smem_desc(b_addr + 32 * s, 16, 1024, 2);
                         const uint32_t acc = (ks > 0 || s > 0) ? 1u : 0u;
                         if (KIND == KIND_NVFP4)
-                            mma_nvfp4(d_tmem, ad, bd, make_idesc<KIND>(0), sfa + 4 * s, sfb + 4 * s, acc);
+                            mma_nvfp4(d_tmem, ad, bd, make_idesc<KIND, TBN>(0), sfa + 4 * s, sfb + 4 * C::RB * s, acc);
                         else
-                            mma_mxfp8(d_tmem, ad, bd, make_idesc<KIND>((uint32_t)s), sfa, sfb, acc);
+                            mma_mxfp8(d_tmem, ad, bd, make_idesc<KIND, TBN>((uint32_t)s), sfa, sfb, acc);
                     }
-                    tc_commit(bar_empty + 8 * stage);
+                    if (CS > 1) tc_commit_mc(bar_empty + 8 * stage, cl_mask);
+                    else tc_commit(bar_empty + 8 * stage);
+                    if (ks == ti.nks - 1) tc_commit(bar_acc_full + 8 * abuf);
+                    PMN_TRACE_POINT(4, n_mma);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                    if (ks + 1 < ti.nks || tn < total) {  // look ahead: next stage's scale factors
+                        if (!mbar_wait(bar_sfr + 8 * stage, phase)) {
+                            fail();
+                            break;
+                        }
+                        tc_fence_after();
+                        copy_sf(stage);
+                    }
+                    PMN_TRACE_POINT(5, n_mma);
+                    ++n_mma;
                 }
-                __syncwarp();
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1;
+                if (++abuf == C::ACC) {
+                    abuf = 0;
+                    aphase ^= 1;
                 }
+                t = tn;
             }
-            if (!ok) break;
-            if (lane == 0) tc_commit(bar_acc_full + 8 * abuf);
-            __syncwarp();
-            if (++abuf == 2) {
-                abuf = 0;
-                aphase ^= 1;
-            }
-        }
-        // drain: every tcgen05 operation of this thread has completed
-        if (lane == 0) {
+            // drain: every tcgen05 operation of this thread has completed
             tc_commit(bar_drain);
             (void)mbar_wait(bar_drain, 0, 1000000000ull);
         }
@@ -420,22 +513,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // full 128-byte lines; a slice cut by an expert boundary is written
         // row by row with predicated stores.
         const int q = warp & 3;
-        uint8_t *stg = staging + q * 2 * STAGE_OUT_BYTES;
+        uint8_t *stg = staging + q * EPI_BUFS * STAGE_OUT_BYTES;
         constexpr int CH_PER_STORE = OUT == PMN_OUT_F32 ? 1 : (OUT == PMN_OUT_BF16 ? 2 : 4);
         uint32_t nstore = 0;
         uint32_t abuf = 0, aphase = 0;
+        int n_epi = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const Tile ti = get_tile<KIND>(t, p, s_off, s_cum);
+            const Tile ti = get_tile<KIND, TBN>(t, p, s_off, s_cum);
             const int64_t row = ti.m0 + 32 * q + lane;
             const bool valid = row < ti.row_end;
             if (ti.nks == 0) {
                 // empty contraction: the product is zero
                 if (valid && OUT == PMN_OUT_F32) {
                     float *o = reinterpret_cast<float *>(p.out) + ((int64_t)ti.g * p.m + row) * p.n + ti.n0;
-                    for (int c = 0; c < BN; c += 4) *reinterpret_cast<float4 *>(o + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int c = 0; c < TBN; c += 4) *reinterpret_cast<float4 *>(o + c) = make_float4(0.f, 0.f, 0.f, 0.f);
                 } else if (valid && OUT == PMN_OUT_BF16) {
                     uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + ((int64_t)ti.g * p.m + row) * p.n + ti.n0;
-                    for (int c = 0; c < BN; c += 8) *reinterpret_cast<uint4 *>(o + c) = make_uint4(0u, 0u, 0u, 0u);
+                    for (int c = 0; c < TBN; c += 8) *reinterpret_cast<uint4 *>(o + c) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 continue;
             }
@@ -447,6 +541,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             }
             tc_fence_after();
+            if (q == 0 && lane == 0) PMN_TRACE_POINT(6, n_epi);
             const bool slice_any = ti.m0 + 32 * q < ti.row_end;
             const bool slice_full = ti.m0 + 32 * q + 32 <= ti.row_end;
             float scale = 1.0f;
@@ -455,15 +550,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t sigma = OUT == PMN_OUT_RHT_S2F6 ? rht_sigma(p.seed) : 0u;
             const int64_t obase = p.group_k ? (int64_t)ti.g * p.m : 0;
             const int64_t orow = obase + row;
-            uint32_t sc_word = 0u;
-            for (int c = 0; c < BN / 32; ++c) {
+            uint64_t sc_word = 0u;
+            for (int c = 0; c < TBN / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + abuf * BN + 32 * c, r);
+                tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + abuf * TBN + 32 * c, r);
                 tmem_ld_wait();
-                if (c == BN / 32 - 1) {
+                if (c == TBN / 32 - 1) {
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_acc_empty + 8 * abuf);
+                    if (lane == 0) {
+                        mbar_arrive(bar_acc_empty + 8 * abuf);
+                        if (q == 0) PMN_TRACE_POINT(7, n_epi);
+                    }
                 }
                 if (!slice_any) continue;
                 float v[32];
@@ -497,13 +595,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     chunk[0] = make_uint4(qv[0], qv[1], qv[2], qv[3]);
                     chunk[1] = make_uint4(qv[4], qv[5], qv[6], qv[7]);
                     nch = 2;
-                    sc_word |= sb << (8 * c);
+                    sc_word |= (uint64_t)sb << (8 * c);
                 }
                 const int part = c % CH_PER_STORE;
                 if (slice_full) {
-                    uint8_t *buf = stg + (nstore & 1u) * STAGE_OUT_BYTES;
+                    uint8_t *buf = stg + (nstore % EPI_BUFS) * STAGE_OUT_BYTES;
                     if (part == 0) {
-                        if (lane == 0) bulk_wait_group_read<1>();  // the older store has left this buffer
+                        if (lane == 0) bulk_wait_group_read<EPI_BUFS - 1>();  // this buffer's last store has read it
                         __syncwarp();
                     }
 #pragma unroll
@@ -533,9 +631,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (j < nch) reinterpret_cast<uint4 *>(o)[j] = chunk[j];
                 }
             }
-            if (OUT == PMN_OUT_RHT_S2F6 && valid)
-                *reinterpret_cast<uint32_t *>(p.out_sc + orow * (p.n / 32) + ti.n0 / 32) = sc_word;
-            if (++abuf == 2) {
+            if (OUT == PMN_OUT_RHT_S2F6 && valid) {
+                if (TBN == 256) *reinterpret_cast<uint64_t *>(p.out_sc + orow * (p.n / 32) + ti.n0 / 32) = sc_word;
+                else *reinterpret_cast<uint32_t *>(p.out_sc + orow * (p.n / 32) + ti.n0 / 32) = (uint32_t)sc_word;
+            }
+            ++n_epi;
+            if (++abuf == C::ACC) {
                 abuf = 0;
                 aphase ^= 1;
             }
@@ -546,6 +647,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (CS > 1) cluster_sync();  // no peer still multicasts into, or arrives on, this CTA
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
@@ -573,13 +675,13 @@ EncodeTiledFn encode_fn()
 // 2-D uint8 tensor [rows, width_bytes] with row pitch `pitch` bytes; box
 // box_w x 128 rows.
 bool make_map(CUtensorMap *m, const void *base, uint64_t width_bytes, uint64_t rows, uint64_t pitch, uint32_t box_w,
-              bool swizzle128)
+              bool swizzle128, uint32_t box_rows = 128)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {width_bytes, rows};
     cuuint64_t strides[1] = {pitch};
-    cuuint32_t box[2] = {box_w, 128};
+    cuuint32_t box[2] = {box_w, box_rows};
     cuuint32_t es[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -617,18 +719,82 @@ int num_sms()
     return n;
 }
 
-template <int KIND, int OUT>
-pmn_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &sa, const CUtensorMap &sb,
-                       const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
+// A 2-D uint8 tensor to be loaded by TMA: base, row width and row pitch in
+// bytes, rows.
+struct MapSpec {
+    const void *base;
+    uint64_t width_bytes, rows, pitch;
+};
+
+struct GemmMaps {
+    MapSpec a, b, sa, sb;
+};
+
+#ifndef PMN_GEMM_CLUSTER_MAX
+#define PMN_GEMM_CLUSTER_MAX 1
+#endif
+
+template <int KIND, int OUT, int CS, int TBN>
+pmn_status launch_gemm_cs(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
 {
-    auto kern = block_scaled_gemm_kernel<KIND, OUT>;
-    const int smem = Cfg<KIND>::SMEM_BYTES;
+    using C = Cfg<KIND, TBN>;
+    CUtensorMap a, b, sa, sb;
+    // MXFP8 scale rows: 32-byte boxes only where a K segment may start at any
+    // multiple of 32 (K-grouped, 128-wide tiles); 16 bytes otherwise.
+    const uint32_t raw_w = (KIND == KIND_NVFP4 || TBN == 256 || !args.group_k) ? 16u : 32u;
+    if (!make_map(&a, ms.a.base, ms.a.width_bytes, ms.a.rows, ms.a.pitch, 128, true, BM / CS) ||
+        !make_map(&b, ms.b.base, ms.b.width_bytes, ms.b.rows, ms.b.pitch, 128, true, TBN) ||
+        !make_map(&sa, ms.sa.base, ms.sa.width_bytes, ms.sa.rows, ms.sa.pitch, raw_w, false, BM) ||
+        !make_map(&sb, ms.sb.base, ms.sb.width_bytes, ms.sb.rows, ms.sb.pitch, raw_w, false, TBN))
+        return PMN_ERR_CUDA;
+    auto kern = block_scaled_gemm_kernel<KIND, OUT, CS, TBN>;
+    const int smem = C::SMEM_BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return PMN_ERR_CUDA;
     const int sms = num_sms();
     if (sms <= 0) return PMN_ERR_CUDA;
-    kern<<<sms, NUM_THREADS, smem, s>>>(a, b, sa, sb, o, args);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.gridDim = dim3(sms);
+    if constexpr (CS > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) return PMN_ERR_CUDA;
+        cfg.gridDim = dim3((unsigned)(clusters * CS));
+    }
+    if (cudaLaunchKernelEx(&cfg, kern, a, b, sa, sb, o, args) != cudaSuccess) return PMN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PMN_OK : PMN_ERR_CUDA;
+}
+
+template <int KIND, int OUT, int TBN>
+pmn_status launch_gemm_tbn(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
+{
+    const int64_t nt = args.n / TBN;
+    if constexpr (PMN_GEMM_CLUSTER_MAX >= 4)
+        if (nt % 4 == 0) return launch_gemm_cs<KIND, OUT, 4, TBN>(ms, o, args, s);
+    if constexpr (PMN_GEMM_CLUSTER_MAX >= 2)
+        if (nt % 2 == 0) return launch_gemm_cs<KIND, OUT, 2, TBN>(ms, o, args, s);
+    return launch_gemm_cs<KIND, OUT, 1, TBN>(ms, o, args, s);
+}
+
+// Tile width: 256 columns (N = 256 MMAs, half the operand traffic per
+// output) for M-grouped problems whose N is a multiple of 256; 128 otherwise
+// (K-grouped gradients: short per-expert K, double-buffered accumulators).
+// Cluster size: the largest of 4, 2, 1 (capped by PMN_GEMM_CLUSTER_MAX) that
+// divides the number of N-tiles.
+template <int KIND, int OUT>
+pmn_status launch_gemm(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
+{
+    if (!args.group_k && args.n % 256 == 0) return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);
+    return launch_gemm_tbn<KIND, OUT, 128>(ms, o, args, s);
 }
 
 pmn_status nvfp4_common(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_outer,
@@ -637,7 +803,7 @@ pmn_status nvfp4_common(const uint8_t *a_codes, const uint8_t *a_scales, const f
                         int out_kind, void *out, uint8_t *out_sc, uint64_t seed, void *stream)
 {
     if (num_experts <= 0 || num_experts > MAX_GROUPS || total_rows < 0 || n <= 0 || k <= 0) return PMN_ERR_INVALID_ARG;
-    if (n % BN != 0 || k % 256 != 0 || total_rows >= (int64_t(1) << 31)) return PMN_ERR_INVALID_ARG;
+    if (n % BN_MIN != 0 || k % 256 != 0 || total_rows >= (int64_t(1) << 31)) return PMN_ERR_INVALID_ARG;
     if (!a_codes || !a_scales || !a_outer || !b_codes || !b_scales || !b_outer || !offsets || !out)
         return PMN_ERR_INVALID_ARG;
     if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(b_codes) || !aligned16(b_scales) ||
@@ -645,14 +811,12 @@ pmn_status nvfp4_common(const uint8_t *a_codes, const uint8_t *a_scales, const f
         return PMN_ERR_INVALID_ARG;
     if (out_kind == PMN_OUT_RHT_S2F6 && !out_sc) return PMN_ERR_INVALID_ARG;
     if (total_rows == 0) return PMN_OK;
-    CUtensorMap ma, mb, msa, msb, mo;
+    CUtensorMap mo;
     const uint64_t brows = (uint64_t)num_experts * (uint64_t)n;
     if (!make_out_map(&mo, out, out_kind, n, total_rows)) return PMN_ERR_CUDA;
-    if (!make_map(&ma, a_codes, k / 2, total_rows, k / 2, 128, true) ||
-        !make_map(&mb, b_codes, k / 2, brows, k / 2, 128, true) ||
-        !make_map(&msa, a_scales, k / 16, total_rows, k / 16, 16, false) ||
-        !make_map(&msb, b_scales, k / 16, brows, k / 16, 16, false))
-        return PMN_ERR_CUDA;
+    const uint64_t kb = (uint64_t)k / 2, ks = (uint64_t)k / 16;
+    const GemmMaps ms{{a_codes, kb, (uint64_t)total_rows, kb}, {b_codes, kb, brows, kb},
+                      {a_scales, ks, (uint64_t)total_rows, ks}, {b_scales, ks, brows, ks}};
     GemmArgs args{};
     args.offsets = offsets;
     args.groups = num_experts;
@@ -668,9 +832,9 @@ pmn_status nvfp4_common(const uint8_t *a_codes, const uint8_t *a_scales, const f
     args.seed = seed;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (out_kind) {
-        case PMN_OUT_BF16: return launch_gemm<KIND_NVFP4, PMN_OUT_BF16>(ma, mb, msa, msb, mo, args, s);
-        case PMN_OUT_F32: return launch_gemm<KIND_NVFP4, PMN_OUT_F32>(ma, mb, msa, msb, mo, args, s);
-        case PMN_OUT_RHT_S2F6: return launch_gemm<KIND_NVFP4, PMN_OUT_RHT_S2F6>(ma, mb, msa, msb, mo, args, s);
+        case PMN_OUT_BF16: return launch_gemm<KIND_NVFP4, PMN_OUT_BF16>(ms, mo, args, s);
+        case PMN_OUT_F32: return launch_gemm<KIND_NVFP4, PMN_OUT_F32>(ms, mo, args, s);
+        case PMN_OUT_RHT_S2F6: return launch_gemm<KIND_NVFP4, PMN_OUT_RHT_S2F6>(ms, mo, args, s);
         default: return PMN_ERR_INVALID_ARG;
     }
 }
@@ -738,7 +902,7 @@ extern "C" pmn_status pmn_gemm_mxfp8(const uint8_t *a, const uint8_t *a_scales, 
     if (num_groups <= 0 || num_groups > MAX_GROUPS || m < 0 || n <= 0 || k < 0) return PMN_ERR_INVALID_ARG;
     if (group_mode != PMN_GROUP_M && group_mode != PMN_GROUP_K) return PMN_ERR_INVALID_ARG;
     if (out_kind != PMN_OUT_BF16 && out_kind != PMN_OUT_F32) return PMN_ERR_INVALID_ARG;
-    if (n % BN != 0 || m >= (int64_t(1) << 31) || k >= (int64_t(1) << 31)) return PMN_ERR_INVALID_ARG;
+    if (n % BN_MIN != 0 || m >= (int64_t(1) << 31) || k >= (int64_t(1) << 31)) return PMN_ERR_INVALID_ARG;
     if (group_mode == PMN_GROUP_M && (k % 128 != 0 || (k / 32) % 16 != 0)) return PMN_ERR_INVALID_ARG;
     if (group_mode == PMN_GROUP_K && (m % BM != 0 || k % 32 != 0 || (k / 32) % 16 != 0)) return PMN_ERR_INVALID_ARG;
     if (!a || !a_scales || !b || !b_scales || !offsets || !out) return PMN_ERR_INVALID_ARG;
@@ -748,14 +912,13 @@ extern "C" pmn_status pmn_gemm_mxfp8(const uint8_t *a, const uint8_t *a_scales, 
     if (m == 0) return PMN_OK;
     if (group_mode == PMN_GROUP_M && k == 0) return PMN_ERR_INVALID_ARG;
     const uint64_t brows = group_mode == PMN_GROUP_M ? (uint64_t)num_groups * (uint64_t)n : (uint64_t)n;
-    CUtensorMap ma, mb, msa, msb, mo;
+    CUtensorMap mo;
     if (k == 0) return PMN_ERR_INVALID_ARG;
     const uint64_t orows = group_mode == PMN_GROUP_M ? (uint64_t)m : (uint64_t)num_groups * (uint64_t)m;
     if (!make_out_map(&mo, out, out_kind, n, orows)) return PMN_ERR_CUDA;
-    if (!make_map(&ma, a, k, m, k, 128, true) || !make_map(&mb, b, k, brows, k, 128, true) ||
-        !make_map(&msa, a_scales, k / 32, m, k / 32, 32, false) ||
-        !make_map(&msb, b_scales, k / 32, brows, k / 32, 32, false))
-        return PMN_ERR_CUDA;
+    const uint64_t uk = (uint64_t)k, ks = (uint64_t)k / 32;
+    const GemmMaps ms{{a, uk, (uint64_t)m, uk}, {b, uk, brows, uk}, {a_scales, ks, (uint64_t)m, ks},
+                      {b_scales, ks, brows, ks}};
     GemmArgs args{};
     args.offsets = offsets;
     args.groups = num_groups;
@@ -766,6 +929,6 @@ extern "C" pmn_status pmn_gemm_mxfp8(const uint8_t *a, const uint8_t *a_scales, 
     args.k = k;
     args.out = out;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (out_kind == PMN_OUT_BF16) return launch_gemm<KIND_MXFP8, PMN_OUT_BF16>(ma, mb, msa, msb, mo, args, s);
-    return launch_gemm<KIND_MXFP8, PMN_OUT_F32>(ma, mb, msa, msb, mo, args, s);
+    if (out_kind == PMN_OUT_BF16) return launch_gemm<KIND_MXFP8, PMN_OUT_BF16>(ms, mo, args, s);
+    return launch_gemm<KIND_MXFP8, PMN_OUT_F32>(ms, mo, args, s);
 }
