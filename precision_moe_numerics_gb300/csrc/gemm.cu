@@ -88,12 +88,13 @@ struct Cfg {
     static constexpr int STAGE_RAW = A_TILE_BYTES + B_TILE_BYTES + RAW_A + RAW_B + SFT_A + SFT_B;
     static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
     static constexpr int STAGES = TBN == 256 ? 3 : PMN_GEMM_STAGES;
+    static constexpr int EPI = EPI_BUFS;  // epilogue staging buffers per warp
     static constexpr int ACC = TBN == 256 ? 1 : 2;
     static constexpr uint32_t SF_COL0 = ACC * TBN;  // scale factors live after the accumulators
     static constexpr uint32_t SFA_COLS = 4 * SFT_CHUNKS, SFB_COLS = 4 * SFT_CHUNKS * RB;
     static constexpr uint32_t SF_COLS_STAGE = SFA_COLS + SFB_COLS;
     static constexpr int SMEM_BYTES =
-        1024 + STAGES * STAGE_BYTES + 4 * EPI_BUFS * STAGE_OUT_BYTES + 1024 + 2 * (MAX_GROUPS + 1) * 4;
+        1024 + STAGES * STAGE_BYTES + 4 * EPI * STAGE_OUT_BYTES + 1024 + 2 * (MAX_GROUPS + 1) * 4;
     static_assert(SF_COL0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -188,8 +189,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
-    uint8_t *staging = smem + STAGES * C::STAGE_BYTES;  // epilogue: 4 warps x EPI_BUFS x 4 KB
-    uint64_t *bars = reinterpret_cast<uint64_t *>(staging + 4 * EPI_BUFS * STAGE_OUT_BYTES);
+    uint8_t *staging = smem + STAGES * C::STAGE_BYTES;  // epilogue: 4 warps x EPI x 4 KB
+    uint64_t *bars = reinterpret_cast<uint64_t *>(staging + 4 * C::EPI * STAGE_OUT_BYTES);
     // barrier slots: full[S], empty[S], sf_ready[S], acc_full[2], acc_empty[2], drain
     const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + 8 * STAGES;
     const uint32_t bar_sfr = bar_empty + 8 * STAGES;  // scale factors re-laid for the stage
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 5);
     int *s_abort = reinterpret_cast<int *>(tmem_slot + 1);
     int *s_total = s_abort + 1;
-    int *s_off = reinterpret_cast<int *>(staging + 4 * EPI_BUFS * STAGE_OUT_BYTES + 1024);
+    int *s_off = reinterpret_cast<int *>(staging + 4 * C::EPI * STAGE_OUT_BYTES + 1024);
     int *s_cum = s_off + (MAX_GROUPS + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -513,7 +514,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // full 128-byte lines; a slice cut by an expert boundary is written
         // row by row with predicated stores.
         const int q = warp & 3;
-        uint8_t *stg = staging + q * EPI_BUFS * STAGE_OUT_BYTES;
+        uint8_t *stg = staging + q * C::EPI * STAGE_OUT_BYTES;
         constexpr int CH_PER_STORE = OUT == PMN_OUT_F32 ? 1 : (OUT == PMN_OUT_BF16 ? 2 : 4);
         uint32_t nstore = 0;
         uint32_t abuf = 0, aphase = 0;
@@ -551,16 +552,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int64_t obase = p.group_k ? (int64_t)ti.g * p.m : 0;
             const int64_t orow = obase + row;
             uint64_t sc_word = 0u;
+            // 128-wide tiles: read the whole accumulator slice (4 x 32 columns)
+            // before converting, so the accumulator is released to the next
+            // tile's MMAs without waiting for this tile's stores to drain.
+            constexpr int PRELOAD = TBN == 128 ? TBN / 32 : 1;
+            uint32_t pre[PRELOAD][32];
+            if (PRELOAD > 1) {
+#pragma unroll
+                for (int c = 0; c < PRELOAD; ++c)
+                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + abuf * TBN + 32 * c, pre[c]);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar_acc_empty + 8 * abuf);
+                    if (q == 0) PMN_TRACE_POINT(7, n_epi);
+                }
+            }
+#pragma unroll(PRELOAD > 1 ? TBN / 32 : 1)
             for (int c = 0; c < TBN / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + abuf * TBN + 32 * c, r);
-                tmem_ld_wait();
-                if (c == TBN / 32 - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(bar_acc_empty + 8 * abuf);
-                        if (q == 0) PMN_TRACE_POINT(7, n_epi);
+                if (PRELOAD > 1) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = pre[PRELOAD > 1 ? c : 0][j];
+                } else {
+                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + abuf * TBN + 32 * c, r);
+                    tmem_ld_wait();
+                    if (c == TBN / 32 - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(bar_acc_empty + 8 * abuf);
+                            if (q == 0) PMN_TRACE_POINT(7, n_epi);
+                        }
                     }
                 }
                 if (!slice_any) continue;
@@ -599,9 +623,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 const int part = c % CH_PER_STORE;
                 if (slice_full) {
-                    uint8_t *buf = stg + (nstore % EPI_BUFS) * STAGE_OUT_BYTES;
+                    uint8_t *buf = stg + (nstore % C::EPI) * STAGE_OUT_BYTES;
                     if (part == 0) {
-                        if (lane == 0) bulk_wait_group_read<EPI_BUFS - 1>();  // this buffer's last store has read it
+                        if (lane == 0) bulk_wait_group_read<C::EPI - 1>();  // this buffer's last store has read it
                         __syncwarp();
                     }
 #pragma unroll

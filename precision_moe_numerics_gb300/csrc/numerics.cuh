@@ -23,20 +23,32 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t code)
     return __uint_as_float(bits | ((code & 8u) << 28));
 }
 
-// Two E2M1 codes (one byte; bits 3:0 = element 0) decoded by the hardware to
-// f16x2 and multiplied by an E4M3 scale held as f16x2: e2m1 (2 significant
-// bits) x E4M3 (4 bits) is exact in f16 (range 2^-10 .. 2688).  Returns the two
-// exact products as binary32 (element 0 in .x).
-__device__ __forceinline__ float2 e2m1x2_mul_scale(uint32_t byte, uint32_t scale_h2)
+// Two E2M1 codes (one byte; bits 3:0 = element 0, in the low half) decoded
+// by the hardware to f16x2 and multiplied by an E4M3 scale held as f16x2:
+// e2m1 (2 significant bits) x E4M3 (4 bits) is exact in f16 (range 2^-10 ..
+// 2688).  Returns the two exact products as f16x2 bits.
+__device__ __forceinline__ uint32_t e2m1x2_mul_h2(uint32_t byte, uint32_t scale_h2)
 {
     uint32_t h2, p;
     const uint16_t b16 = (uint16_t)(byte & 0xFFu);
     asm("{\n\t.reg .b8 lo, hi;\n\tmov.b16 {lo, hi}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, lo;\n\t}" : "=r"(h2) : "h"(b16));
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(p) : "r"(h2), "r"(scale_h2));
-    float lo, hi;
-    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-        : "=f"(lo), "=f"(hi) : "r"(p));
-    return make_float2(lo, hi);
+    return p;
+}
+
+// The low / high f16 of an f16x2 word as binary32 (exact).
+__device__ __forceinline__ float h2_lo_to_f32(uint32_t h2)
+{
+    float f;
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %1;\n\tcvt.f32.f16 %0, a;\n\t}" : "=f"(f) : "r"(h2));
+    return f;
+}
+
+__device__ __forceinline__ float h2_hi_to_f32(uint32_t h2)
+{
+    float f;
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %1;\n\tcvt.f32.f16 %0, b;\n\t}" : "=f"(f) : "r"(h2));
+    return f;
 }
 
 // E4M3 byte -> the same value twice as f16x2 (exact: E4M3 is a subset of f16).

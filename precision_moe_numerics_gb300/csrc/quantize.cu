@@ -337,141 +337,138 @@ __global__ void __launch_bounds__(256) mxfp8_quant_transposed_kernel(const uint1
 }
 
 // ------------------------------------------------------------------ requant [SR]
-// Persistent kernel over tiles of 128 input rows x 128 input cols.  Phase 1:
-// dequantise d = (dec(code) * dec(S)) * g in binary32 into shared memory,
-// stored transposed (output row c holds d[r, c] for the tile's 128 rows r, in
-// four 32-blocks each padded to 36 floats so both phases are conflict-free).
-// Phase 2: task (c, rb) forms the 32-block of output row c, its E8M0 exponent
-// e, y = d * 2^-e (exact) and the E4M3 bytes -- stochastic rounding by the
-// hardware convert fed with Philox words (one Philox call per 16 elements) or
-// round-to-nearest-even.  Four consecutive lanes write one 128-byte line.
-// The next tile's codes are loaded into registers before phase 2 so its HBM
-// latency overlaps the current tile's arithmetic.
+// One CTA per tile of 128 input rows x 128 input cols.
+// Phase 1: each thread decodes an 8-row x 8-column block: code * S is exact
+//   in f16 (E2M1 x E4M3, 2^-10 .. 2688), formed by the hardware E2M1 decode
+//   and a packed f16 multiply, transposed in registers and written as 128-bit
+//   rows of the transposed tile cS[c][r] (f16, chunk index XOR-swizzled so
+//   both phases are bank-conflict free).
+// Phase 2: task (c, rb) forms the 32-block of output row c.  The canonical
+//   dequantised value is d = (code * S) * g (one rounding); with the block's
+//   E8M0 exponent e, y = d * 2^-e equals RN(code * S * (g * 2^-e)) because a
+//   power-of-two scaling commutes with rounding -- so y takes one multiply.
+//   For a per-expert g the block maximum is fl(max|code * S| * g) (rounding
+//   is monotone), found on the f16 bit patterns with packed integer max.
+//   E4M3 bytes: hardware stochastic rounding fed with Philox words (one
+//   Philox call per 16 elements), or round-to-nearest-even.
 constexpr int RQ_T = 128;
-constexpr int RQ_BLK = 36;                // padded 32-block (floats)
-constexpr int RQ_ROW = 4 * RQ_BLK;        // one output row of the tile (floats)
 
-struct RqRegs {
-    uint4 q0, q1;
-    uint32_t sw;
-    float g;
-    bool ok;
-};
-
-__device__ __forceinline__ RqRegs requant_load(const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales,
-                                               const float *__restrict__ outer, int outer_per_row, int64_t rows,
-                                               int64_t cols, int64_t b, int64_t r0, int64_t c0, int r, int h)
+__device__ __forceinline__ int rq_chunk(int c, int logical)  // 8-row chunk of row c
 {
-    RqRegs x;
-    const int64_t src = b * rows + r0 + r;
-    x.ok = (r0 + r < rows) && (c0 + h * 64 < cols);
-    x.q0 = make_uint4(0u, 0u, 0u, 0u);
-    x.q1 = x.q0;
-    x.sw = 0u;
-    x.g = 0.0f;
-    if (x.ok) {
-        x.g = outer_per_row ? __ldg(outer + src) : __ldg(outer + b);
-        const uint8_t *pc = codes + src * (cols / 2) + (c0 + h * 64) / 2;
-        x.q0 = __ldg(reinterpret_cast<const uint4 *>(pc));
-        x.q1 = __ldg(reinterpret_cast<const uint4 *>(pc + 16));
-        x.sw = __ldg(reinterpret_cast<const uint32_t *>(scales + src * (cols / 16) + (c0 + h * 64) / 16));
-    }
-    return x;
+    return c * 16 + (logical ^ ((c ^ (c >> 3)) & 7));
 }
 
-__global__ void __launch_bounds__(256, 3) requant_transpose_kernel(
+__global__ void __launch_bounds__(256) requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, const float *__restrict__ outer,
-    int outer_per_row, int64_t batch, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, int stochastic,
+    int outer_per_row, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, int stochastic,
     uint8_t *__restrict__ out, uint8_t *__restrict__ out_sc)
 {
-    extern __shared__ float dT[];  // [RQ_T (c)][4 blocks][RQ_BLK]
-    const int64_t tiles_c = (cols + RQ_T - 1) / RQ_T, tiles_r = (rows + RQ_T - 1) / RQ_T;
-    const int64_t ntiles = batch * tiles_r * tiles_c;
-    const int r = threadIdx.x & 127, h = threadIdx.x >> 7;
-    auto coords = [&](int64_t t, int64_t &b, int64_t &r0, int64_t &c0) {
-        c0 = (t % tiles_c) * RQ_T;
-        const int64_t u = t / tiles_c;
-        r0 = (u % tiles_r) * RQ_T;
-        b = u / tiles_r;
-    };
-    int64_t t = blockIdx.x;
-    if (t >= ntiles) return;
-    int64_t b, r0, c0;
-    coords(t, b, r0, c0);
-    RqRegs cur = requant_load(codes, scales, outer, outer_per_row, rows, cols, b, r0, c0, r, h);
-    for (; t < ntiles; t += gridDim.x) {
-        // phase 1: row r of the tile, 64 columns (half h)
-        {
-            const uint32_t cw[8] = {cur.q0.x, cur.q0.y, cur.q0.z, cur.q0.w, cur.q1.x, cur.q1.y, cur.q1.z, cur.q1.w};
-            float *dst = dT + (h * 64) * RQ_ROW + (r >> 5) * RQ_BLK + (r & 31);
+    __shared__ __align__(16) uint4 cS[RQ_T * 16];  // [c][16 chunks of 8 rows] f16
+    __shared__ __align__(16) float gS[RQ_T];        // per-row outer scales (activations)
+    const int64_t b = blockIdx.z;
+    const int64_t r0 = (int64_t)blockIdx.y * RQ_T, c0 = (int64_t)blockIdx.x * RQ_T;
+    const int64_t cols2 = cols / 2, cols16 = cols / 16;
+    const float g_batch = outer_per_row ? 0.0f : __ldg(outer + b);
+    // ---- phase 1: rows 8rg .. 8rg+7, columns 8cg .. 8cg+7
+    {
+        const int cg = threadIdx.x & 15, rg = threadIdx.x >> 4;
+        const bool col_ok = c0 + 8 * cg < cols;
+        uint32_t h2[8][4];  // row i: f16x2 pairs of columns (0,1) (2,3) (4,5) (6,7)
 #pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-                const uint32_t dS2 = e4m3_to_h2((cur.sw >> (8 * blk)) & 0xFFu);
-#pragma unroll
-                for (int j = 0; j < 16; j += 2) {
-                    const int jj = blk * 16 + j;
-                    const uint32_t byte = (cw[jj >> 3] >> (4 * (jj & 7))) & 0xFFu;
-                    const float2 cs = e2m1x2_mul_scale(byte, dS2);  // exact code * scale
-                    dst[jj * RQ_ROW] = cur.ok ? __fmul_rn(cs.x, cur.g) : 0.0f;
-                    dst[(jj + 1) * RQ_ROW] = cur.ok ? __fmul_rn(cs.y, cur.g) : 0.0f;
-                }
+        for (int i = 0; i < 8; ++i) {
+            const int64_t r = r0 + 8 * rg + i;
+            const int64_t src = b * rows + r;
+            uint32_t word = 0u, sbyte = 0u;
+            if (col_ok && r < rows) {
+                word = __ldg(reinterpret_cast<const uint32_t *>(codes + src * cols2 + (c0 + 8 * cg) / 2));
+                sbyte = __ldg(scales + src * cols16 + (c0 + 8 * cg) / 16);
             }
+            if (outer_per_row && cg == 0) gS[8 * rg + i] = r < rows ? __ldg(outer + src) : 0.0f;
+            const uint32_t dS2 = e4m3_to_h2(sbyte);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) h2[i][k] = e2m1x2_mul_h2((word >> (8 * k)) & 0xFFu, dS2);
         }
-        __syncthreads();
-        // prefetch the next tile while this one is rounded
-        int64_t nb = 0, nr0 = 0, nc0 = 0;
-        const int64_t tn = t + gridDim.x;
-        RqRegs nxt;
-        nxt.ok = false;
-        if (tn < ntiles) {
-            coords(tn, nb, nr0, nc0);
-            nxt = requant_load(codes, scales, outer, outer_per_row, rows, cols, nb, nr0, nc0, r, h);
+        // transpose: column j gets rows 0..7 as four f16x2
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t lo[4], hi[4];  // columns 2k and 2k+1
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                lo[i] = __byte_perm(h2[2 * i][k], h2[2 * i + 1][k], 0x5410);
+                hi[i] = __byte_perm(h2[2 * i][k], h2[2 * i + 1][k], 0x7632);
+            }
+            const int cl = 8 * cg + 2 * k;
+            cS[rq_chunk(cl, rg)] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            cS[rq_chunk(cl + 1, rg)] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         }
-        // phase 2: 128 output rows x 4 row-blocks = 512 tasks, 2 per thread
+    }
+    __syncthreads();
+    // ---- phase 2: 128 output rows x 4 row-blocks = 512 tasks, 2 per thread;
+    // four consecutive lanes cover one 128-byte line of an output row.
 #pragma unroll 1
-        for (int task = threadIdx.x; task < RQ_T * 4; task += blockDim.x) {
-            const int c = task >> 2, rb = task & 3;
-            const int64_t oc = c0 + c, orow0 = r0 + rb * 32;
-            if (oc >= cols || orow0 >= rows) continue;
-            float v[32];
-            const float4 *src = reinterpret_cast<const float4 *>(dT + c * RQ_ROW + rb * RQ_BLK);
-            float amax = 0.0f;
+    for (int task = threadIdx.x; task < RQ_T * 4; task += blockDim.x) {
+        const int c = task >> 2, rb = task & 3;
+        const int64_t oc = c0 + c, orow0 = r0 + rb * 32;
+        if (oc >= cols || orow0 >= rows) continue;
+        uint32_t hw[16];  // 32 f16 values: rows rb*32 .. rb*32+31
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float4 f = src[k];
-                v[4 * k] = f.x;
-                v[4 * k + 1] = f.y;
-                v[4 * k + 2] = f.z;
-                v[4 * k + 3] = f.w;
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+        for (int k = 0; k < 4; ++k) {
+            const uint4 u = cS[rq_chunk(c, 4 * rb + k)];
+            hw[4 * k] = u.x;
+            hw[4 * k + 1] = u.y;
+            hw[4 * k + 2] = u.z;
+            hw[4 * k + 3] = u.w;
+        }
+        float y[32];
+        int e;
+        if (!outer_per_row) {
+            uint32_t m = 0u;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) m = __vmaxu2(m, hw[j] & 0x7FFF7FFFu);
+            const float amax_cs = fmaxf(h2_lo_to_f32(m), h2_hi_to_f32(m));
+            e = mx_exponent_448(__fmul_rn(amax_cs, g_batch));
+            // exact; an all-zero block keeps its signed zeros (g * 2^127 could overflow)
+            const float gp = amax_cs == 0.0f ? 0.0f : __fmul_rn(g_batch, exp2_neg(e));
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                y[2 * j] = __fmul_rn(h2_lo_to_f32(hw[j]), gp);
+                y[2 * j + 1] = __fmul_rn(h2_hi_to_f32(hw[j]), gp);
             }
-            const int e = mx_exponent_448(amax);
+        } else {
+            float amax = 0.0f;
+            const float4 *gp4 = reinterpret_cast<const float4 *>(gS + rb * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 g4 = gp4[q];
+                y[4 * q] = __fmul_rn(h2_lo_to_f32(hw[2 * q]), g4.x);
+                y[4 * q + 1] = __fmul_rn(h2_hi_to_f32(hw[2 * q]), g4.y);
+                y[4 * q + 2] = __fmul_rn(h2_lo_to_f32(hw[2 * q + 1]), g4.z);
+                y[4 * q + 3] = __fmul_rn(h2_hi_to_f32(hw[2 * q + 1]), g4.w);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(y[4 * q]), fabsf(y[4 * q + 1])),
+                                         fmaxf(fabsf(y[4 * q + 2]), fabsf(y[4 * q + 3]))));
+            }
+            e = mx_exponent_448(amax);
             const float sc = exp2_neg(e);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(v[j], sc);  // exact scaling
-            const int64_t i0 = (b * cols + oc) * rows + orow0;      // output index, multiple of 32
-            uint32_t o[8];
-            if (stochastic) {
-                const uint4 wa = sr_words16(seed, tag, (uint64_t)i0 >> 4);
-                const uint4 wb = sr_words16(seed, tag, ((uint64_t)i0 >> 4) + 1);
-                const uint32_t wd[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-                for (int k = 0; k < 8; ++k) o[k] = cvt_e4m3x4_rs(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], wd[k]);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    o[k] = cvt_e4m3x2_rn(v[4 * k], v[4 * k + 1]) | (cvt_e4m3x2_rn(v[4 * k + 2], v[4 * k + 3]) << 16);
-            }
-            uint4 *po = reinterpret_cast<uint4 *>(out + i0);
-            po[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            po[1] = make_uint4(o[4], o[5], o[6], o[7]);
-            out_sc[(b * cols + oc) * (rows / 32) + orow0 / 32] = (uint8_t)(e + 127);
+            for (int j = 0; j < 32; ++j) y[j] = __fmul_rn(y[j], sc);  // exact
         }
-        __syncthreads();
-        cur = nxt;
-        b = nb;
-        r0 = nr0;
-        c0 = nc0;
+        const int64_t i0 = (b * cols + oc) * rows + orow0;  // output index, multiple of 32
+        uint32_t o[8];
+        if (stochastic) {
+            const uint4 wa = sr_words16(seed, tag, (uint64_t)i0 >> 4);
+            const uint4 wb = sr_words16(seed, tag, ((uint64_t)i0 >> 4) + 1);
+            const uint32_t wd[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] = cvt_e4m3x4_rs(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3], wd[k]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                o[k] = cvt_e4m3x2_rn(y[4 * k], y[4 * k + 1]) | (cvt_e4m3x2_rn(y[4 * k + 2], y[4 * k + 3]) << 16);
+        }
+        uint4 *po = reinterpret_cast<uint4 *>(out + i0);
+        po[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        po[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        out_sc[(b * cols + oc) * (rows / 32) + orow0 / 32] = (uint8_t)(e + 127);
     }
 }
 
@@ -595,20 +592,10 @@ extern "C" pmn_status pmn_requant_transpose_sr_mxfp8(const uint8_t *codes, const
     if (!aligned16(codes) || !aligned16(scales) || !aligned16(out) || ((uintptr_t)outer & 3u)) return PMN_ERR_INVALID_ARG;
     if (batch == 0 || rows == 0 || cols == 0) return PMN_OK;
     if ((cols / 16) % 4 != 0) return PMN_ERR_INVALID_ARG;  // 4-byte scale words per 64 columns
-    const int smem = RQ_T * RQ_ROW * (int)sizeof(float);
-    if (cudaFuncSetAttribute(requant_transpose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-        return PMN_ERR_CUDA;
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_transpose_kernel, 256, smem) != cudaSuccess)
-        return PMN_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t ntiles = batch * ((rows + RQ_T - 1) / RQ_T) * ((cols + RQ_T - 1) / RQ_T);
-    const int64_t grid = std::min<int64_t>(ntiles, (int64_t)sms * std::max(per_sm, 1));
-    requant_transpose_kernel<<<(unsigned)grid, 256, smem, s>>>(codes, scales, outer, outer_mode == PMN_OUTER_PER_ROW,
-                                                               batch, rows, cols, seed, tag, rounding == PMN_ROUND_SR,
-                                                               out, out_scales);
+    dim3 grid((unsigned)((cols + RQ_T - 1) / RQ_T), (unsigned)((rows + RQ_T - 1) / RQ_T), (unsigned)batch);
+    requant_transpose_kernel<<<grid, 256, 0, s>>>(codes, scales, outer, outer_mode == PMN_OUTER_PER_ROW, rows, cols,
+                                                   seed, tag, rounding == PMN_ROUND_SR, out, out_scales);
     return launch_status();
 }
 
