@@ -181,28 +181,42 @@ __global__ void __launch_bounds__(256) nvfp4_quant_rows_kernel(
 }
 
 // PER_GROUP quantisation once the group amax is known: every 16-block is
-// independent, so one thread per block streams x (32 bytes in, 9 bytes out).
+// independent, so threads stream x; each thread takes two blocks (at bi and
+// bi + stride) and issues all four 16-byte loads before any arithmetic.
 __global__ void __launch_bounds__(256) nvfp4_quant_blocks_kernel(const uint16_t *__restrict__ x, int64_t nblocks,
                                                                  int64_t blocks_per_group,
                                                                  const uint32_t *__restrict__ group_amax,
                                                                  int four_over_six, uint8_t *__restrict__ codes,
                                                                  uint8_t *__restrict__ scales)
 {
-    const int64_t bi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (bi >= nblocks) return;
-    const uint4 *p = reinterpret_cast<const uint4 *>(x + bi * 16);
-    const uint4 v0 = __ldg(p), v1 = __ldg(p + 1);
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float xf[16];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t b0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t bis[2] = {b0, b0 + stride};
+    uint4 v[2][2];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-        xf[2 * t] = bf16_lo(w[t]);
-        xf[2 * t + 1] = bf16_hi(w[t]);
+    for (int u = 0; u < 2; ++u) {
+        if (bis[u] < nblocks) {
+            const uint4 *p = reinterpret_cast<const uint4 *>(x + bis[u] * 16);
+            v[u][0] = __ldg(p);
+            v[u][1] = __ldg(p + 1);
+        }
     }
-    const float g = outer_from_amax(__uint_as_float(__ldg(group_amax + bi / blocks_per_group)), four_over_six != 0);
-    const BlockQ q = quant_block(xf, g, four_over_six != 0);
-    *reinterpret_cast<uint2 *>(codes + bi * 8) = make_uint2(q.w0, q.w1);
-    scales[bi] = (uint8_t)q.sbyte;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int64_t bi = bis[u];
+        if (bi >= nblocks) continue;
+        const uint32_t w[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+        float xf[16];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            xf[2 * t] = bf16_lo(w[t]);
+            xf[2 * t + 1] = bf16_hi(w[t]);
+        }
+        const float g = outer_from_amax(__uint_as_float(__ldg(group_amax + bi / blocks_per_group)), four_over_six != 0);
+        const BlockQ q = quant_block(xf, g, four_over_six != 0);
+        *reinterpret_cast<uint2 *>(codes + bi * 8) = make_uint2(q.w0, q.w1);
+        scales[bi] = (uint8_t)q.sbyte;
+    }
 }
 
 // amax of each group of rows (contiguous: ldx == cols), as binary32 bits,
@@ -341,8 +355,8 @@ __global__ void __launch_bounds__(256) mxfp8_quant_transposed_kernel(const uint1
 // Phase 1: each thread decodes an 8-row x 8-column block: code * S is exact
 //   in f16 (E2M1 x E4M3, 2^-10 .. 2688), formed by the hardware E2M1 decode
 //   and a packed f16 multiply, transposed in registers and written as 128-bit
-//   rows of the transposed tile cS[c][r] (f16, chunk index XOR-swizzled so
-//   both phases are bank-conflict free).
+//   rows of the transposed tile cS[c][r] (f16, chunk index swizzled so both
+//   phases are bank-conflict free).
 // Phase 2: task (c, rb) forms the 32-block of output row c.  The canonical
 //   dequantised value is d = (code * S) * g (one rounding); with the block's
 //   E8M0 exponent e, y = d * 2^-e equals RN(code * S * (g * 2^-e)) because a
@@ -353,10 +367,19 @@ __global__ void __launch_bounds__(256) mxfp8_quant_transposed_kernel(const uint1
 //   Philox call per 16 elements), or round-to-nearest-even.
 constexpr int RQ_T = 128;
 
-__device__ __forceinline__ int rq_chunk(int c, int logical)  // 8-row chunk of row c
+// 16-byte chunk `logical` (rows 8*logical ..) of transposed row c.  A 128-bit
+// shared access is served per quarter-warp, so 8 lanes must land in 8 distinct
+// 16-byte bank groups (index mod 8).  Phase 1 quarters vary c over 8 columns
+// 8 apart (XOR with c ^ c>>3 spreads them); phase 2 quarters take 2 adjacent
+// c times logical chunks k, 4+k, 8+k, 12+k: bit 3 of `logical` is folded into
+// bit 1 so those four differ mod 8, and adjacent c differ in bit 0.
+__device__ __forceinline__ int rq_chunk(int c, int logical)
 {
-    return c * 16 + (logical ^ ((c ^ (c >> 3)) & 7));
+    return c * 16 + (logical ^ ((c ^ (c >> 3)) & 7) ^ ((logical >> 3) << 1));
 }
+// per-row outer scales, 4 floats of padding per 32 rows so the four row-blocks
+// of a quarter-warp read different banks
+__device__ __forceinline__ int rq_gidx(int r) { return r + ((r >> 5) << 2); }
 
 __global__ void __launch_bounds__(256) requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, const float *__restrict__ outer,
@@ -364,7 +387,7 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
     uint8_t *__restrict__ out, uint8_t *__restrict__ out_sc)
 {
     __shared__ __align__(16) uint4 cS[RQ_T * 16];  // [c][16 chunks of 8 rows] f16
-    __shared__ __align__(16) float gS[RQ_T];        // per-row outer scales (activations)
+    __shared__ __align__(16) float gS[RQ_T + RQ_T / 8];  // per-row outer scales (activations)
     const int64_t b = blockIdx.z;
     const int64_t r0 = (int64_t)blockIdx.y * RQ_T, c0 = (int64_t)blockIdx.x * RQ_T;
     const int64_t cols2 = cols / 2, cols16 = cols / 16;
@@ -383,7 +406,7 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
                 word = __ldg(reinterpret_cast<const uint32_t *>(codes + src * cols2 + (c0 + 8 * cg) / 2));
                 sbyte = __ldg(scales + src * cols16 + (c0 + 8 * cg) / 16);
             }
-            if (outer_per_row && cg == 0) gS[8 * rg + i] = r < rows ? __ldg(outer + src) : 0.0f;
+            if (outer_per_row && cg == 0) gS[rq_gidx(8 * rg + i)] = r < rows ? __ldg(outer + src) : 0.0f;
             const uint32_t dS2 = e4m3_to_h2(sbyte);
 #pragma unroll
             for (int k = 0; k < 4; ++k) h2[i][k] = e2m1x2_mul_h2((word >> (8 * k)) & 0xFFu, dS2);
@@ -436,7 +459,7 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
             }
         } else {
             float amax = 0.0f;
-            const float4 *gp4 = reinterpret_cast<const float4 *>(gS + rb * 32);
+            const float4 *gp4 = reinterpret_cast<const float4 *>(gS + rq_gidx(rb * 32));
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const float4 g4 = gp4[q];
@@ -535,7 +558,7 @@ extern "C" pmn_status pmn_nvfp4_quantize(const void *x, int64_t rows, int64_t co
     }
     if (outer_mode == PMN_OUTER_PER_GROUP) {
         const int64_t nblocks = rows * (cols / 16);
-        nvfp4_quant_blocks_kernel<<<(unsigned)((nblocks + 255) / 256), 256, 0, s>>>(
+        nvfp4_quant_blocks_kernel<<<(unsigned)((nblocks + 511) / 512), 256, 0, s>>>(
             xb, nblocks, rows_per_group * (cols / 16), gam, four_over_six, codes, scales);
         if (launch_status() != PMN_OK) return PMN_ERR_CUDA;
         group_outer_finish_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, s>>>(outer, groups, four_over_six);
