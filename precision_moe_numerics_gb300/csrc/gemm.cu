@@ -76,19 +76,27 @@ constexpr uint32_t TMEM_COLS = 512;
 
 // Per (format, N-tile width) layout.  TBN = 256 tiles hold a single TMEM
 // accumulator (two of 256 columns would leave no room for scale factors) and
-// three stages; TBN = 128 tiles double-buffer the accumulator.
+// three stages; TBN = 128 tiles double-buffer the accumulator.  A stage holds
+// the A and B tiles (TMA) and the stage's scale factors in the tcgen05.cp
+// chunk layout, re-laid by the scale-factor warps from either raw scale rows
+// that TMA brought into the stage (SF_TMA) or plain global loads.  Global
+// loads win only where a warp-wide load covers few cache lines: MXFP8 scale
+// rows of the M-grouped 256-wide problems are 48..128 bytes long; K-grouped
+// rows are whole token ranges apart, NVFP4 rows are 16 bytes per stage.
 template <int KIND, int TBN>
 struct Cfg {
-    static constexpr int RB = TBN / 128;                                         // 128-row blocks of B
-    static constexpr int RAW_W = (KIND == KIND_NVFP4 || TBN == 256) ? 16 : 32;   // raw scale bytes per row
+    static constexpr int RB = TBN / 128;  // 128-row blocks of B
+    static constexpr bool SF_TMA = !(KIND == KIND_MXFP8 && TBN == 256);
+    static constexpr int RAW_W = !SF_TMA ? 0 : (KIND == KIND_NVFP4 ? 16 : 32);  // raw scale bytes per row
     static constexpr int B_TILE_BYTES = TBN * 128;
     static constexpr int RAW_A = 128 * RAW_W, RAW_B = TBN * RAW_W;
     static constexpr int SFT_CHUNKS = KIND == KIND_NVFP4 ? 4 : 1;  // K-step chunks per stage
     static constexpr int SFT_A = 512 * SFT_CHUNKS, SFT_B = 512 * SFT_CHUNKS * RB;
-    static constexpr int STAGE_RAW = A_TILE_BYTES + B_TILE_BYTES + RAW_A + RAW_B + SFT_A + SFT_B;
+    static constexpr int SFT_OFF = A_TILE_BYTES + B_TILE_BYTES + RAW_A + RAW_B;  // re-laid chunks in a stage
+    static constexpr int STAGE_RAW = SFT_OFF + SFT_A + SFT_B;
     static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
     static constexpr int STAGES = TBN == 256 ? 3 : PMN_GEMM_STAGES;
-    static constexpr int EPI = EPI_BUFS;  // epilogue staging buffers per warp
+    static constexpr int EPI = TBN == 256 ? 2 : EPI_BUFS;  // epilogue staging buffers per warp
     static constexpr int ACC = TBN == 256 ? 1 : 2;
     static constexpr uint32_t SF_COL0 = ACC * TBN;  // scale factors live after the accumulators
     static constexpr uint32_t SFA_COLS = 4 * SFT_CHUNKS, SFB_COLS = 4 * SFT_CHUNKS * RB;
@@ -107,6 +115,8 @@ struct GemmArgs {
     int64_t m;               // rows of A (M-grouped: total rows)
     int64_t n;
     int64_t k;               // contraction length (K-grouped: total)
+    const uint8_t *sa, *sb;  // scale factors of A and B (row-major, one row per operand row)
+    int64_t sa_pitch, sb_pitch;
     const float *a_outer;    // NVFP4 only
     const float *b_outer;
     void *out;
@@ -134,15 +144,17 @@ __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id)
            ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
 }
 
+// Tile t of the grouped problem.  `gc` is the caller's group cursor: every
+// role walks its tiles in increasing order, so the group of t is found by
+// stepping forward from the group of the previous lookup (a few shared-memory
+// reads, against a binary search on the critical path between tiles).
 template <int KIND, int TBN>
-__device__ __forceinline__ Tile get_tile(int t, const GemmArgs &p, const int *s_off, const int *s_cum)
+__device__ __forceinline__ Tile get_tile(int t, const GemmArgs &p, const int *s_off, const int *s_cum, int &gc)
 {
-    int lo = 0, hi = p.groups;
-    while (hi - lo > 1) {
-        int mid = (lo + hi) >> 1;
-        if (s_cum[mid] <= t) lo = mid;
-        else hi = mid;
-    }
+    int lo = gc;
+    if (s_cum[lo] > t) lo = 0;  // not monotone: restart from the first group
+    while (lo + 1 < p.groups && s_cum[lo + 1] <= t) ++lo;
+    gc = lo;
     Tile ti;
     ti.g = lo;
     const int local = t - s_cum[lo];
@@ -169,6 +181,11 @@ __device__ __forceinline__ Tile get_tile(int t, const GemmArgs &p, const int *s_
 }
 
 __device__ __forceinline__ void latch_error(int bit) { atomicOr(&g_pmn_device_error, bit); }
+
+__device__ __forceinline__ uint32_t u4_word(const uint4 &v, int i)
+{
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
 
 // Every lane of the warp waits; the outcome is made warp-uniform so that a
 // timeout can never split the warp before a .sync.aligned instruction.
@@ -225,8 +242,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        tma_prefetch_desc(&tmSA);
-        tma_prefetch_desc(&tmSB);
+        if (C::SF_TMA) {
+            tma_prefetch_desc(&tmSA);
+            tma_prefetch_desc(&tmSB);
+        }
         tma_prefetch_desc(&tmO);
     }
     if (warp == 0) {
@@ -271,9 +290,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // ------------------------------------------------ TMA producer
             uint32_t stage = 0, phase = 0;
             uint32_t issued = 0, last_parity = 0;
-            int n_issued = 0;
+            int n_issued = 0, gc = 0;
             for (int t = blockIdx.x; t < total && !*(volatile int *)s_abort; t += gridDim.x) {
-                const Tile ti = get_tile<KIND, TBN>(t, p, s_off, s_cum);
+                const Tile ti = get_tile<KIND, TBN>(t, p, s_off, s_cum, gc);
                 const int64_t brow = p.group_k ? ti.n0 : (int64_t)ti.g * p.n + ti.n0;
                 for (int ks = 0; ks < ti.nks; ++ks) {
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1)) {
@@ -285,25 +304,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ++n_issued;
                     uint8_t *st = stages + stage * C::STAGE_BYTES;
                     const uint32_t fb = bar_full + 8 * stage;
-                    const uint32_t raw_w = (KIND == KIND_NVFP4 || TBN == 256 || !p.group_k) ? 16u : 32u;
-                    mbar_arrive_expect_tx(fb, A_TILE_BYTES + C::B_TILE_BYTES + (128u + TBN) * raw_w);
-                    int32_t xk, xs;
-                    if (KIND == KIND_NVFP4) {
-                        xk = ks * 128;  // 256 fp4 values per stage
-                        xs = ks * 16;   // 16 scale bytes per stage
-                    } else {
-                        const int64_t k0 = ti.kb + (int64_t)ks * 128;
-                        xk = (int32_t)k0;
-                        xs = (int32_t)((k0 / 32) & ~int64_t(15));  // 16-byte aligned start
-                    }
+                    const uint32_t raw_w = (KIND == KIND_NVFP4 || !p.group_k) ? 16u : 32u;  // raw scale box
+                    mbar_arrive_expect_tx(fb, A_TILE_BYTES + C::B_TILE_BYTES + (C::SF_TMA ? (128u + TBN) * raw_w : 0u));
+                    // 128 bytes of K per stage: 256 fp4 or 128 fp8 values
+                    const int32_t xk = (int32_t)(KIND == KIND_NVFP4 ? (int64_t)ks * 128 : ti.kb + (int64_t)ks * 128);
                     if (CS > 1)
                         tma_load_2d_mc(smem_u32(st) + rank * (BM / CS) * 128, &tmA, fb, xk,
                                        (int32_t)(ti.m0 + rank * (BM / CS)), cl_mask);
                     else
                         tma_load_2d(smem_u32(st), &tmA, fb, xk, (int32_t)ti.m0);
                     tma_load_2d(smem_u32(st + A_TILE_BYTES), &tmB, fb, xk, (int32_t)brow);
-                    tma_load_2d(smem_u32(st + A_TILE_BYTES + C::B_TILE_BYTES), &tmSA, fb, xs, (int32_t)ti.m0);
-                    tma_load_2d(smem_u32(st + A_TILE_BYTES + C::B_TILE_BYTES + C::RAW_A), &tmSB, fb, xs, (int32_t)brow);
+                    if (C::SF_TMA) {
+                        // raw scale rows; MXFP8 K-grouped boxes start 16-byte aligned below the segment
+                        const int32_t xs = KIND == KIND_NVFP4 ? ks * 16 : (int32_t)((xk / 32) & ~int32_t(15));
+                        tma_load_2d(smem_u32(st + A_TILE_BYTES + C::B_TILE_BYTES), &tmSA, fb, xs, (int32_t)ti.m0);
+                        tma_load_2d(smem_u32(st + A_TILE_BYTES + C::B_TILE_BYTES + C::RAW_A), &tmSB, fb, xs,
+                                    (int32_t)brow);
+                    }
                     issued |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -317,87 +334,215 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (issued & (1u << s)) (void)mbar_wait(bar_full + 8 * s, (last_parity >> s) & 1u, 1000000000ull);
         }
     } else if (warp == 2 || warp == 3) {
-        // ---------------------------------------------------- scale-factor re-lay
-        // Waits for a stage's TMA data, re-lays its scale factors into the
-        // 32 x 128-bit chunks tcgen05.cp expects (chunk s, 16-byte line r0 =
-        // the scale words of rows r0, r0+32, r0+64, r0+96) and signals
-        // sf_ready; it runs up to STAGES stages ahead of the MMA issuer.
-        // Warp 2 owns the even stage slots, warp 3 the odd ones.
-        const uint32_t mine = (uint32_t)(warp - 2);
-        const int raw_w = (KIND == KIND_NVFP4 || TBN == 256 || !p.group_k) ? 16 : 32;
-        uint32_t stage = 0, phase = 0;
-        bool ok = true;
-        int n_seq = 0;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const Tile ti = get_tile<KIND, TBN>(t, p, s_off, s_cum);
-            for (int ks = 0; ks < ti.nks; ++ks) {
-                const int seq = n_seq++;
-                if ((stage & 1u) != mine) {
+        // ---------------------------------------------------- scale factors
+        // A stage's scale factors are written into the 32 x 128-bit chunks
+        // tcgen05.cp expects (chunk c, 16-byte line r0 = the scale words of
+        // rows r0, r0+32, r0+64, r0+96); then sf_ready.
+        if constexpr (C::SF_TMA) {
+            // Raw rows arrive with the stage's TMA data: wait for it, re-lay.
+            // Warp 2 owns the even stage slots, warp 3 the odd ones.
+            const uint32_t mine = (uint32_t)(warp - 2);
+            const int raw_w = (KIND == KIND_NVFP4 || !p.group_k) ? 16 : 32;
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            int n_seq = 0, gc = 0;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile ti = get_tile<KIND, TBN>(t, p, s_off, s_cum, gc);
+                for (int ks = 0; ks < ti.nks; ++ks) {
+                    const int seq = n_seq++;
+                    if ((stage & 1u) != mine) {
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                        continue;
+                    }
+                    ok = warp_wait(bar_full + 8 * stage, phase);
+                    if (!ok || __any_sync(0xFFFFFFFFu, *(volatile int *)s_abort != 0)) {
+                        if (!ok && lane == 0) {
+                            *(volatile int *)s_abort = 1;
+                            latch_error(PMN_DEVERR_WAIT_TIMEOUT);
+                        }
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) PMN_TRACE_POINT(1, seq);
+                    uint8_t *st = stages + stage * C::STAGE_BYTES;
+                    const uint8_t *rawA = st + A_TILE_BYTES + C::B_TILE_BYTES, *rawB = rawA + C::RAW_A;
+                    uint8_t *sftA = st + C::SFT_OFF, *sftB = sftA + C::SFT_A;
+                    // operand op, 128-row block h: chunks at sft + (c * blocks + h) * 512
+    #pragma unroll
+                    for (int blk = 0; blk < 1 + C::RB; ++blk) {
+                        const int op = blk == 0 ? 0 : 1, h = blk == 0 ? 0 : blk - 1;
+                        const uint8_t *raw = (op ? rawB : rawA) + h * 128 * raw_w;
+                        uint8_t *sft = (op ? sftB : sftA) + h * 512;
+                        const int cstride = (op ? C::RB : 1) * 512;
+                        if (KIND == KIND_NVFP4) {
+                            uint4 w[4];
+    #pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                w[j] = *reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * 16);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                *reinterpret_cast<uint4 *>(sft + c * cstride + lane * 16) =
+                                    make_uint4(u4_word(w[0], c), u4_word(w[1], c), u4_word(w[2], c), u4_word(w[3], c));
+                        } else {
+                            const int64_t k0 = ti.kb + (int64_t)ks * 128;
+                            const int rem = (int)((k0 / 32) & 15);  // offset of the stage's 4 scales in the raw row
+                            const int wsel = rem >> 2, sh = (rem & 3) * 8;  // warp-uniform
+                            uint32_t v[4];
+    #pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint4 *rw = reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * raw_w);
+                                const uint4 a0 = rw[0], a1 = raw_w == 32 ? rw[1] : a0;
+                                uint32_t lo, hi;
+                                switch (wsel) {
+                                    case 0: lo = a0.x; hi = a0.y; break;
+                                    case 1: lo = a0.y; hi = a0.z; break;
+                                    case 2: lo = a0.z; hi = a0.w; break;
+                                    default: lo = a0.w; hi = a1.x; break;
+                                }
+                                v[j] = sh ? __funnelshift_r(lo, hi, sh) : lo;
+                            }
+                            *reinterpret_cast<uint4 *>(sft + lane * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        PMN_TRACE_POINT(2, seq);
+                        mbar_arrive(bar_sfr + 8 * stage);
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
-                    continue;
                 }
-                ok = warp_wait(bar_full + 8 * stage, phase);
+            }
+        } else {
+            // Rows are read straight from global memory (four per lane and
+            // operand block).  Warp 2 takes the even stages of the sequence,
+            // warp 3 the odd ones; a warp's loads run two of its stages ahead
+            // of the stage it writes, so their latency overlaps the waits.
+            const uint32_t mine = (uint32_t)(warp - 2);
+            constexpr int W = KIND == KIND_NVFP4 ? 4 : 1;  // scale words per row and stage
+            constexpr int NR = 4 * (1 + C::RB);  // scale rows one lane fetches
+            struct It {
+                int t, ks, gc;
+                Tile ti;
+            };
+            auto settle = [&](It &it) {  // first stage at or after (t, ks)
+                while (it.t < total && it.ks >= it.ti.nks) {
+                    it.t += gridDim.x;
+                    it.ks = 0;
+                    if (it.t < total) it.ti = get_tile<KIND, TBN>(it.t, p, s_off, s_cum, it.gc);
+                }
+            };
+            auto fetch = [&](const It &it, uint32_t (&v)[NR][W]) {
+                const int64_t brow = p.group_k ? it.ti.n0 : (int64_t)it.ti.g * p.n + it.ti.n0;
+    #pragma unroll
+                for (int j = 0; j < NR; ++j) {
+                    const bool opa = j < 4;
+                    const int64_t row = opa ? it.ti.m0 + lane + 32 * j : brow + lane + 32 * (j - 4);
+                    const bool ok_row = !opa || p.group_k || row < p.m;  // M-grouped A: last tile may pass the end
+                    const uint8_t *base = opa ? p.sa : p.sb;
+                    const int64_t pitch = opa ? p.sa_pitch : p.sb_pitch;
+                    const uint8_t *rp = base + row * pitch;
+                    if constexpr (W == 4) {
+                        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                        if (ok_row) w = __ldg(reinterpret_cast<const uint4 *>(rp + 16 * it.ks));
+                        v[j][0] = w.x;
+                        v[j][1] = w.y;
+                        v[j][2] = w.z;
+                        v[j][3] = w.w;
+                    } else if (!p.group_k) {
+                        v[j][0] = ok_row ? __ldg(reinterpret_cast<const uint32_t *>(rp + 4 * it.ks)) : 0u;
+                    } else {
+                        // K segments start at any multiple of 32: the four bytes
+                        // may straddle two aligned words; bytes past the row end
+                        // are never used (the stage's last K-steps are skipped)
+                        const int64_t c0 = (it.ti.kb + (int64_t)it.ks * 128) / 32;
+                        const int64_t ca = c0 & ~int64_t(3);
+                        const uint32_t w0 = __ldg(reinterpret_cast<const uint32_t *>(rp + ca));
+                        const uint32_t w1 =
+                            ca + 4 < pitch ? __ldg(reinterpret_cast<const uint32_t *>(rp + ca + 4)) : 0u;
+                        v[j][0] = __funnelshift_r(w0, w1, (uint32_t)(c0 & 3) * 8u);
+                    }
+                }
+            };
+            // stages of this warp, in order: f is the next one to fetch
+            It f{(int)blockIdx.x, 0, 0, Tile{}};
+            if (f.t < total) f.ti = get_tile<KIND, TBN>(f.t, p, s_off, s_cum, f.gc);
+            settle(f);
+            uint32_t fseq = 0;
+            if (mine) {
+                ++f.ks;
+                settle(f);
+                fseq = 1;
+            }
+            auto prefetch = [&](uint32_t (&v)[NR][W], bool &valid, uint32_t &seq) {
+                valid = f.t < total;
+                seq = fseq;
+                if (valid) fetch(f, v);
+                ++f.ks;
+                settle(f);
+                ++f.ks;
+                settle(f);
+                fseq += 2;
+            };
+            bool ok = true;
+            // write the stage held in `use` (fetched DEPTH - 1 turns earlier),
+            // after fetching a later stage into `pre`; register sets rotate by
+            // name, so no load result is consumed before its turn comes
+            auto turn = [&](uint32_t (&use)[NR][W], bool vuse, uint32_t quse, uint32_t (&pre)[NR][W], bool &vpre,
+                            uint32_t &qpre) {
+                if (!vuse) return false;
+                prefetch(pre, vpre, qpre);
+                const uint32_t stage = quse % STAGES, phase = (quse / STAGES) & 1u;
+                ok = warp_wait(bar_empty + 8 * stage, phase ^ 1u);
                 if (!ok || __any_sync(0xFFFFFFFFu, *(volatile int *)s_abort != 0)) {
                     if (!ok && lane == 0) {
                         *(volatile int *)s_abort = 1;
                         latch_error(PMN_DEVERR_WAIT_TIMEOUT);
                     }
                     ok = false;
-                    break;
+                    return false;
                 }
-                if (lane == 0) PMN_TRACE_POINT(1, seq);
-                uint8_t *st = stages + stage * C::STAGE_BYTES;
-                const uint8_t *rawA = st + A_TILE_BYTES + C::B_TILE_BYTES, *rawB = rawA + C::RAW_A;
-                uint8_t *sftA = st + A_TILE_BYTES + C::B_TILE_BYTES + C::RAW_A + C::RAW_B, *sftB = sftA + C::SFT_A;
-                // operand op, 128-row block h: chunks at sft + (c * blocks + h) * 512
-#pragma unroll
+                if (lane == 0) PMN_TRACE_POINT(1, quse);
+                uint8_t *sftA = stages + stage * C::STAGE_BYTES + C::SFT_OFF;
+                uint8_t *sftB = sftA + C::SFT_A;
+    #pragma unroll
                 for (int blk = 0; blk < 1 + C::RB; ++blk) {
-                    const int op = blk == 0 ? 0 : 1, h = blk == 0 ? 0 : blk - 1;
-                    const uint8_t *raw = (op ? rawB : rawA) + h * 128 * raw_w;
-                    uint8_t *sft = (op ? sftB : sftA) + h * 512;
-                    const int cstride = (op ? C::RB : 1) * 512;
-                    if (KIND == KIND_NVFP4) {
-                        uint4 w[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * 16);
-                        *reinterpret_cast<uint4 *>(sft + 0 * cstride + lane * 16) = make_uint4(w[0].x, w[1].x, w[2].x, w[3].x);
-                        *reinterpret_cast<uint4 *>(sft + 1 * cstride + lane * 16) = make_uint4(w[0].y, w[1].y, w[2].y, w[3].y);
-                        *reinterpret_cast<uint4 *>(sft + 2 * cstride + lane * 16) = make_uint4(w[0].z, w[1].z, w[2].z, w[3].z);
-                        *reinterpret_cast<uint4 *>(sft + 3 * cstride + lane * 16) = make_uint4(w[0].w, w[1].w, w[2].w, w[3].w);
-                    } else {
-                        const int64_t k0 = ti.kb + (int64_t)ks * 128;
-                        const int rem = (int)((k0 / 32) & 15);  // byte offset of this stage's 4 scales in the raw row
-                        const int wsel = rem >> 2, sh = (rem & 3) * 8;  // warp-uniform
-                        uint32_t v[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint4 *rw = reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * raw_w);
-                            const uint4 a0 = rw[0], a1 = raw_w == 32 ? rw[1] : a0;
-                            uint32_t lo, hi;
-                            switch (wsel) {
-                                case 0: lo = a0.x; hi = a0.y; break;
-                                case 1: lo = a0.y; hi = a0.z; break;
-                                case 2: lo = a0.z; hi = a0.w; break;
-                                default: lo = a0.w; hi = a1.x; break;
-                            }
-                            v[j] = sh ? __funnelshift_r(lo, hi, sh) : lo;
-                        }
-                        *reinterpret_cast<uint4 *>(sft + lane * 16) = make_uint4(v[0], v[1], v[2], v[3]);
-                    }
+                    // operand block: A, or 128-row block h of B; chunk c at
+                    // sft + (c * blocks + h) * 512
+                    uint8_t *sft = blk == 0 ? sftA : sftB + (blk - 1) * 512;
+                    const int cstride = (blk == 0 ? 1 : C::RB) * 512;
+                    const int j0 = 4 * blk;
+    #pragma unroll
+                    for (int c = 0; c < C::SFT_CHUNKS; ++c)
+                        *reinterpret_cast<uint4 *>(sft + c * cstride + lane * 16) =
+                            make_uint4(use[j0][c], use[j0 + 1][c], use[j0 + 2][c], use[j0 + 3][c]);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    PMN_TRACE_POINT(2, seq);
+                    PMN_TRACE_POINT(2, quse);
                     mbar_arrive(bar_sfr + 8 * stage);
                 }
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1;
-                }
+                return true;
+            };
+            uint32_t s0[NR][W], s1[NR][W];
+            bool v0, v1;
+            uint32_t q0, q1;
+            prefetch(s0, v0, q0);
+            uint32_t s2[NR][W];
+            bool v2;
+            uint32_t q2;
+            prefetch(s1, v1, q1);
+            while (ok) {
+                if (!turn(s0, v0, q0, s2, v2, q2)) break;
+                if (!turn(s1, v1, q1, s0, v0, q0)) break;
+                if (!turn(s2, v2, q2, s1, v1, q1)) break;
             }
         }
     } else if (warp == 1) {
@@ -411,14 +556,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
             bool ok = true;
             int n_mma = 0;
-            auto next_tile = [&](int t0) {
-                for (int tt = t0; tt < total; tt += gridDim.x)
-                    if (get_tile<KIND, TBN>(tt, p, s_off, s_cum).nks > 0) return tt;
+            // next tile with a non-empty contraction at or after t0 (the
+            // epilogue writes the zero product of an empty one by itself)
+            int gc = 0;
+            auto next_tile = [&](int t0, Tile &out) {
+                for (int tt = t0; tt < total; tt += gridDim.x) {
+                    out = get_tile<KIND, TBN>(tt, p, s_off, s_cum, gc);
+                    if (out.nks > 0) return tt;
+                }
                 return total;
             };
             auto copy_sf = [&](uint32_t stg) {
                 uint8_t *st = stages + stg * C::STAGE_BYTES;
-                const uint8_t *sftA = st + A_TILE_BYTES + C::B_TILE_BYTES + C::RAW_A + C::RAW_B;
+                const uint8_t *sftA = st + C::SFT_OFF;
                 const uint8_t *sftB = sftA + C::SFT_A;
                 const uint32_t sfa = tmem + C::SF_COL0 + stg * C::SF_COLS_STAGE;
                 const uint32_t sfb = sfa + C::SFA_COLS;
@@ -436,7 +586,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 latch_error(PMN_DEVERR_WAIT_TIMEOUT);
                 ok = false;
             };
-            int t = next_tile(blockIdx.x);
+            Tile ti;
+            int t = next_tile(blockIdx.x, ti);
             if (t < total) {
                 if (mbar_wait(bar_sfr + 8 * stage, phase)) {
                     tc_fence_after();
@@ -446,16 +597,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             while (ok && t < total) {
-                const Tile ti = get_tile<KIND, TBN>(t, p, s_off, s_cum);
                 if (!mbar_wait(bar_acc_empty + 8 * abuf, aphase ^ 1) || *(volatile int *)s_abort) {
                     if (!*(volatile int *)s_abort) fail();
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int tn = next_tile(t + gridDim.x);
+                int tn = total;
+                Tile tin;
                 const uint32_t d_tmem = tmem + abuf * TBN;
                 for (int ks = 0; ks < ti.nks; ++ks) {
+                    // the stage's A and B tiles (implied by sf_ready where the
+                    // scale-factor warps waited for the stage's TMA data)
+                    if (!C::SF_TMA) {
+                        if (!mbar_wait(bar_full + 8 * stage, phase)) {
+                            fail();
+                            break;
+                        }
+                        tc_fence_after();
+                    }
                     PMN_TRACE_POINT(3, n_mma);
                     uint8_t *st = stages + stage * C::STAGE_BYTES;
                     const uint32_t sfa = tmem + C::SF_COL0 + stage * C::SF_COLS_STAGE;
@@ -479,6 +639,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (CS > 1) tc_commit_mc(bar_empty + 8 * stage, cl_mask);
                     else tc_commit(bar_empty + 8 * stage);
                     if (ks == ti.nks - 1) tc_commit(bar_acc_full + 8 * abuf);
+                    // the next tile is looked up while this stage's MMAs run
+                    if (ks == 0) tn = next_tile(t + gridDim.x, tin);
                     PMN_TRACE_POINT(4, n_mma);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -500,6 +662,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     aphase ^= 1;
                 }
                 t = tn;
+                ti = tin;
             }
             // drain: every tcgen05 operation of this thread has completed
             tc_commit(bar_drain);
@@ -518,9 +681,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr int CH_PER_STORE = OUT == PMN_OUT_F32 ? 1 : (OUT == PMN_OUT_BF16 ? 2 : 4);
         uint32_t nstore = 0;
         uint32_t abuf = 0, aphase = 0;
-        int n_epi = 0;
+        int n_epi = 0, gc = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const Tile ti = get_tile<KIND, TBN>(t, p, s_off, s_cum);
+            const Tile ti = get_tile<KIND, TBN>(t, p, s_off, s_cum, gc);
             const int64_t row = ti.m0 + 32 * q + lane;
             const bool valid = row < ti.row_end;
             if (ti.nks == 0) {
@@ -763,14 +926,19 @@ pmn_status launch_gemm_cs(const GemmMaps &ms, const CUtensorMap &o, const GemmAr
 {
     using C = Cfg<KIND, TBN>;
     CUtensorMap a, b, sa, sb;
-    // MXFP8 scale rows: 32-byte boxes only where a K segment may start at any
-    // multiple of 32 (K-grouped, 128-wide tiles); 16 bytes otherwise.
-    const uint32_t raw_w = (KIND == KIND_NVFP4 || TBN == 256 || !args.group_k) ? 16u : 32u;
+    // raw MXFP8 scale rows: 32-byte boxes where a K segment may start at any
+    // multiple of 32 (K-grouped); 16 bytes otherwise
+    const uint32_t raw_w = (KIND == KIND_NVFP4 || !args.group_k) ? 16u : 32u;
     if (!make_map(&a, ms.a.base, ms.a.width_bytes, ms.a.rows, ms.a.pitch, 128, true, BM / CS) ||
         !make_map(&b, ms.b.base, ms.b.width_bytes, ms.b.rows, ms.b.pitch, 128, true, TBN) ||
         !make_map(&sa, ms.sa.base, ms.sa.width_bytes, ms.sa.rows, ms.sa.pitch, raw_w, false, BM) ||
         !make_map(&sb, ms.sb.base, ms.sb.width_bytes, ms.sb.rows, ms.sb.pitch, raw_w, false, TBN))
         return PMN_ERR_CUDA;
+    GemmArgs ka = args;  // for scale-factor warps that read global memory
+    ka.sa = static_cast<const uint8_t *>(ms.sa.base);
+    ka.sb = static_cast<const uint8_t *>(ms.sb.base);
+    ka.sa_pitch = (int64_t)ms.sa.pitch;
+    ka.sb_pitch = (int64_t)ms.sb.pitch;
     auto kern = block_scaled_gemm_kernel<KIND, OUT, CS, TBN>;
     const int smem = C::SMEM_BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -794,7 +962,7 @@ pmn_status launch_gemm_cs(const GemmMaps &ms, const CUtensorMap &o, const GemmAr
         if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) return PMN_ERR_CUDA;
         cfg.gridDim = dim3((unsigned)(clusters * CS));
     }
-    if (cudaLaunchKernelEx(&cfg, kern, a, b, sa, sb, o, args) != cudaSuccess) return PMN_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, a, b, sa, sb, o, ka) != cudaSuccess) return PMN_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PMN_OK : PMN_ERR_CUDA;
 }
 
