@@ -187,6 +187,27 @@ __device__ __forceinline__ uint32_t u4_word(const uint4 &v, int i)
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+// Copies a stage's re-laid scale-factor chunks from shared memory into the
+// stage's TMEM columns (A: one 32x128b.warpx4 copy per K-step; B: one per
+// K-step and 128-row block).  Issued by one thread, which then commits.
+template <int KIND, int TBN>
+__device__ __forceinline__ void sf_to_tmem(uint8_t *stages, uint32_t stg, uint32_t tmem)
+{
+    using C = Cfg<KIND, TBN>;
+    const uint8_t *sftA = stages + stg * C::STAGE_BYTES + C::SFT_OFF;
+    const uint8_t *sftB = sftA + C::SFT_A;
+    const uint32_t sfa = tmem + C::SF_COL0 + stg * C::SF_COLS_STAGE;
+    const uint32_t sfb = sfa + C::SFA_COLS;
+#pragma unroll
+    for (int c = 0; c < C::SFT_CHUNKS; ++c) {
+        tc_cp_32x128b_warpx4(sfa + 4 * c, smem_desc(smem_u32(sftA + 512 * c), 0, 128, 0));
+#pragma unroll
+        for (int h = 0; h < C::RB; ++h)
+            tc_cp_32x128b_warpx4(sfb + 4 * (c * C::RB + h),
+                                 smem_desc(smem_u32(sftB + 512 * (c * C::RB + h)), 0, 128, 0));
+    }
+}
+
 // Every lane of the warp waits; the outcome is made warp-uniform so that a
 // timeout can never split the warp before a .sync.aligned instruction.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity)
@@ -411,7 +432,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     __syncwarp();
                     if (lane == 0) {
                         PMN_TRACE_POINT(2, seq);
-                        mbar_arrive(bar_sfr + 8 * stage);
+                        tc_fence_after();
+                        sf_to_tmem<KIND, TBN>(stages, stage, tmem);
+                        tc_commit(bar_sfr + 8 * stage);  // sf_ready once the copies land
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -527,7 +550,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     PMN_TRACE_POINT(2, quse);
-                    mbar_arrive(bar_sfr + 8 * stage);
+                    tc_fence_after();
+                    sf_to_tmem<KIND, TBN>(stages, stage, tmem);
+                    tc_commit(bar_sfr + 8 * stage);  // sf_ready once the copies land
                 }
                 return true;
             };
@@ -547,11 +572,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer
-        // One lane issues everything.  Each stage's scale factors are copied
-        // into TMEM one stage ahead (right after the previous stage's MMAs),
-        // so the copy latency hides behind tensor-core work; the TMEM slot of
-        // a stage is only rewritten after that stage's earlier MMAs completed
-        // (the producer refilled it after their commit).
+        // One lane issues the MMAs.  The scale-factor warps have already
+        // copied the stage's scale factors into its TMEM slot (sf_ready is
+        // their commit); a slot is only rewritten after the stage's earlier
+        // MMAs completed (their commit freed the stage).
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
             bool ok = true;
@@ -566,21 +590,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 return total;
             };
-            auto copy_sf = [&](uint32_t stg) {
-                uint8_t *st = stages + stg * C::STAGE_BYTES;
-                const uint8_t *sftA = st + C::SFT_OFF;
-                const uint8_t *sftB = sftA + C::SFT_A;
-                const uint32_t sfa = tmem + C::SF_COL0 + stg * C::SF_COLS_STAGE;
-                const uint32_t sfb = sfa + C::SFA_COLS;
-#pragma unroll
-                for (int c = 0; c < C::SFT_CHUNKS; ++c) {
-                    tc_cp_32x128b_warpx4(sfa + 4 * c, smem_desc(smem_u32(sftA + 512 * c), 0, 128, 0));
-#pragma unroll
-                    for (int h = 0; h < C::RB; ++h)
-                        tc_cp_32x128b_warpx4(sfb + 4 * (c * C::RB + h),
-                                             smem_desc(smem_u32(sftB + 512 * (c * C::RB + h)), 0, 128, 0));
-                }
-            };
             auto fail = [&]() {
                 *(volatile int *)s_abort = 1;
                 latch_error(PMN_DEVERR_WAIT_TIMEOUT);
@@ -588,14 +597,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             };
             Tile ti;
             int t = next_tile(blockIdx.x, ti);
-            if (t < total) {
-                if (mbar_wait(bar_sfr + 8 * stage, phase)) {
-                    tc_fence_after();
-                    copy_sf(stage);
-                } else {
-                    fail();
-                }
-            }
             while (ok && t < total) {
                 if (!mbar_wait(bar_acc_empty + 8 * abuf, aphase ^ 1) || *(volatile int *)s_abort) {
                     if (!*(volatile int *)s_abort) fail();
@@ -608,14 +609,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t d_tmem = tmem + abuf * TBN;
                 for (int ks = 0; ks < ti.nks; ++ks) {
                     // the stage's A and B tiles (implied by sf_ready where the
-                    // scale-factor warps waited for the stage's TMA data)
-                    if (!C::SF_TMA) {
-                        if (!mbar_wait(bar_full + 8 * stage, phase)) {
-                            fail();
-                            break;
-                        }
-                        tc_fence_after();
+                    // scale-factor warps waited for the stage's TMA data) and
+                    // its scale factors in TMEM
+                    if ((!C::SF_TMA && !mbar_wait(bar_full + 8 * stage, phase)) ||
+                        !mbar_wait(bar_sfr + 8 * stage, phase)) {
+                        fail();
+                        break;
                     }
+                    tc_fence_after();
                     PMN_TRACE_POINT(3, n_mma);
                     uint8_t *st = stages + stage * C::STAGE_BYTES;
                     const uint32_t sfa = tmem + C::SF_COL0 + stage * C::SF_COLS_STAGE;
@@ -645,14 +646,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
-                    }
-                    if (ks + 1 < ti.nks || tn < total) {  // look ahead: next stage's scale factors
-                        if (!mbar_wait(bar_sfr + 8 * stage, phase)) {
-                            fail();
-                            break;
-                        }
-                        tc_fence_after();
-                        copy_sf(stage);
                     }
                     PMN_TRACE_POINT(5, n_mma);
                     ++n_mma;
