@@ -14,7 +14,8 @@
  *
  * Conventions for every call
  *  - All tensor arguments are DEVICE pointers owned by the caller; the library
- *    never allocates, frees or synchronises the device inside a call.  Work is
+ *    never synchronises the device inside a call and allocates nothing but
+ *    the small stream-ordered scratch named below.  Work is
  *    enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy
  *    default stream) and returns immediately.
  *  - Layouts are row-major and dense unless a leading dimension is given.
@@ -109,8 +110,11 @@ PMN_API pmn_status pmn_get_device_error(void *stream, int32_t *err);
  *  outer    out float32 (see outer_mode).
  *  h_out    optional out bf16 [rows, cols]: the SwiGLU value that was
  *           quantised (PMN_IN_BF16_SWIGLU only; NULL to skip).
- * PER_GROUP enqueues a reduction pass, the quantisation pass and a finishing
- * pass; `outer` holds intermediate values until the last pass completes.
+ * PER_GROUP runs one persistent kernel that reads each group for its amax and
+ * codes it while it is still in L2.  It draws (64 + 2 * groups) * 4 bytes of
+ * scratch from the stream-ordered allocator (cudaMallocAsync / cudaFreeAsync
+ * on `stream`); a failed allocation returns PMN_ERR_CUDA.  A group whose amax
+ * pass never completes (bounded wait, 4 s) latches PMN_DEVERR_WAIT_TIMEOUT.
  */
 PMN_API pmn_status pmn_nvfp4_quantize(const void *x, int64_t rows, int64_t cols, int64_t ldx, int in_mode,
                               int outer_mode, int64_t rows_per_group, int four_over_six,

@@ -913,6 +913,9 @@ struct GemmMaps {
 #ifndef PMN_GEMM_CLUSTER_MAX
 #define PMN_GEMM_CLUSTER_MAX 1
 #endif
+#ifndef PMN_GEMM_WIDE_M  // 256-wide tiles for M-grouped problems
+#define PMN_GEMM_WIDE_M 1
+#endif
 
 template <int KIND, int OUT, int CS, int TBN>
 pmn_status launch_gemm_cs(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
@@ -978,7 +981,7 @@ pmn_status launch_gemm_tbn(const GemmMaps &ms, const CUtensorMap &o, const GemmA
 template <int KIND, int OUT>
 pmn_status launch_gemm(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
 {
-    if (!args.group_k && args.n % 256 == 0) return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);
+    if (PMN_GEMM_WIDE_M && !args.group_k && args.n % 256 == 0) return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);
     return launch_gemm_tbn<KIND, OUT, 128>(ms, o, args, s);
 }
 
@@ -1041,10 +1044,14 @@ extern "C" const char *pmn_status_string(pmn_status st)
     }
 }
 
+pmn_status pmn_take_quant_device_error(cudaStream_t s, int *bits);  // quantize.cu
+
 extern "C" pmn_status pmn_get_device_error(void *stream, int32_t *err)
 {
     if (!err) return PMN_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int qbits = 0;
+    if (pmn_take_quant_device_error(s, &qbits) != PMN_OK) return PMN_ERR_CUDA;
     int host = 0;
     if (cudaMemcpyFromSymbolAsync(&host, g_pmn_device_error, sizeof(int), 0, cudaMemcpyDeviceToHost, s) !=
         cudaSuccess)
@@ -1057,7 +1064,7 @@ extern "C" pmn_status pmn_get_device_error(void *stream, int32_t *err)
             cudaStreamSynchronize(s) != cudaSuccess)
             return PMN_ERR_CUDA;
     }
-    *err = host;
+    *err = host | qbits;
     return PMN_OK;
 }
 

@@ -101,8 +101,7 @@ __device__ __forceinline__ float outer_from_amax(float amax, bool four_over_six)
 // once.  SWIGLU: h = silu(gate) * up in binary32, rounded to bf16 first.
 template <int NB, bool SWIGLU>
 __global__ void __launch_bounds__(256) nvfp4_quant_rows_kernel(
-    const uint16_t *__restrict__ x, int64_t rows, int cols, int64_t ldx, int per_group,
-    int64_t rows_per_group, const uint32_t *__restrict__ group_amax, int four_over_six,
+    const uint16_t *__restrict__ x, int64_t rows, int cols, int64_t ldx, int four_over_six,
     uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, float *__restrict__ outer,
     uint16_t *__restrict__ h_out)
 {
@@ -154,14 +153,9 @@ __global__ void __launch_bounds__(256) nvfp4_quant_rows_kernel(
         }
     }
     const bool fos = four_over_six != 0;
-    float g;
-    if (!per_group) {
-        amax = warp_max(amax);
-        g = outer_from_amax(amax, fos);
-        if (lane == 0) outer[row] = g;
-    } else {
-        g = outer_from_amax(__uint_as_float(group_amax[row / rows_per_group]), fos);
-    }
+    amax = warp_max(amax);
+    const float g = outer_from_amax(amax, fos);
+    if (lane == 0) outer[row] = g;
 #pragma unroll
     for (int i = 0; i < NB; ++i) {
         int b = lane + 32 * i;
@@ -180,95 +174,184 @@ __global__ void __launch_bounds__(256) nvfp4_quant_rows_kernel(
     }
 }
 
-// PER_GROUP quantisation once the group amax is known: every 16-block is
-// independent, so threads stream x; each thread takes two blocks (at bi and
-// bi + stride) and issues all four 16-byte loads before any arithmetic.
-__global__ void __launch_bounds__(256) nvfp4_quant_blocks_kernel(const uint16_t *__restrict__ x, int64_t nblocks,
-                                                                 int64_t blocks_per_group,
-                                                                 const uint32_t *__restrict__ group_amax,
-                                                                 int four_over_six, uint8_t *__restrict__ codes,
-                                                                 uint8_t *__restrict__ scales)
+// ---------------------------------------------------------- per-group NVFP4
+// Weights (one outer scale per expert) need the expert's amax before any of
+// its blocks can be coded.  One persistent kernel does both passes over two
+// streams of work items handed out by a ticket counter: A_i = amax of chunk i
+// (chunk c of group g is i = g * nch + c), B_i = NVFP4 coding of chunk i.
+// Tickets run A_0 .. A_{D-1}, then A_{D+k}, B_k alternately, then the last
+// B items: the A stream leads by D >= nch items, so B_i's group has all its A
+// items ticketed first; with D = nch + (CTAs in flight) they have mostly
+// finished, and a chunk is coded about one group after its amax pass read
+// it, while its rows are still in L2: HBM sees each weight byte read once.
+// B waits (bounded) for its group's A count; no A item ever waits, so the
+// streams progress whatever the number of resident CTAs.
+constexpr int QG_THREADS = 256;
+constexpr int QG_CHUNK = 4096;  // 16-blocks per work item (64 Ki values)
+constexpr int QG_PAD = 64;      // the ticket sits alone in its 256-byte line
+
+// scratch words: [0] ticket, [QG_PAD + g] done count of A(g, *),
+// [QG_PAD + groups + g] amax bits of group g; all zero at launch
+inline size_t quant_groups_scratch_bytes(int64_t groups) { return (size_t)(QG_PAD + 2 * groups) * 4u; }
+
+__device__ int g_pmn_quant_error = 0;
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p)
 {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const int64_t b0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t bis[2] = {b0, b0 + stride};
-    uint4 v[2][2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        if (bis[u] < nblocks) {
-            const uint4 *p = reinterpret_cast<const uint4 *>(x + bis[u] * 16);
-            v[u][0] = __ldg(p);
-            v[u][1] = __ldg(p + 1);
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int64_t bi = bis[u];
-        if (bi >= nblocks) continue;
-        const uint32_t w[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
-        float xf[16];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            xf[2 * t] = bf16_lo(w[t]);
-            xf[2 * t + 1] = bf16_hi(w[t]);
-        }
-        const float g = outer_from_amax(__uint_as_float(__ldg(group_amax + bi / blocks_per_group)), four_over_six != 0);
-        const BlockQ q = quant_block(xf, g, four_over_six != 0);
-        *reinterpret_cast<uint2 *>(codes + bi * 8) = make_uint2(q.w0, q.w1);
-        scales[bi] = (uint8_t)q.sbyte;
-    }
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
-// amax of each group of rows (contiguous: ldx == cols), as binary32 bits,
-// combined with atomicMax (order-independent, hence deterministic).
-__global__ void __launch_bounds__(256) group_amax_kernel(const uint16_t *__restrict__ x,
-                                                         int64_t elems_per_group, int64_t chunk,
-                                                         uint32_t *__restrict__ amax_bits)
+__device__ __forceinline__ uint64_t global_ns()
 {
-    const int64_t grp = blockIdx.y;
-    const int64_t begin = (int64_t)blockIdx.x * chunk;
-    int64_t end = begin + chunk;
-    if (end > elems_per_group) end = elems_per_group;
-    const uint16_t *base = x + grp * elems_per_group;
-    uint32_t m = 0u;
-    for (int64_t i = begin + (int64_t)threadIdx.x * 8; i < end; i += (int64_t)blockDim.x * 8) {
-        uint4 q = __ldg(reinterpret_cast<const uint4 *>(base + i));
-        uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            m = max(m, w[t] & 0x7FFFu);
-            m = max(m, (w[t] >> 16) & 0x7FFFu);
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    __shared__ uint32_t red[8];
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__global__ void __launch_bounds__(QG_THREADS, 3) nvfp4_quant_groups_kernel(
+    const uint16_t *__restrict__ x, int64_t groups, int64_t blocks_per_group, int64_t nch, int64_t lead,
+    int four_over_six, uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, float *__restrict__ outer,
+    uint32_t *scratch)
+{
+    __shared__ uint32_t s_red[QG_THREADS / 32];
+    __shared__ uint32_t s_ticket;
+    __shared__ float s_g;
+    __shared__ int s_stop;
+    uint32_t *ticket = scratch, *done = scratch + QG_PAD, *amax = scratch + QG_PAD + groups;
+    const int tid = threadIdx.x;
+    const int64_t na = groups * nch, total = 2 * na, paired = na - lead;
+    const bool fos = four_over_six != 0;
+    if (tid == 0) s_ticket = atomicAdd(ticket, 1u);
     __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t r = red[0];
-        for (int i = 1; i < (int)(blockDim.x >> 5); ++i) r = max(r, red[i]);
-        atomicMax(amax_bits + grp, r << 16);
+    for (;;) {
+        const int64_t t = s_ticket;
+        if (t >= total) break;
+        // the next item's ticket is taken now and published at the end of
+        // this item, so the atomic's round trip overlaps this item's work
+        uint32_t next = 0u;
+        if (tid == 0) next = atomicAdd(ticket, 1u);
+        bool is_a;
+        int64_t i;  // chunk index in its stream
+        if (t < lead) {
+            is_a = true;
+            i = t;
+        } else if (t - lead < 2 * paired) {
+            is_a = ((t - lead) & 1) == 0;
+            i = is_a ? lead + ((t - lead) >> 1) : ((t - lead) >> 1);
+        } else {
+            is_a = false;
+            i = paired + (t - lead - 2 * paired);
+        }
+        const int64_t g = i / nch, c = i - g * nch;
+        const int64_t b0 = c * QG_CHUNK, b1 = min(b0 + QG_CHUNK, blocks_per_group);
+        const uint16_t *xg = x + g * blocks_per_group * 16;
+        bool stop = false;
+        if (is_a) {
+            {
+                // ---- A(g, c): max |x| over the chunk on bf16 bit patterns
+                uint32_t m = 0u;
+#pragma unroll 4
+                for (int64_t b = b0 + tid; b < b1; b += QG_THREADS) {
+                    const uint4 *q = reinterpret_cast<const uint4 *>(xg + b * 16);
+                    const uint4 v0 = __ldg(q), v1 = __ldg(q + 1);
+                    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) m = __vmaxu2(m, w[k] & 0x7FFF7FFFu);  // per 16-bit half
+                }
+                m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+                if ((tid & 31) == 0) s_red[tid >> 5] = m;
+                __syncthreads();
+                if (tid == 0) {
+                    uint32_t r = s_red[0];
+                    for (int i = 1; i < QG_THREADS / 32; ++i) r = max(r, s_red[i]);
+                    atomicMax(amax + g, r << 16);  // binary32 bits of the bf16 amax
+                    __threadfence();
+                    atomicAdd(done + g, 1u);
+                }
+            }
+        } else {
+            // ---- B(g, c): code the chunk once the group's amax is final.  The
+            // first two blocks' loads are in flight while thread 0 waits.
+            uint4 v[2][2];
+            auto load2 = [&](int64_t bb) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int64_t bi = bb + u * QG_THREADS;
+                    if (bi < b1) {
+                        const uint4 *q = reinterpret_cast<const uint4 *>(xg + bi * 16);
+                        v[u][0] = __ldg(q);
+                        v[u][1] = __ldg(q + 1);
+                    }
+                }
+            };
+            load2(b0 + tid);
+            if (tid == 0) {
+                int st = 0;
+                if (ld_acquire_u32(done + g) < (uint32_t)nch) {
+                    const uint64_t t0 = global_ns();
+                    while (ld_acquire_u32(done + g) < (uint32_t)nch) {
+                        __nanosleep(128);
+                        if (global_ns() - t0 > 4000000000ull) {
+                            atomicOr(&g_pmn_quant_error, PMN_DEVERR_WAIT_TIMEOUT);
+                            st = 1;
+                            break;
+                        }
+                    }
+                }
+                const float gv = outer_from_amax(__uint_as_float(ld_acquire_u32(amax + g)), fos);
+                if (c == 0 && !st) outer[g] = gv;
+                s_g = gv;
+                s_stop = st;
+            }
+            __syncthreads();
+            stop = s_stop != 0;
+            const float gv = s_g;
+            for (int64_t bb = b0 + tid; bb < b1 && !stop; bb += 2 * QG_THREADS) {
+                uint4 cur[2][2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    cur[u][0] = v[u][0];
+                    cur[u][1] = v[u][1];
+                }
+                if (bb + 2 * QG_THREADS < b1) load2(bb + 2 * QG_THREADS);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int64_t bi = bb + u * QG_THREADS;
+                    if (bi >= b1) continue;
+                    const uint32_t w[8] = {cur[u][0].x, cur[u][0].y, cur[u][0].z, cur[u][0].w,
+                                           cur[u][1].x, cur[u][1].y, cur[u][1].z, cur[u][1].w};
+                    float xf[16];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        xf[2 * k] = bf16_lo(w[k]);
+                        xf[2 * k + 1] = bf16_hi(w[k]);
+                    }
+                    const BlockQ qb = quant_block(xf, gv, fos);
+                    const int64_t gb = g * blocks_per_group + bi;
+                    *reinterpret_cast<uint2 *>(codes + gb * 8) = make_uint2(qb.w0, qb.w1);
+                    scales[gb] = (uint8_t)qb.sbyte;
+                }
+            }
+        }
+        __syncthreads();  // every thread is done with s_red, s_g and s_ticket
+        if (stop) break;
+        if (tid == 0) s_ticket = next;
+        __syncthreads();
     }
-}
-
-__global__ void group_outer_finish_kernel(float *outer, int64_t groups, int four_over_six)
-{
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < groups) outer[i] = outer_from_amax(outer[i], four_over_six != 0);
 }
 
 template <int NB>
 void launch_rows(bool swiglu, dim3 grid, dim3 block, cudaStream_t s, const uint16_t *x, int64_t rows,
-                 int cols, int64_t ldx, int per_group, int64_t rpg, const uint32_t *gam, int fos,
-                 uint8_t *codes, uint8_t *scales, float *outer, uint16_t *h_out)
+                 int cols, int64_t ldx, int fos, uint8_t *codes, uint8_t *scales, float *outer, uint16_t *h_out)
 {
     if (swiglu)
-        nvfp4_quant_rows_kernel<NB, true><<<grid, block, 0, s>>>(x, rows, cols, ldx, per_group, rpg, gam, fos,
-                                                                 codes, scales, outer, h_out);
+        nvfp4_quant_rows_kernel<NB, true><<<grid, block, 0, s>>>(x, rows, cols, ldx, fos, codes, scales, outer, h_out);
     else
-        nvfp4_quant_rows_kernel<NB, false><<<grid, block, 0, s>>>(x, rows, cols, ldx, per_group, rpg, gam, fos,
-                                                                  codes, scales, outer, h_out);
+        nvfp4_quant_rows_kernel<NB, false><<<grid, block, 0, s>>>(x, rows, cols, ldx, fos, codes, scales, outer, h_out);
 }
 
 // ------------------------------------------------------------------ MXFP8 RN (dY)
@@ -521,7 +604,49 @@ __global__ void __launch_bounds__(256) rht_s2f6_kernel(const float *__restrict__
     out_sc[t] = (uint8_t)sb;
 }
 
+// Clears the scratch, then runs the per-group kernel on as many CTAs as fit.
+pmn_status launch_quant_groups(const uint16_t *x, int64_t groups, int64_t blocks_per_group, int four_over_six,
+                               uint8_t *codes, uint8_t *scales, float *outer, uint32_t *scratch, cudaStream_t s)
+{
+    if (cudaMemsetAsync(scratch, 0, quant_groups_scratch_bytes(groups), s) != cudaSuccess) return PMN_ERR_CUDA;
+    static int grid = 0;
+    if (grid == 0) {
+        int dev = 0, sms = 0, per_sm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nvfp4_quant_groups_kernel, QG_THREADS, 0) !=
+                cudaSuccess)
+            return PMN_ERR_CUDA;
+        grid = std::max(1, sms * per_sm);
+    }
+    const int64_t nch = (blocks_per_group + QG_CHUNK - 1) / QG_CHUNK;
+    // one group plus one item per CTA (measured best of 0, 1 and 2 per CTA)
+    const int64_t lead = std::min(groups * nch, nch + (int64_t)grid);
+    nvfp4_quant_groups_kernel<<<(unsigned)grid, QG_THREADS, 0, s>>>(x, groups, blocks_per_group, nch, lead,
+                                                                     four_over_six, codes, scales, outer, scratch);
+    return launch_status();
+}
+
 }  // namespace
+
+// Reads and clears the quantisation kernels' device error bits (called by
+// pmn_get_device_error, which owns the stream synchronisation).
+pmn_status pmn_take_quant_device_error(cudaStream_t s, int *bits)
+{
+    int host = 0;
+    if (cudaMemcpyFromSymbolAsync(&host, g_pmn_quant_error, sizeof(int), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return PMN_ERR_CUDA;
+    if (host != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbolAsync(g_pmn_quant_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) !=
+                cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return PMN_ERR_CUDA;
+    }
+    *bits = host;
+    return PMN_OK;
+}
 
 // ====================================================================== C ABI
 extern "C" pmn_status pmn_nvfp4_quantize(const void *x, int64_t rows, int64_t cols, int64_t ldx, int in_mode,
@@ -544,41 +669,26 @@ extern "C" pmn_status pmn_nvfp4_quantize(const void *x, int64_t rows, int64_t co
     if (rows == 0) return PMN_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint16_t *xb = reinterpret_cast<const uint16_t *>(x);
-    const uint32_t *gam = nullptr;
-    int64_t groups = 0;
     if (outer_mode == PMN_OUTER_PER_GROUP) {
-        groups = rows / rows_per_group;
-        const int64_t epg = rows_per_group * cols;
-        const int64_t chunk = 1 << 16;
-        if (cudaMemsetAsync(outer, 0, groups * sizeof(float), s) != cudaSuccess) return PMN_ERR_CUDA;
-        dim3 g((unsigned)((epg + chunk - 1) / chunk), (unsigned)groups);
-        group_amax_kernel<<<g, 256, 0, s>>>(xb, epg, chunk, reinterpret_cast<uint32_t *>(outer));
-        if (launch_status() != PMN_OK) return PMN_ERR_CUDA;
-        gam = reinterpret_cast<const uint32_t *>(outer);
-    }
-    if (outer_mode == PMN_OUTER_PER_GROUP) {
-        const int64_t nblocks = rows * (cols / 16);
-        nvfp4_quant_blocks_kernel<<<(unsigned)((nblocks + 511) / 512), 256, 0, s>>>(
-            xb, nblocks, rows_per_group * (cols / 16), gam, four_over_six, codes, scales);
-        if (launch_status() != PMN_OK) return PMN_ERR_CUDA;
-        group_outer_finish_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, s>>>(outer, groups, four_over_six);
-        return launch_status();
+        const int64_t groups = rows / rows_per_group;
+        const size_t ws_bytes = quant_groups_scratch_bytes(groups);
+        void *ws = nullptr;
+        if (cudaMallocAsync(&ws, ws_bytes, s) != cudaSuccess) return PMN_ERR_CUDA;
+        pmn_status st = launch_quant_groups(xb, groups, rows_per_group * (cols / 16), four_over_six, codes, scales,
+                                            outer, static_cast<uint32_t *>(ws), s);
+        if (cudaFreeAsync(ws, s) != cudaSuccess) st = PMN_ERR_CUDA;
+        return st;
     }
     const int nb = (int)((cols / 16 + 31) / 32);
     dim3 block(256), grid((unsigned)((rows + 7) / 8));
-    const int pg = outer_mode == PMN_OUTER_PER_GROUP;
     uint16_t *ho = reinterpret_cast<uint16_t *>(h_out);
-    if (nb <= 1) launch_rows<1>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, pg, rows_per_group, gam, four_over_six, codes, scales, outer, ho);
-    else if (nb <= 2) launch_rows<2>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, pg, rows_per_group, gam, four_over_six, codes, scales, outer, ho);
-    else if (nb <= 4) launch_rows<4>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, pg, rows_per_group, gam, four_over_six, codes, scales, outer, ho);
-    else if (nb <= 8) launch_rows<8>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, pg, rows_per_group, gam, four_over_six, codes, scales, outer, ho);
-    else launch_rows<16>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, pg, rows_per_group, gam, four_over_six, codes, scales, outer, ho);
-    if (launch_status() != PMN_OK) return PMN_ERR_CUDA;
-    if (outer_mode == PMN_OUTER_PER_GROUP) {
-        group_outer_finish_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, s>>>(outer, groups, four_over_six);
-        if (launch_status() != PMN_OK) return PMN_ERR_CUDA;
-    }
-    return PMN_OK;
+    const int fos = four_over_six;
+    if (nb <= 1) launch_rows<1>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, fos, codes, scales, outer, ho);
+    else if (nb <= 2) launch_rows<2>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, fos, codes, scales, outer, ho);
+    else if (nb <= 4) launch_rows<4>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, fos, codes, scales, outer, ho);
+    else if (nb <= 8) launch_rows<8>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, fos, codes, scales, outer, ho);
+    else launch_rows<16>(swiglu, grid, block, s, xb, rows, (int)cols, ldx, fos, codes, scales, outer, ho);
+    return launch_status();
 }
 
 extern "C" pmn_status pmn_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int transpose, uint8_t *out,

@@ -77,6 +77,23 @@ def test_nvfp4_quantize_per_expert_weights(pmn):
     assert_same(c, rc, "codes")
 
 
+def test_nvfp4_quantize_per_expert_multichunk(pmn):
+    """Groups spanning several work chunks of 4096 blocks with a ragged last
+    chunk; each expert's amax sits in a different chunk (first, middle, the
+    partial last one), so every chunk's amax must reach the group's scale."""
+    rng = np.random.default_rng(11)
+    E, N, K = 3, 520, 1024  # 33280 blocks per expert: 8 full chunks + 512 blocks
+    w = W.normal_bf16_host(rng, (E * N, K), 0.02)
+    for e, r in enumerate((3, 260, N - 1)):
+        w[e * N + r, 17] = W.f32_to_bf16_bits(np.array([-7.5], np.float32))[0]
+    c, s, g = pmn.nvfp4_quantize(to_dev_bf16(w), outer_mode=pmn.OUTER_PER_GROUP, rows_per_group=N)
+    rc, rs, rg = oracle.nvfp4_quantize(w, oracle.OUTER_PER_GROUP, group_offsets=np.arange(E + 1) * N)
+    assert_same(g, rg, "outer")
+    assert_same(s, rs, "scales")
+    assert_same(c, rc, "codes")
+    assert pmn.get_device_error() == 0
+
+
 def test_nvfp4_quantize_expert_case_activations(pmn):
     d = W.expert(0, tokens=512)
     c, s, g = pmn.nvfp4_quantize(to_dev_bf16(d["x"]), four_over_six=True)
