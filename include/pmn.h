@@ -122,6 +122,24 @@ PMN_API pmn_status pmn_nvfp4_quantize(const void *x, int64_t rows, int64_t cols,
                               void *stream);
 
 /*
+ * pmn_nvfp4_quantize with PMN_OUTER_PER_GROUP (ldx = cols, no 4/6 input
+ * restriction), computing the same bytes, but with its scratch in a fixed
+ * device array of the library instead of a stream-ordered allocation: the
+ * call allocates nothing.  The pages have no counterpart to this entry point;
+ * it exists for callers that must not allocate (graph capture without a
+ * memory pool, allocation-free serving loops).
+ *  rows / rows_per_group <= 1024 groups, else PMN_ERR_INVALID_ARG.
+ *  Other arguments and rules as pmn_nvfp4_quantize.
+ * The fixed scratch is shared by all calls on a device: calls on different
+ * streams must not overlap in time (calls on one stream are ordered).  The
+ * scratch is cleared on `stream` before the kernel runs.
+ */
+PMN_API pmn_status pmn_nvfp4_quantize_per_group_noalloc(const void *x, int64_t rows, int64_t cols,
+                                                        int64_t rows_per_group, int four_over_six,
+                                                        uint8_t *codes, uint8_t *scales, float *outer,
+                                                        void *stream);
+
+/*
  * Dequantise -> transpose -> requantise to MXFP8 [SR]: the saved NVFP4 tensor
  * is dequantised in float32, d = (code * scale) * g, transposed, and rounded
  * to E4M3 with one E8M0 scale per 32 values along the ORIGINAL rows.  The

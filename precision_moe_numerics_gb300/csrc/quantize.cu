@@ -10,6 +10,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/pmn.h"
 #include "numerics.cuh"
@@ -195,6 +196,10 @@ constexpr int QG_PAD = 64;      // the ticket sits alone in its 256-byte line
 inline size_t quant_groups_scratch_bytes(int64_t groups) { return (size_t)(QG_PAD + 2 * groups) * 4u; }
 
 __device__ int g_pmn_quant_error = 0;
+
+// Fixed scratch of the no-allocation entry point (groups <= QG_NOALLOC_GROUPS).
+constexpr int QG_NOALLOC_GROUPS = 1024;
+static __device__ __align__(256) uint32_t g_qg_scratch[QG_PAD + 2 * QG_NOALLOC_GROUPS];
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p)
 {
@@ -648,7 +653,44 @@ pmn_status pmn_take_quant_device_error(cudaStream_t s, int *bits)
     return PMN_OK;
 }
 
+// Device address of the fixed scratch, looked up once per device.
+pmn_status noalloc_scratch(uint32_t **out)
+{
+    constexpr int MAX_DEV = 64;
+    static std::mutex mu;
+    static void *addr[MAX_DEV] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return PMN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_qg_scratch) != cudaSuccess || !p) return PMN_ERR_CUDA;
+        addr[dev] = p;
+    }
+    *out = static_cast<uint32_t *>(addr[dev]);
+    return PMN_OK;
+}
+
 // ====================================================================== C ABI
+extern "C" pmn_status pmn_nvfp4_quantize_per_group_noalloc(const void *x, int64_t rows, int64_t cols,
+                                                            int64_t rows_per_group, int four_over_six,
+                                                            uint8_t *codes, uint8_t *scales, float *outer,
+                                                            void *stream)
+{
+    if (rows < 0 || cols <= 0 || cols % 16 != 0 || cols > 8192) return PMN_ERR_INVALID_ARG;
+    if (four_over_six != 0 && four_over_six != 1) return PMN_ERR_INVALID_ARG;
+    if (rows_per_group <= 0 || rows % rows_per_group != 0) return PMN_ERR_INVALID_ARG;
+    if (rows / rows_per_group > QG_NOALLOC_GROUPS) return PMN_ERR_INVALID_ARG;
+    if (!x || !codes || !scales || !outer) return PMN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(outer)) return PMN_ERR_INVALID_ARG;
+    if (rows == 0) return PMN_OK;
+    uint32_t *scratch = nullptr;
+    if (noalloc_scratch(&scratch) != PMN_OK) return PMN_ERR_CUDA;
+    return launch_quant_groups(reinterpret_cast<const uint16_t *>(x), rows / rows_per_group,
+                               rows_per_group * (cols / 16), four_over_six, codes, scales, outer, scratch,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" pmn_status pmn_nvfp4_quantize(const void *x, int64_t rows, int64_t cols, int64_t ldx, int in_mode,
                                          int outer_mode, int64_t rows_per_group, int four_over_six,
                                          uint8_t *codes, uint8_t *scales, float *outer, void *h_out,

@@ -34,6 +34,7 @@ SIGNATURES = {
     "pmn_status_string": ([_I], ctypes.c_char_p),
     "pmn_get_device_error": ([_P, _P], _I),
     "pmn_nvfp4_quantize": ([_P, _I64, _I64, _I64, _I, _I, _I64, _I, _P, _P, _P, _P, _P], _I),
+    "pmn_nvfp4_quantize_per_group_noalloc": ([_P, _I64, _I64, _I64, _I, _P, _P, _P, _P], _I),
     "pmn_requant_transpose_sr_mxfp8": ([_P, _P, _P, _I, _I64, _I64, _I64, _U64, _U32, _I, _P, _P, _P], _I),
     "pmn_mxfp8_quantize": ([_P, _I64, _I64, _I, _P, _P, _P], _I),
     "pmn_grouped_gemm_nvfp4": ([_P, _P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P], _I),
@@ -123,6 +124,24 @@ def nvfp4_quantize(x, cols=None, four_over_six=False, outer_mode=OUTER_PER_ROW, 
                                   _ptr(h), _stream(stream))
     _check(st, "nvfp4_quantize")
     return (codes, scales, outer, h) if want_h else (codes, scales, outer)
+
+
+def nvfp4_quantize_per_group_noalloc(x, rows_per_group, four_over_six=False, out=None, stream=None):
+    """As nvfp4_quantize(x, outer_mode=OUTER_PER_GROUP, ...), through the entry point whose scratch is a
+    fixed device array (no allocation inside the call)."""
+    _dev(x, torch.bfloat16)
+    rows, cols = x.shape
+    dev = x.device
+    if out is None:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+        scales = torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev)
+        outer = torch.empty((rows // rows_per_group,), dtype=torch.float32, device=dev)
+    else:
+        codes, scales, outer = out
+    st = lib().pmn_nvfp4_quantize_per_group_noalloc(_ptr(x), rows, cols, rows_per_group, int(four_over_six),
+                                                    _ptr(codes), _ptr(scales), _ptr(outer), _stream(stream))
+    _check(st, "nvfp4_quantize_per_group_noalloc")
+    return codes, scales, outer
 
 
 def requant_transpose_sr_mxfp8(codes, scales, outer, outer_per_row, batch, rows, cols, seed, tag,

@@ -57,6 +57,10 @@ def test_host_argument_checks_need_no_gpu(libpath):
                                     null) == pmn.ERR_INVALID_ARG
     assert L.pmn_gemm_mxfp8(null, null, null, null, null, 1, 5, 128, 128, 512, 0, null, null) == pmn.ERR_INVALID_ARG
     assert L.pmn_rht_s2f6_quantize(null, 1, 31, 0, null, null, null) == pmn.ERR_INVALID_ARG
+    # more groups than the fixed scratch holds: rejected before any pointer is used
+    fake = 1 << 20
+    assert L.pmn_nvfp4_quantize_per_group_noalloc(fake, 1025 * 16, 64, 16, 0, fake, fake, fake,
+                                                  null) == pmn.ERR_INVALID_ARG
 
 
 def test_product_path_does_not_import_oracle():
