@@ -40,35 +40,95 @@ __device__ __forceinline__ float warp_max(float v)
 // One candidate block scale m (6, or 4 for the 4/6 choice) with outer scale g:
 //   s = amax / (m g); S = RN_E4M3(s); sd = dec(S) g; r = 1/sd (0 if sd == 0)
 //   c_i = RN_E2M1(x_i r)   (packed: element 2i low nibble)
-// Returns the summed squared dequantisation error (tree order i+8, +4, +2, +1)
-// when want_err is set.
+// With the 4/6 choice each candidate also yields its summed squared
+// dequantisation error (tree order i+8, +4, +2, +1).
 struct BlockQ {
     uint32_t w0, w1;  // 8 code bytes
     uint32_t sbyte;
 };
 
-__device__ __forceinline__ float quant_block_candidate(const float (&x)[16], float amax, float g, float m,
-                                                       bool want_err, BlockQ &out)
+// Constants of one row's or one group's blocks: d = RN(m g), rd = RN(1/d).
+struct QCtx {
+    float g, d6, rd6, d4, rd4;
+    bool fast6, fast4;  // rd finite and normal: the quotient shortcut below applies
+};
+
+__device__ __forceinline__ bool normal_finite(float v) { return fabsf(v) >= 1.17549435e-38f && fabsf(v) <= 3.4e38f; }
+
+__device__ __forceinline__ QCtx make_qctx(float g, bool four_over_six)
 {
-    float s = __fdiv_rn(amax, __fmul_rn(m, g));
-    uint32_t S = cvt_e4m3(s);
-    float dS = e4m3_to_f32(S);
-    float sd = __fmul_rn(dS, g);
-    float r = (sd == 0.0f) ? 0.0f : __fdiv_rn(1.0f, sd);
+    QCtx c;
+    c.g = g;
+    c.d6 = __fmul_rn(6.0f, g);
+    c.rd6 = __frcp_rn(c.d6);
+    c.fast6 = normal_finite(c.d6) && normal_finite(c.rd6);
+    c.d4 = c.d6;
+    c.rd4 = c.rd6;
+    c.fast4 = false;
+    if (four_over_six) {
+        c.d4 = __fmul_rn(4.0f, g);
+        c.rd4 = __frcp_rn(c.d4);
+        c.fast4 = normal_finite(c.d4) && normal_finite(c.rd4);
+    }
+    return c;
+}
+
+// S = RN_E4M3(RN(amax / d)) for amax >= 0.  q = RN(amax * rd) is within
+// about one ulp of amax / d (two roundings of relative size 2^-24 each), so
+// the true quotient and its binary32 rounding both lie in [q - 2 ulp, q + 2
+// ulp]; E4M3 rounding is monotone, so when both ends of that interval round
+// to the same byte, so does RN(amax / d).  Otherwise (q within two ulps of an
+// E4M3 rounding boundary) the correctly rounded quotient is formed.
+__device__ __forceinline__ uint32_t block_scale_byte(float amax, float d, float rd, bool fast)
+{
+    if (amax == 0.0f) return 0u;
+    if (fast) {
+        const uint32_t qb = __float_as_uint(__fmul_rn(amax, rd));
+        const uint32_t lo = cvt_e4m3(__uint_as_float(qb - 2u)), hi = cvt_e4m3(__uint_as_float(qb + 2u));
+        if (lo == hi) return lo;
+    }
+    return cvt_e4m3(__fdiv_rn(amax, d));
+}
+
+// Packed binary32 product (each lane rounded to nearest even).  Used only
+// where the product feeds a conversion: measured on sm_103a, a packed multiply
+// whose result feeds a packed add is contracted into a fused multiply-add
+// despite the .rn modifiers, so sums of products stay on the scalar
+// intrinsics, which are never contracted.
+__device__ __forceinline__ void mul2(float a0, float a1, float b0, float b1, float &c0, float &c1)
+{
+    asm("{\n\t.reg .b64 a, b, c;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 c, a, b;\n\tmov.b64 {%0, %1}, c;\n\t}"
+        : "=f"(c0), "=f"(c1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ float quant_block_candidate(const float (&x)[16], float amax, float g, float d, float rd,
+                                                       bool fast, bool want_err, BlockQ &out)
+{
+    const uint32_t S = block_scale_byte(amax, d, rd, fast);
+    const uint32_t dS2 = e4m3_to_h2(S);  // dec(S) in both f16 halves (exact)
+    const float sd = __fmul_rn(h2_lo_to_f32(dS2), g);
+    const float r = (sd == 0.0f) ? 0.0f : __frcp_rn(sd);
     uint32_t c[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = cvt_e2m1x2(__fmul_rn(x[2 * i], r), __fmul_rn(x[2 * i + 1], r));
-    out.w0 = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-    out.w1 = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+    for (int i = 0; i < 8; ++i) {
+        float p0, p1;
+        mul2(x[2 * i], x[2 * i + 1], r, r, p0, p1);
+        c[i] = cvt_e2m1x2(p0, p1);
+    }
+    out.w0 = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
+    out.w1 = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
     out.sbyte = S;
     if (!want_err) return 0.0f;
+    // dequantised value RN(RN(code * dec(S)) * g); code * dec(S) is exact in f16
     float e[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        uint32_t code = (c[i >> 1] >> (4 * (i & 1))) & 15u;
-        float deq = __fmul_rn(__fmul_rn(e2m1_to_f32(code), dS), g);
-        float d = __fsub_rn(x[i], deq);
-        e[i] = __fmul_rn(d, d);
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t cs2 = e2m1x2_mul_h2(c[i], dS2);
+        const float d0 = __fsub_rn(x[2 * i], __fmul_rn(h2_lo_to_f32(cs2), g));
+        const float d1 = __fsub_rn(x[2 * i + 1], __fmul_rn(h2_hi_to_f32(cs2), g));
+        e[2 * i] = __fmul_rn(d0, d0);
+        e[2 * i + 1] = __fmul_rn(d1, d1);
     }
 #pragma unroll
     for (int h = 8; h >= 1; h >>= 1)
@@ -77,15 +137,15 @@ __device__ __forceinline__ float quant_block_candidate(const float (&x)[16], flo
     return e[0];
 }
 
-__device__ __forceinline__ BlockQ quant_block(const float (&x)[16], float g, bool four_over_six)
+__device__ __forceinline__ BlockQ quant_block(const float (&x)[16], const QCtx &c, bool four_over_six)
 {
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
     BlockQ q6, q4;
-    float err6 = quant_block_candidate(x, amax, g, 6.0f, four_over_six, q6);
+    const float err6 = quant_block_candidate(x, amax, c.g, c.d6, c.rd6, c.fast6, four_over_six, q6);
     if (four_over_six) {
-        float err4 = quant_block_candidate(x, amax, g, 4.0f, true, q4);
+        const float err4 = quant_block_candidate(x, amax, c.g, c.d4, c.rd4, c.fast4, true, q4);
         if (err4 < err6) return q4;
     }
     return q6;
@@ -156,6 +216,7 @@ __global__ void __launch_bounds__(256) nvfp4_quant_rows_kernel(
     const bool fos = four_over_six != 0;
     amax = warp_max(amax);
     const float g = outer_from_amax(amax, fos);
+    const QCtx qc = make_qctx(g, fos);
     if (lane == 0) outer[row] = g;
 #pragma unroll
     for (int i = 0; i < NB; ++i) {
@@ -168,7 +229,7 @@ __global__ void __launch_bounds__(256) nvfp4_quant_rows_kernel(
                 xf[2 * t] = bf16_lo(w[t]);
                 xf[2 * t + 1] = bf16_hi(w[t]);
             }
-            BlockQ q = quant_block(xf, g, fos);
+            BlockQ q = quant_block(xf, qc, fos);
             *reinterpret_cast<uint2 *>(codes + row * (cols >> 1) + b * 8) = make_uint2(q.w0, q.w1);
             scales[row * nblk + b] = (uint8_t)q.sbyte;
         }
@@ -315,6 +376,7 @@ __global__ void __launch_bounds__(QG_THREADS, 3) nvfp4_quant_groups_kernel(
             __syncthreads();
             stop = s_stop != 0;
             const float gv = s_g;
+            const QCtx qc = make_qctx(gv, fos);
             for (int64_t bb = b0 + tid; bb < b1 && !stop; bb += 2 * QG_THREADS) {
                 uint4 cur[2][2];
 #pragma unroll
@@ -335,7 +397,7 @@ __global__ void __launch_bounds__(QG_THREADS, 3) nvfp4_quant_groups_kernel(
                         xf[2 * k] = bf16_lo(w[k]);
                         xf[2 * k + 1] = bf16_hi(w[k]);
                     }
-                    const BlockQ qb = quant_block(xf, gv, fos);
+                    const BlockQ qb = quant_block(xf, qc, fos);
                     const int64_t gb = g * blocks_per_group + bi;
                     *reinterpret_cast<uint2 *>(codes + gb * 8) = make_uint2(qb.w0, qb.w1);
                     scales[gb] = (uint8_t)qb.sbyte;
@@ -469,6 +531,49 @@ __device__ __forceinline__ int rq_chunk(int c, int logical)
 // of a quarter-warp read different banks
 __device__ __forceinline__ int rq_gidx(int r) { return r + ((r >> 5) << 2); }
 
+// One output 32-block with a per-group outer scale g: y = cs * (g * 2^-e)
+// from 32 exact f16 values cs = code * S (16 f16x2 words); returns e.
+__device__ __forceinline__ int rq_group_y(const uint32_t (&hw)[16], float g, float (&y)[32])
+{
+    uint32_t m = 0u;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m = __vmaxu2(m, hw[j] & 0x7FFF7FFFu);
+    const float amax_cs = fmaxf(h2_lo_to_f32(m), h2_hi_to_f32(m));
+    const int e = mx_exponent_448(__fmul_rn(amax_cs, g));
+    // exact; an all-zero block keeps its signed zeros (g * 2^127 could overflow)
+    const float gp = amax_cs == 0.0f ? 0.0f : __fmul_rn(g, exp2_neg(e));
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        y[2 * j] = __fmul_rn(h2_lo_to_f32(hw[j]), gp);
+        y[2 * j + 1] = __fmul_rn(h2_hi_to_f32(hw[j]), gp);
+    }
+    return e;
+}
+
+// E4M3 bytes of one output 32-block (output elements i0 .. i0+31, i0 a
+// multiple of 32): hardware stochastic rounding fed with the Philox words of
+// elements 16j .. 16j+15, or round-to-nearest-even; then its E8M0 byte.
+__device__ __forceinline__ void rq_emit(const float (&y)[32], int e, uint64_t i0, uint64_t seed, uint32_t tag,
+                                        int stochastic, uint8_t *out, uint8_t *sc)
+{
+    uint32_t o[8];
+    if (stochastic) {
+        const uint4 wa = sr_words16(seed, tag, i0 >> 4);
+        const uint4 wb = sr_words16(seed, tag, (i0 >> 4) + 1);
+        const uint32_t wd[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[k] = cvt_e4m3x4_rs(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3], wd[k]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            o[k] = cvt_e4m3x2_rn(y[4 * k], y[4 * k + 1]) | (cvt_e4m3x2_rn(y[4 * k + 2], y[4 * k + 3]) << 16);
+    }
+    uint4 *po = reinterpret_cast<uint4 *>(out + i0);
+    po[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    po[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    *sc = (uint8_t)(e + 127);
+}
+
 __global__ void __launch_bounds__(256) requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, const float *__restrict__ outer,
     int outer_per_row, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, int stochastic,
@@ -533,18 +638,7 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
         float y[32];
         int e;
         if (!outer_per_row) {
-            uint32_t m = 0u;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) m = __vmaxu2(m, hw[j] & 0x7FFF7FFFu);
-            const float amax_cs = fmaxf(h2_lo_to_f32(m), h2_hi_to_f32(m));
-            e = mx_exponent_448(__fmul_rn(amax_cs, g_batch));
-            // exact; an all-zero block keeps its signed zeros (g * 2^127 could overflow)
-            const float gp = amax_cs == 0.0f ? 0.0f : __fmul_rn(g_batch, exp2_neg(e));
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                y[2 * j] = __fmul_rn(h2_lo_to_f32(hw[j]), gp);
-                y[2 * j + 1] = __fmul_rn(h2_hi_to_f32(hw[j]), gp);
-            }
+            e = rq_group_y(hw, g_batch, y);
         } else {
             float amax = 0.0f;
             const float4 *gp4 = reinterpret_cast<const float4 *>(gS + rq_gidx(rb * 32));
@@ -564,22 +658,7 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
             for (int j = 0; j < 32; ++j) y[j] = __fmul_rn(y[j], sc);  // exact
         }
         const int64_t i0 = (b * cols + oc) * rows + orow0;  // output index, multiple of 32
-        uint32_t o[8];
-        if (stochastic) {
-            const uint4 wa = sr_words16(seed, tag, (uint64_t)i0 >> 4);
-            const uint4 wb = sr_words16(seed, tag, ((uint64_t)i0 >> 4) + 1);
-            const uint32_t wd[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-            for (int k = 0; k < 8; ++k) o[k] = cvt_e4m3x4_rs(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3], wd[k]);
-        } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                o[k] = cvt_e4m3x2_rn(y[4 * k], y[4 * k + 1]) | (cvt_e4m3x2_rn(y[4 * k + 2], y[4 * k + 3]) << 16);
-        }
-        uint4 *po = reinterpret_cast<uint4 *>(out + i0);
-        po[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        po[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        out_sc[(b * cols + oc) * (rows / 32) + orow0 / 32] = (uint8_t)(e + 127);
+        rq_emit(y, e, (uint64_t)i0, seed, tag, stochastic, out, out_sc + (b * cols + oc) * (rows / 32) + orow0 / 32);
     }
 }
 

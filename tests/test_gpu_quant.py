@@ -94,6 +94,32 @@ def test_nvfp4_quantize_per_expert_multichunk(pmn):
     assert pmn.get_device_error() == 0
 
 
+def test_nvfp4_block_scale_rounding_boundaries(pmn):
+    """Block amax values sweep every bf16 pattern from 2^-8 to 2^8, with outer
+    scales chosen so that m * g is a power of two: amax / (m g) then lands
+    exactly on E4M3 rounding midpoints (ties) and next to them, where the
+    block scale's quotient must be the correctly rounded one."""
+    rng = np.random.default_rng(17)
+    v = np.arange(0x3B80, 0x4380, dtype=np.uint16)  # 2048 bf16 patterns
+    amax = W.bf16_bits_to_f32(v)
+    x = amax[:, None] * rng.uniform(-1.0, 1.0, (len(v), 16)).astype(np.float32)
+    x[:, 0] = amax * np.where(rng.random(len(v)) < 0.5, -1.0, 1.0)
+    x = W.f32_to_bf16_bits(x.reshape(16, 2048).astype(np.float32))
+    x[:, 0] = W.f32_to_bf16_bits(np.array([448.0], np.float32))[0]  # group / row amax 448
+    # per group: g = 448 / 2688, 6 g = 1
+    c, s, g = pmn.nvfp4_quantize(to_dev_bf16(x), outer_mode=pmn.OUTER_PER_GROUP, rows_per_group=16)
+    rc, rs, rg = oracle.nvfp4_quantize(x, oracle.OUTER_PER_GROUP, group_offsets=[0, 16])
+    assert_same(g, rg, "outer")
+    assert_same(s, rs, "scales")
+    assert_same(c, rc, "codes")
+    # per row with 4/6: g = 448 / 1792, 4 g = 1 and 6 g = 1.5
+    c, s, g = pmn.nvfp4_quantize(to_dev_bf16(x), four_over_six=True)
+    rc, rs, rg = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW, four_over_six=True)
+    assert_same(g, rg, "outer")
+    assert_same(s, rs, "scales")
+    assert_same(c, rc, "codes")
+
+
 def test_nvfp4_quantize_expert_case_activations(pmn):
     d = W.expert(0, tokens=512)
     c, s, g = pmn.nvfp4_quantize(to_dev_bf16(d["x"]), four_over_six=True)
