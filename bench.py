@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "NVFP4 expert-GEMM TFLOPS (% FP4 peak); quant/requant GB/s (% HBM peak)"
 WORKLOAD = ("moe_expert_layer_step: 384 experts, top-8 of 16384 tokens (131072 routed rows, expert segments "
-            "padded to 32), d_model 4096, d_ff 1536; NVFP4 fwd + RHT/S2F6 combine + SR-MXFP8 bwd")
+            "padded to 128), d_model 4096, d_ff 1536; NVFP4 fwd + RHT/S2F6 combine + SR-MXFP8 bwd")
 NOMINAL_TC_RATIO = {"fp4": 13.5 / 2.25, "fp8": 4.5 / 2.25}
 
 

@@ -234,10 +234,13 @@ PMN_API pmn_status pmn_rht_s2f6_quantize(const float *x, int64_t rows, int64_t c
  *           rows of group g are offsets[g] <= row < offsets[g+1]; out [m, n].
  * group_mode PMN_GROUP_K (dW = dY^T . X per expert): A [m, k], B [n, k] with k
  *           the routed-row axis; group g contracts offsets[g] <= k <
- *           offsets[g+1] (multiples of 32); out [num_groups, m, n].
+ *           offsets[g+1] (multiples of 128); out [num_groups, m, n].
  *  offsets  DEVICE int32 [num_groups + 1], non-decreasing, within [0, m]
- *           (GROUP_M) or [0, k] and multiples of 32 (GROUP_K); checked on the
- *           device (invalid: nothing runs, PMN_DEVERR_BAD_OFFSETS latched).
+ *           (GROUP_M) or [0, k] and multiples of 128 (GROUP_K: expert
+ *           segments of the routed rows padded with zero rows to multiples of
+ *           128, so every 128-deep K stage starts on a 4-scale boundary);
+ *           checked on the device (invalid: nothing runs,
+ *           PMN_DEVERR_BAD_OFFSETS latched).
  *  scale tensors need a row pitch that is a multiple of 16 bytes: k % 512 == 0.
  *  m        multiple of 128 for PMN_GROUP_K;  n multiple of 128;  k multiple
  *           of 512.  num_groups <= 1024.

@@ -58,8 +58,11 @@ namespace {
 constexpr int KIND_NVFP4 = 0, KIND_MXFP8 = 1;
 constexpr int BM = 128;
 constexpr int BN_MIN = 128;  // N-tiles are 128 or 256 columns
-#ifndef PMN_GEMM_STAGES
+#ifndef PMN_GEMM_STAGES  // 128-wide NVFP4 tiles
 #define PMN_GEMM_STAGES 4
+#endif
+#ifndef PMN_GEMM_STAGES_MXFP8  // 128-wide MXFP8 tiles (the K-grouped weight gradients)
+#define PMN_GEMM_STAGES_MXFP8 5
 #endif
 #ifndef PMN_EPI_BUFS
 #define PMN_EPI_BUFS 2
@@ -87,7 +90,10 @@ template <int KIND, int TBN>
 struct Cfg {
     static constexpr int RB = TBN / 128;  // 128-row blocks of B
     static constexpr bool SF_TMA = !(KIND == KIND_MXFP8 && TBN == 256);
-    static constexpr int RAW_W = !SF_TMA ? 0 : (KIND == KIND_NVFP4 ? 16 : 32);  // raw scale bytes per row
+    // raw scale bytes per row and stage: NVFP4 needs 16; MXFP8 needs 4, which
+    // never straddle a 16-byte box because every K start (M-grouped: 0,
+    // K-grouped: expert segments aligned to 128) is a multiple of 128
+    static constexpr int RAW_W = !SF_TMA ? 0 : 16;
     static constexpr int B_TILE_BYTES = TBN * 128;
     static constexpr int RAW_A = 128 * RAW_W, RAW_B = TBN * RAW_W;
     static constexpr int SFT_CHUNKS = KIND == KIND_NVFP4 ? 4 : 1;  // K-step chunks per stage
@@ -95,14 +101,14 @@ struct Cfg {
     static constexpr int SFT_OFF = A_TILE_BYTES + B_TILE_BYTES + RAW_A + RAW_B;  // re-laid chunks in a stage
     static constexpr int STAGE_RAW = SFT_OFF + SFT_A + SFT_B;
     static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
-    static constexpr int STAGES = TBN == 256 ? 3 : PMN_GEMM_STAGES;
+    static constexpr int STAGES = TBN == 256 ? 3 : (KIND == KIND_MXFP8 ? PMN_GEMM_STAGES_MXFP8 : PMN_GEMM_STAGES);
     static constexpr int EPI = TBN == 256 ? 2 : EPI_BUFS;  // epilogue staging buffers per warp
     static constexpr int ACC = TBN == 256 ? 1 : 2;
     static constexpr uint32_t SF_COL0 = ACC * TBN;  // scale factors live after the accumulators
     static constexpr uint32_t SFA_COLS = 4 * SFT_CHUNKS, SFB_COLS = 4 * SFT_CHUNKS * RB;
     static constexpr uint32_t SF_COLS_STAGE = SFA_COLS + SFB_COLS;
     static constexpr int SMEM_BYTES =
-        1024 + STAGES * STAGE_BYTES + 4 * EPI * STAGE_OUT_BYTES + 1024 + 2 * (MAX_GROUPS + 1) * 4;
+        1024 + STAGES * STAGE_BYTES + 4 * EPI * STAGE_OUT_BYTES + 1024 + (MAX_GROUPS + 1) * 4;
     static_assert(SF_COL0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -149,7 +155,7 @@ __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id)
 // stepping forward from the group of the previous lookup (a few shared-memory
 // reads, against a binary search on the critical path between tiles).
 template <int KIND, int TBN>
-__device__ __forceinline__ Tile get_tile(int t, const GemmArgs &p, const int *s_off, const int *s_cum, int &gc)
+__device__ __forceinline__ Tile get_tile(int t, const GemmArgs &p, const int *s_cum, int &gc)
 {
     int lo = gc;
     if (s_cum[lo] > t) lo = 0;  // not monotone: restart from the first group
@@ -161,9 +167,9 @@ __device__ __forceinline__ Tile get_tile(int t, const GemmArgs &p, const int *s_
     if (!p.group_k) {
         const int nt = (int)(p.n / TBN);
         const int mi = local / nt, ni = local - mi * nt;  // consecutive tiles: adjacent N-tiles (cluster peers)
-        ti.m0 = s_off[lo] + (int64_t)mi * BM;
+        ti.m0 = __ldg(p.offsets + lo) + (int64_t)mi * BM;
         ti.n0 = (int64_t)ni * TBN;
-        ti.row_end = s_off[lo + 1];
+        ti.row_end = __ldg(p.offsets + lo + 1);
         ti.kb = 0;
         ti.ke = p.k;
     } else {
@@ -172,8 +178,8 @@ __device__ __forceinline__ Tile get_tile(int t, const GemmArgs &p, const int *s_
         ti.m0 = (int64_t)mi * BM;
         ti.n0 = (int64_t)ni * TBN;
         ti.row_end = p.m;
-        ti.kb = s_off[lo];
-        ti.ke = s_off[lo + 1];
+        ti.kb = __ldg(p.offsets + lo);
+        ti.ke = __ldg(p.offsets + lo + 1);
     }
     const int64_t kbytes = KIND == KIND_NVFP4 ? (ti.ke - ti.kb) / 2 : (ti.ke - ti.kb);
     ti.nks = (int)((kbytes + 127) / 128);
@@ -237,8 +243,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 5);
     int *s_abort = reinterpret_cast<int *>(tmem_slot + 1);
     int *s_total = s_abort + 1;
-    int *s_off = reinterpret_cast<int *>(staging + 4 * C::EPI * STAGE_OUT_BYTES + 1024);
-    int *s_cum = s_off + (MAX_GROUPS + 1);
+    int *s_cum = reinterpret_cast<int *>(staging + 4 * C::EPI * STAGE_OUT_BYTES + 1024);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Cluster of CS CTAs along N: consecutive tiles (same expert and M-tile,
@@ -275,27 +280,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (threadIdx.x == 32) {
         // per-group tile counts and their prefix (tile -> group lookup); the
-        // offsets are checked first (monotone, in range, K segments 32-aligned
-        // so every TMA coordinate stays 16-byte aligned) -- bad offsets run
-        // no tile and latch PMN_DEVERR_BAD_OFFSETS.
+        // offsets are checked first (monotone, in range, K segments 128-aligned
+        // so every stage's scale bytes sit in one 16-byte box) -- bad offsets
+        // run no tile and latch PMN_DEVERR_BAD_OFFSETS.  Tiles read the
+        // offsets themselves from global memory (cached).
         int cum = 0;
         bool good = true;
         const int64_t limit = p.group_k ? p.k : p.m;
+        int prev = 0;
         for (int gi = 0; gi <= p.groups; ++gi) {
-            s_off[gi] = p.offsets[gi];
-            if (s_off[gi] < 0 || s_off[gi] > limit || (gi > 0 && s_off[gi] < s_off[gi - 1])) good = false;
-            if (p.group_k && (s_off[gi] & 31)) good = false;
+            const int o = p.offsets[gi];
+            if (o < 0 || o > limit || (gi > 0 && o < prev)) good = false;
+            if (p.group_k && (o & 127)) good = false;
+            prev = o;
         }
-        for (int gi = 0; gi < p.groups; ++gi) {
+        for (int gi = 0; gi < p.groups && good; ++gi) {
             s_cum[gi] = cum;
             if (!p.group_k) {
-                int rows = s_off[gi + 1] - s_off[gi];
+                int rows = p.offsets[gi + 1] - p.offsets[gi];
                 cum += ((rows + BM - 1) / BM) * (int)(p.n / TBN);
             } else {
                 cum += (int)(p.m / BM) * (int)(p.n / TBN);
             }
         }
-        s_cum[p.groups] = cum;
+        if (good) s_cum[p.groups] = cum;
         *s_total = good ? cum : 0;
         if (!good && blockIdx.x == 0) latch_error(PMN_DEVERR_BAD_OFFSETS);
     }
@@ -313,7 +321,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t issued = 0, last_parity = 0;
             int n_issued = 0, gc = 0;
             for (int t = blockIdx.x; t < total && !*(volatile int *)s_abort; t += gridDim.x) {
-                const Tile ti = get_tile<KIND, TBN>(t, p, s_off, s_cum, gc);
+                const Tile ti = get_tile<KIND, TBN>(t, p, s_cum, gc);
                 const int64_t brow = p.group_k ? ti.n0 : (int64_t)ti.g * p.n + ti.n0;
                 for (int ks = 0; ks < ti.nks; ++ks) {
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1)) {
@@ -325,8 +333,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ++n_issued;
                     uint8_t *st = stages + stage * C::STAGE_BYTES;
                     const uint32_t fb = bar_full + 8 * stage;
-                    const uint32_t raw_w = (KIND == KIND_NVFP4 || !p.group_k) ? 16u : 32u;  // raw scale box
-                    mbar_arrive_expect_tx(fb, A_TILE_BYTES + C::B_TILE_BYTES + (C::SF_TMA ? (128u + TBN) * raw_w : 0u));
+                    mbar_arrive_expect_tx(fb, A_TILE_BYTES + C::B_TILE_BYTES + (C::SF_TMA ? (128u + TBN) * 16u : 0u));
                     // 128 bytes of K per stage: 256 fp4 or 128 fp8 values
                     const int32_t xk = (int32_t)(KIND == KIND_NVFP4 ? (int64_t)ks * 128 : ti.kb + (int64_t)ks * 128);
                     if (CS > 1)
@@ -336,7 +343,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tma_load_2d(smem_u32(st), &tmA, fb, xk, (int32_t)ti.m0);
                     tma_load_2d(smem_u32(st + A_TILE_BYTES), &tmB, fb, xk, (int32_t)brow);
                     if (C::SF_TMA) {
-                        // raw scale rows; MXFP8 K-grouped boxes start 16-byte aligned below the segment
+                        // raw scale rows: 16-byte boxes (the MXFP8 stage's 4 bytes at (xk / 32) % 16)
                         const int32_t xs = KIND == KIND_NVFP4 ? ks * 16 : (int32_t)((xk / 32) & ~int32_t(15));
                         tma_load_2d(smem_u32(st + A_TILE_BYTES + C::B_TILE_BYTES), &tmSA, fb, xs, (int32_t)ti.m0);
                         tma_load_2d(smem_u32(st + A_TILE_BYTES + C::B_TILE_BYTES + C::RAW_A), &tmSB, fb, xs,
@@ -363,12 +370,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // Raw rows arrive with the stage's TMA data: wait for it, re-lay.
             // Warp 2 owns the even stage slots, warp 3 the odd ones.
             const uint32_t mine = (uint32_t)(warp - 2);
-            const int raw_w = (KIND == KIND_NVFP4 || !p.group_k) ? 16 : 32;
+            constexpr int raw_w = 16;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             int n_seq = 0, gc = 0;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile ti = get_tile<KIND, TBN>(t, p, s_off, s_cum, gc);
+                const Tile ti = get_tile<KIND, TBN>(t, p, s_cum, gc);
                 for (int ks = 0; ks < ti.nks; ++ks) {
                     const int seq = n_seq++;
                     if ((stage & 1u) != mine) {
@@ -392,7 +399,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint8_t *rawA = st + A_TILE_BYTES + C::B_TILE_BYTES, *rawB = rawA + C::RAW_A;
                     uint8_t *sftA = st + C::SFT_OFF, *sftB = sftA + C::SFT_A;
                     // operand op, 128-row block h: chunks at sft + (c * blocks + h) * 512
-    #pragma unroll
+#pragma unroll
                     for (int blk = 0; blk < 1 + C::RB; ++blk) {
                         const int op = blk == 0 ? 0 : 1, h = blk == 0 ? 0 : blk - 1;
                         const uint8_t *raw = (op ? rawB : rawA) + h * 128 * raw_w;
@@ -400,7 +407,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const int cstride = (op ? C::RB : 1) * 512;
                         if (KIND == KIND_NVFP4) {
                             uint4 w[4];
-    #pragma unroll
+#pragma unroll
                             for (int j = 0; j < 4; ++j)
                                 w[j] = *reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * 16);
 #pragma unroll
@@ -408,23 +415,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 *reinterpret_cast<uint4 *>(sft + c * cstride + lane * 16) =
                                     make_uint4(u4_word(w[0], c), u4_word(w[1], c), u4_word(w[2], c), u4_word(w[3], c));
                         } else {
+                            // the stage's 4 scale bytes: word ((k0 / 32) % 16) / 4 of the raw row
                             const int64_t k0 = ti.kb + (int64_t)ks * 128;
-                            const int rem = (int)((k0 / 32) & 15);  // offset of the stage's 4 scales in the raw row
-                            const int wsel = rem >> 2, sh = (rem & 3) * 8;  // warp-uniform
+                            const int wsel = (int)((k0 / 32) & 15) >> 2;  // warp-uniform
                             uint32_t v[4];
-    #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const uint4 *rw = reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * raw_w);
-                                const uint4 a0 = rw[0], a1 = raw_w == 32 ? rw[1] : a0;
-                                uint32_t lo, hi;
-                                switch (wsel) {
-                                    case 0: lo = a0.x; hi = a0.y; break;
-                                    case 1: lo = a0.y; hi = a0.z; break;
-                                    case 2: lo = a0.z; hi = a0.w; break;
-                                    default: lo = a0.w; hi = a1.x; break;
-                                }
-                                v[j] = sh ? __funnelshift_r(lo, hi, sh) : lo;
-                            }
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                v[j] = u4_word(*reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * raw_w), wsel);
                             *reinterpret_cast<uint4 *>(sft + lane * 16) = make_uint4(v[0], v[1], v[2], v[3]);
                         }
                     }
@@ -458,12 +455,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 while (it.t < total && it.ks >= it.ti.nks) {
                     it.t += gridDim.x;
                     it.ks = 0;
-                    if (it.t < total) it.ti = get_tile<KIND, TBN>(it.t, p, s_off, s_cum, it.gc);
+                    if (it.t < total) it.ti = get_tile<KIND, TBN>(it.t, p, s_cum, it.gc);
                 }
             };
             auto fetch = [&](const It &it, uint32_t (&v)[NR][W]) {
                 const int64_t brow = p.group_k ? it.ti.n0 : (int64_t)it.ti.g * p.n + it.ti.n0;
-    #pragma unroll
+#pragma unroll
                 for (int j = 0; j < NR; ++j) {
                     const bool opa = j < 4;
                     const int64_t row = opa ? it.ti.m0 + lane + 32 * j : brow + lane + 32 * (j - 4);
@@ -495,7 +492,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             };
             // stages of this warp, in order: f is the next one to fetch
             It f{(int)blockIdx.x, 0, 0, Tile{}};
-            if (f.t < total) f.ti = get_tile<KIND, TBN>(f.t, p, s_off, s_cum, f.gc);
+            if (f.t < total) f.ti = get_tile<KIND, TBN>(f.t, p, s_cum, f.gc);
             settle(f);
             uint32_t fseq = 0;
             if (mine) {
@@ -534,14 +531,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) PMN_TRACE_POINT(1, quse);
                 uint8_t *sftA = stages + stage * C::STAGE_BYTES + C::SFT_OFF;
                 uint8_t *sftB = sftA + C::SFT_A;
-    #pragma unroll
+#pragma unroll
                 for (int blk = 0; blk < 1 + C::RB; ++blk) {
                     // operand block: A, or 128-row block h of B; chunk c at
                     // sft + (c * blocks + h) * 512
                     uint8_t *sft = blk == 0 ? sftA : sftB + (blk - 1) * 512;
                     const int cstride = (blk == 0 ? 1 : C::RB) * 512;
                     const int j0 = 4 * blk;
-    #pragma unroll
+#pragma unroll
                     for (int c = 0; c < C::SFT_CHUNKS; ++c)
                         *reinterpret_cast<uint4 *>(sft + c * cstride + lane * 16) =
                             make_uint4(use[j0][c], use[j0 + 1][c], use[j0 + 2][c], use[j0 + 3][c]);
@@ -585,7 +582,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int gc = 0;
             auto next_tile = [&](int t0, Tile &out) {
                 for (int tt = t0; tt < total; tt += gridDim.x) {
-                    out = get_tile<KIND, TBN>(tt, p, s_off, s_cum, gc);
+                    out = get_tile<KIND, TBN>(tt, p, s_cum, gc);
                     if (out.nks > 0) return tt;
                 }
                 return total;
@@ -676,7 +673,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t abuf = 0, aphase = 0;
         int n_epi = 0, gc = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const Tile ti = get_tile<KIND, TBN>(t, p, s_off, s_cum, gc);
+            const Tile ti = get_tile<KIND, TBN>(t, p, s_cum, gc);
             const int64_t row = ti.m0 + 32 * q + lane;
             const bool valid = row < ti.row_end;
             if (ti.nks == 0) {
@@ -922,9 +919,7 @@ pmn_status launch_gemm_cs(const GemmMaps &ms, const CUtensorMap &o, const GemmAr
 {
     using C = Cfg<KIND, TBN>;
     CUtensorMap a, b, sa, sb;
-    // raw MXFP8 scale rows: 32-byte boxes where a K segment may start at any
-    // multiple of 32 (K-grouped); 16 bytes otherwise
-    const uint32_t raw_w = (KIND == KIND_NVFP4 || !args.group_k) ? 16u : 32u;
+    const uint32_t raw_w = 16;  // raw scale rows: one 16-byte box per row and stage
     if (!make_map(&a, ms.a.base, ms.a.width_bytes, ms.a.rows, ms.a.pitch, 128, true, BM / CS) ||
         !make_map(&b, ms.b.base, ms.b.width_bytes, ms.b.rows, ms.b.pitch, 128, true, TBN) ||
         !make_map(&sa, ms.sa.base, ms.sa.width_bytes, ms.sa.rows, ms.sa.pitch, raw_w, false, BM) ||

@@ -13,7 +13,7 @@ expert d_ff 1536):
             w2 [4096,1536] ~ N(0, 0.02^2)
   moe       16384 tokens, logits [16384,384] ~ N(0,1), top-8 (ties to the lower
             expert), routed rows sorted by expert then token, every expert
-            segment padded with zero rows to a multiple of 32; 384 experts of
+            segment padded with zero rows to a multiple of 128; 384 experts of
             w1/w2 as above
   backward  the moe layout plus dY [rows,4096] and dY1 [rows,3072] ~ N(0,1e-3^2)
   decode    64 tokens, top-8 -> 512 rows over the distinct experts hit
@@ -29,7 +29,7 @@ N_EXPERTS = 384
 TOP_K = 8
 MOE_TOKENS = 16384
 DECODE_TOKENS = 64
-PAD = 32
+PAD = 128  # expert segments: whole 128-deep K stages for the weight-gradient GEMMs
 
 
 def f32_to_bf16_bits(a):

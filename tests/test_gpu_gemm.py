@@ -177,7 +177,7 @@ def test_gemm_mxfp8_mgrouped(pmn):
 def test_gemm_mxfp8_kgrouped(pmn):
     rng = np.random.default_rng(22)
     M, N, Kt = 256, 128, 1024
-    offs = np.array([0, 96, 96, 512, 544, 1024], np.int32)  # empty, ragged (multiples of 32)
+    offs = np.array([0, 128, 128, 512, 640, 1024], np.int32)  # an empty group, ragged (multiples of 128)
     G = len(offs) - 1
     a, asc = oracle.mxfp8_quantize(W.normal_bf16_host(rng, (Kt, M), 1e-3), transpose=True)
     b, bsc = oracle.mxfp8_quantize(W.normal_bf16_host(rng, (Kt, N), 1.0), transpose=True)
@@ -191,6 +191,20 @@ def test_gemm_mxfp8_kgrouped(pmn):
         absab = np.abs(oracle.mxfp8_dequant_f64(a[:, lo:hi], asc[:, lo // 32:hi // 32])) @ np.abs(
             oracle.mxfp8_dequant_f64(b[:, lo:hi], bsc[:, lo // 32:hi // 32])).T
         check_mx(out[g], ref[g], absab, "mxfp8 K-grouped g=%d" % g)
+
+
+def test_gemm_mxfp8_kgrouped_rejects_unaligned_segments(pmn):
+    """K segments must start on 128-row boundaries; a 32-aligned one runs no
+    tile and latches the bad-offsets bit (checked on the device)."""
+    rng = np.random.default_rng(23)
+    M, N, Kt = 128, 128, 512
+    offs = np.array([0, 96, 512], np.int32)
+    a, asc = oracle.mxfp8_quantize(W.normal_bf16_host(rng, (Kt, M), 1e-3), transpose=True)
+    b, bsc = oracle.mxfp8_quantize(W.normal_bf16_host(rng, (Kt, N), 1.0), transpose=True)
+    pmn.gemm_mxfp8(dev(a), dev(asc), dev(b), dev(bsc), dev(offs), pmn.GROUP_K, torch.float32)
+    torch.cuda.synchronize()
+    assert pmn.get_device_error() == pmn.DEVERR_BAD_OFFSETS
+    assert pmn.get_device_error() == 0  # read and cleared
 
 
 def test_gemm_deterministic(pmn):
