@@ -705,58 +705,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int64_t obase = p.group_k ? (int64_t)ti.g * p.m : 0;
             const int64_t orow = obase + row;
             uint64_t sc_word = 0u;
-            // 128-wide tiles: read the whole accumulator slice (4 x 32 columns)
-            // before converting, so the accumulator is released to the next
-            // tile's MMAs without waiting for this tile's stores to drain.
-            constexpr int PRELOAD = TBN == 128 ? TBN / 32 : 1;
-            uint32_t pre[PRELOAD][32];
-            if (PRELOAD > 1) {
-#pragma unroll
-                for (int c = 0; c < PRELOAD; ++c)
-                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + abuf * TBN + 32 * c, pre[c]);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar_acc_empty + 8 * abuf);
-                    if (q == 0) PMN_TRACE_POINT(7, n_epi);
-                }
-            }
-#pragma unroll(PRELOAD > 1 ? TBN / 32 : 1)
-            for (int c = 0; c < TBN / 32; ++c) {
-                uint32_t r[32];
-                if (PRELOAD > 1) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = pre[PRELOAD > 1 ? c : 0][j];
-                } else {
-                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + abuf * TBN + 32 * c, r);
-                    tmem_ld_wait();
-                    if (c == TBN / 32 - 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) {
-                            mbar_arrive(bar_acc_empty + 8 * abuf);
-                            if (q == 0) PMN_TRACE_POINT(7, n_epi);
-                        }
-                    }
-                }
-                if (!slice_any) continue;
+            // The accumulator slice is read 32 columns at a time and converted
+            // to the output's bytes.  Where the converted slice fits in
+            // registers (at most 128 words a thread: bf16 tiles and 128-wide
+            // fp32 tiles) every chunk is read first and the accumulator released
+            // to the next tile's MMAs before any store; otherwise (and for the
+            // register-hungry RHT + S2F6 conversion) chunks are read, converted
+            // and stored in turn and the release follows the last read.
+            constexpr int NCH = OUT == PMN_OUT_F32 ? 8 : (OUT == PMN_OUT_BF16 ? 4 : 2);  // 16-byte pieces per chunk
+            constexpr int NC = TBN / 32;
+            constexpr bool TWO_PHASE = NC * NCH <= 32 && OUT != PMN_OUT_RHT_S2F6;
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + abuf * TBN;
+            auto convert = [&](uint32_t (&r)[32], int c, uint4 (&o)[NCH]) {
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     v[j] = __uint_as_float(r[j]);
                     if (KIND == KIND_NVFP4) v[j] = __fmul_rn(__fmul_rn(v[j], scale), gb);
                 }
-                // the 16-byte chunks this 32-column piece contributes to a 128-byte row
-                uint4 chunk[8];
-                int nch;
-                if (OUT == PMN_OUT_F32) {
+                if constexpr (OUT == PMN_OUT_F32) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        chunk[j] = make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
-                                              __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
-                    nch = 8;
-                } else if (OUT == PMN_OUT_BF16) {
+                        o[j] = make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                                          __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+                } else if constexpr (OUT == PMN_OUT_BF16) {
                     uint32_t w[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
@@ -764,16 +736,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         w[j] = *reinterpret_cast<uint32_t *>(&b2);
                     }
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) chunk[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                    nch = 4;
+                    for (int j = 0; j < 4; ++j) o[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                 } else {
                     uint32_t qv[8];
                     const uint32_t sb = rht32_s2f6(v, sigma, qv);
-                    chunk[0] = make_uint4(qv[0], qv[1], qv[2], qv[3]);
-                    chunk[1] = make_uint4(qv[4], qv[5], qv[6], qv[7]);
-                    nch = 2;
+                    o[0] = make_uint4(qv[0], qv[1], qv[2], qv[3]);
+                    o[1] = make_uint4(qv[4], qv[5], qv[6], qv[7]);
                     sc_word |= (uint64_t)sb << (8 * c);
                 }
+            };
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar_acc_empty + 8 * abuf);
+                    if (q == 0) PMN_TRACE_POINT(7, n_epi);
+                }
+            };
+            auto store = [&](int c, const uint4 (&o)[NCH]) {
                 const int part = c % CH_PER_STORE;
                 if (slice_full) {
                     uint8_t *buf = stg + (nstore % C::EPI) * STAGE_OUT_BYTES;
@@ -782,11 +762,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         __syncwarp();
                     }
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (j < nch) {
-                            const int ci = part * nch + j;
-                            *reinterpret_cast<uint4 *>(buf + lane * 128 + ((ci ^ (lane & 7)) << 4)) = chunk[j];
-                        }
+                    for (int j = 0; j < NCH; ++j) {
+                        const int ci = part * NCH + j;
+                        *reinterpret_cast<uint4 *>(buf + lane * 128 + ((ci ^ (lane & 7)) << 4)) = o[j];
+                    }
                     if (part == CH_PER_STORE - 1) {
                         fence_proxy_async_smem();
                         __syncwarp();
@@ -799,13 +778,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 } else if (valid) {
                     const int64_t col = ti.n0 + 32 * c;
-                    uint8_t *o;
-                    if (OUT == PMN_OUT_F32) o = reinterpret_cast<uint8_t *>(reinterpret_cast<float *>(p.out) + orow * p.n + col);
-                    else if (OUT == PMN_OUT_BF16) o = reinterpret_cast<uint8_t *>(reinterpret_cast<uint16_t *>(p.out) + orow * p.n + col);
-                    else o = reinterpret_cast<uint8_t *>(p.out) + orow * p.n + col;
+                    uint8_t *o8;
+                    if (OUT == PMN_OUT_F32) o8 = reinterpret_cast<uint8_t *>(reinterpret_cast<float *>(p.out) + orow * p.n + col);
+                    else if (OUT == PMN_OUT_BF16) o8 = reinterpret_cast<uint8_t *>(reinterpret_cast<uint16_t *>(p.out) + orow * p.n + col);
+                    else o8 = reinterpret_cast<uint8_t *>(p.out) + orow * p.n + col;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (j < nch) reinterpret_cast<uint4 *>(o)[j] = chunk[j];
+                    for (int j = 0; j < NCH; ++j) reinterpret_cast<uint4 *>(o8)[j] = o[j];
+                }
+            };
+            if constexpr (TWO_PHASE) {
+                uint4 ch[NC][NCH];
+                if constexpr (OUT == PMN_OUT_F32) {
+                    // fp32: the chunks' words are the output; one wait for all reads
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) tmem_ld_32x32b_x32(tbase + 32 * c, reinterpret_cast<uint32_t (&)[32]>(ch[c]));
+                    tmem_ld_wait();
+                    release();
+                    if (KIND == KIND_NVFP4) {
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) convert(reinterpret_cast<uint32_t (&)[32]>(ch[c]), c, ch[c]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(tbase + 32 * c, r);
+                        tmem_ld_wait();
+                        convert(r, c, ch[c]);
+                    }
+                    release();
+                }
+                if (slice_any) {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) store(c, ch[c]);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < NC; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + 32 * c, r);
+                    tmem_ld_wait();
+                    if (c == NC - 1) release();
+                    if (!slice_any) continue;
+                    uint4 o[NCH];
+                    convert(r, c, o);
+                    store(c, o);
                 }
             }
             if (OUT == PMN_OUT_RHT_S2F6 && valid) {
