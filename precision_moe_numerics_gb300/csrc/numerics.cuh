@@ -36,6 +36,29 @@ __device__ __forceinline__ uint32_t e2m1x2_mul_h2(uint32_t byte, uint32_t scale_
     return p;
 }
 
+// The four bytes of a code word at once (element 2k, 2k+1 of byte k in the
+// low, high half of out[k]), each times the f16x2 scale: exact as above.
+__device__ __forceinline__ void e2m1x8_mul_h2(uint32_t word, uint32_t scale_h2, uint32_t (&out)[4])
+{
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .b32 t0, t1, t2, t3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 t0, b0;\n\tcvt.rn.f16x2.e2m1x2 t1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 t2, b2;\n\tcvt.rn.f16x2.e2m1x2 t3, b3;\n\t"
+        "mul.rn.f16x2 %0, t0, %5;\n\tmul.rn.f16x2 %1, t1, %5;\n\t"
+        "mul.rn.f16x2 %2, t2, %5;\n\tmul.rn.f16x2 %3, t3, %5;\n\t}"
+        : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+        : "r"(word), "r"(scale_h2));
+}
+
+// max(|a|, |b|) per f16 half with the sign bit the XOR of the inputs' signs
+// (finite inputs); clear the sign bits to read a magnitude.
+__device__ __forceinline__ uint32_t h2_absmax_xs(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // The low / high f16 of an f16x2 word as binary32 (exact).
 __device__ __forceinline__ float h2_lo_to_f32(uint32_t h2)
 {

@@ -535,18 +535,20 @@ __device__ __forceinline__ int rq_gidx(int r) { return r + ((r >> 5) << 2); }
 // from 32 exact f16 values cs = code * S (16 f16x2 words); returns e.
 __device__ __forceinline__ int rq_group_y(const uint32_t (&hw)[16], float g, float (&y)[32])
 {
-    uint32_t m = 0u;
+    uint32_t m[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) m = __vmaxu2(m, hw[j] & 0x7FFF7FFFu);
-    const float amax_cs = fmaxf(h2_lo_to_f32(m), h2_hi_to_f32(m));
+    for (int j = 0; j < 8; ++j) m[j] = h2_absmax_xs(hw[2 * j], hw[2 * j + 1]);
+#pragma unroll
+    for (int h = 4; h >= 1; h >>= 1)
+#pragma unroll
+        for (int j = 0; j < h; ++j) m[j] = h2_absmax_xs(m[j], m[j + h]);
+    const uint32_t mm = m[0] & 0x7FFF7FFFu;
+    const float amax_cs = fmaxf(h2_lo_to_f32(mm), h2_hi_to_f32(mm));
     const int e = mx_exponent_448(__fmul_rn(amax_cs, g));
     // exact; an all-zero block keeps its signed zeros (g * 2^127 could overflow)
     const float gp = amax_cs == 0.0f ? 0.0f : __fmul_rn(g, exp2_neg(e));
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        y[2 * j] = __fmul_rn(h2_lo_to_f32(hw[j]), gp);
-        y[2 * j + 1] = __fmul_rn(h2_hi_to_f32(hw[j]), gp);
-    }
+    for (int j = 0; j < 16; ++j) mul2(h2_lo_to_f32(hw[j]), h2_hi_to_f32(hw[j]), gp, gp, y[2 * j], y[2 * j + 1]);
     return e;
 }
 
@@ -589,20 +591,20 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
     {
         const int cg = threadIdx.x & 15, rg = threadIdx.x >> 4;
         const bool col_ok = c0 + 8 * cg < cols;
+        const int64_t src0 = b * rows + r0 + 8 * rg;  // source row of i = 0
+        const uint8_t *cp = codes + src0 * cols2 + (c0 + 8 * cg) / 2;
+        const uint8_t *sp = scales + src0 * cols16 + (c0 + 8 * cg) / 16;
+        const int rows_left = (int)min((int64_t)8, rows - (r0 + 8 * rg));  // valid rows of this group
         uint32_t h2[8][4];  // row i: f16x2 pairs of columns (0,1) (2,3) (4,5) (6,7)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int64_t r = r0 + 8 * rg + i;
-            const int64_t src = b * rows + r;
             uint32_t word = 0u, sbyte = 0u;
-            if (col_ok && r < rows) {
-                word = __ldg(reinterpret_cast<const uint32_t *>(codes + src * cols2 + (c0 + 8 * cg) / 2));
-                sbyte = __ldg(scales + src * cols16 + (c0 + 8 * cg) / 16);
+            if (col_ok && i < rows_left) {
+                word = __ldg(reinterpret_cast<const uint32_t *>(cp + i * cols2));
+                sbyte = __ldg(sp + i * cols16);
             }
-            if (outer_per_row && cg == 0) gS[rq_gidx(8 * rg + i)] = r < rows ? __ldg(outer + src) : 0.0f;
-            const uint32_t dS2 = e4m3_to_h2(sbyte);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) h2[i][k] = e2m1x2_mul_h2((word >> (8 * k)) & 0xFFu, dS2);
+            if (outer_per_row && cg == 0) gS[rq_gidx(8 * rg + i)] = i < rows_left ? __ldg(outer + src0 + i) : 0.0f;
+            e2m1x8_mul_h2(word, e4m3_to_h2(sbyte), h2[i]);
         }
         // transpose: column j gets rows 0..7 as four f16x2
 #pragma unroll
@@ -645,17 +647,15 @@ __global__ void __launch_bounds__(256) requant_transpose_kernel(
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const float4 g4 = gp4[q];
-                y[4 * q] = __fmul_rn(h2_lo_to_f32(hw[2 * q]), g4.x);
-                y[4 * q + 1] = __fmul_rn(h2_hi_to_f32(hw[2 * q]), g4.y);
-                y[4 * q + 2] = __fmul_rn(h2_lo_to_f32(hw[2 * q + 1]), g4.z);
-                y[4 * q + 3] = __fmul_rn(h2_hi_to_f32(hw[2 * q + 1]), g4.w);
+                mul2(h2_lo_to_f32(hw[2 * q]), h2_hi_to_f32(hw[2 * q]), g4.x, g4.y, y[4 * q], y[4 * q + 1]);
+                mul2(h2_lo_to_f32(hw[2 * q + 1]), h2_hi_to_f32(hw[2 * q + 1]), g4.z, g4.w, y[4 * q + 2], y[4 * q + 3]);
                 amax = fmaxf(amax, fmaxf(fmaxf(fabsf(y[4 * q]), fabsf(y[4 * q + 1])),
                                          fmaxf(fabsf(y[4 * q + 2]), fabsf(y[4 * q + 3]))));
             }
             e = mx_exponent_448(amax);
             const float sc = exp2_neg(e);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) y[j] = __fmul_rn(y[j], sc);  // exact
+            for (int j = 0; j < 32; j += 2) mul2(y[j], y[j + 1], sc, sc, y[j], y[j + 1]);  // exact
         }
         const int64_t i0 = (b * cols + oc) * rows + orow0;  // output index, multiple of 32
         rq_emit(y, e, (uint64_t)i0, seed, tag, stochastic, out, out_sc + (b * cols + oc) * (rows / 32) + orow0 / 32);
