@@ -188,10 +188,6 @@ __device__ __forceinline__ Tile get_tile(int t, const GemmArgs &p, const int *s_
 
 __device__ __forceinline__ void latch_error(int bit) { atomicOr(&g_pmn_device_error, bit); }
 
-__device__ __forceinline__ uint32_t u4_word(const uint4 &v, int i)
-{
-    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
 
 // Copies a stage's re-laid scale-factor chunks from shared memory into the
 // stage's TMEM columns (A: one 32x128b.warpx4 copy per K-step; B: one per

@@ -59,6 +59,12 @@ __device__ __forceinline__ uint32_t h2_absmax_xs(uint32_t a, uint32_t b)
     return d;
 }
 
+// Word i (0..3) of a 16-byte vector (i a compile-time constant after unrolling).
+__device__ __forceinline__ uint32_t u4_word(const uint4 &v, int i)
+{
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
 // The low / high f16 of an f16x2 word as binary32 (exact).
 __device__ __forceinline__ float h2_lo_to_f32(uint32_t h2)
 {

@@ -452,53 +452,6 @@ __global__ void __launch_bounds__(256) mxfp8_quant_rowwise_kernel(const uint16_t
     (void)bpr;
 }
 
-// transposed: tile of 128 rows x 64 cols staged in shared memory; thread
-// (c, rb) quantises the 32 values of column c in row block rb.
-__global__ void __launch_bounds__(256) mxfp8_quant_transposed_kernel(const uint16_t *__restrict__ x,
-                                                                     int64_t rows, int64_t cols,
-                                                                     uint8_t *__restrict__ out,
-                                                                     uint8_t *__restrict__ out_sc)
-{
-    constexpr int TR = 128, TC = 64, PITCH = TC + 2;  // elements
-    __shared__ uint16_t tile[TR * PITCH];
-    const int64_t r0 = (int64_t)blockIdx.y * TR, c0 = (int64_t)blockIdx.x * TC;
-    // load: 128 rows x 128 bytes; thread t loads 16 bytes: row t/8 (+32k), segment t%8
-    for (int k = 0; k < 4; ++k) {
-        int rr = (threadIdx.x >> 3) + 32 * k;
-        int seg = threadIdx.x & 7;
-        uint4 q = make_uint4(0u, 0u, 0u, 0u);
-        if (r0 + rr < rows && c0 + seg * 8 < cols)
-            q = __ldg(reinterpret_cast<const uint4 *>(x + (r0 + rr) * cols + c0 + seg * 8));
-        uint32_t *dst = reinterpret_cast<uint32_t *>(tile + rr * PITCH + seg * 8);
-        dst[0] = q.x;
-        dst[1] = q.y;
-        dst[2] = q.z;
-        dst[3] = q.w;
-    }
-    __syncthreads();
-    const int c = threadIdx.x & 63, rb = threadIdx.x >> 6;
-    if (c0 + c >= cols || r0 + rb * 32 >= rows) return;
-    float v[32];
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        v[j] = __uint_as_float((uint32_t)tile[(rb * 32 + j) * PITCH + c] << 16);
-        amax = fmaxf(amax, fabsf(v[j]));
-    }
-    const int e = mx_exponent_448(amax);
-    const float sc = exp2_neg(e);
-    uint32_t o[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t lo = cvt_e4m3x2_rn(__fmul_rn(v[4 * i], sc), __fmul_rn(v[4 * i + 1], sc));
-        const uint32_t hi = cvt_e4m3x2_rn(__fmul_rn(v[4 * i + 2], sc), __fmul_rn(v[4 * i + 3], sc));
-        o[i] = lo | (hi << 16);
-    }
-    uint4 *po = reinterpret_cast<uint4 *>(out + (c0 + c) * rows + r0 + rb * 32);
-    po[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    po[1] = make_uint4(o[4], o[5], o[6], o[7]);
-    out_sc[(c0 + c) * (rows / 32) + (r0 / 32) + rb] = (uint8_t)(e + 127);
-}
 
 // ------------------------------------------------------------------ requant [SR]
 // One CTA per tile of 128 input rows x 128 input cols.
@@ -530,6 +483,79 @@ __device__ __forceinline__ int rq_chunk(int c, int logical)
 // per-row outer scales, 4 floats of padding per 32 rows so the four row-blocks
 // of a quarter-warp read different banks
 __device__ __forceinline__ int rq_gidx(int r) { return r + ((r >> 5) << 2); }
+
+// transposed MXFP8 (RN): 128 x 128 tile.  Phase 1 as in the requantisation:
+// each thread loads an 8-row x 8-column block (16-byte row pieces), transposes
+// it in registers and stores 16-byte chunks (8 rows of one column) into the
+// swizzled tile.  Phase 2: task (c, rb) forms the 32-block of output row c;
+// four consecutive lanes write one 128-byte line of the output row.
+__global__ void __launch_bounds__(256) mxfp8_quant_transposed_kernel(const uint16_t *__restrict__ x,
+                                                                     int64_t rows, int64_t cols,
+                                                                     uint8_t *__restrict__ out,
+                                                                     uint8_t *__restrict__ out_sc)
+{
+    __shared__ __align__(16) uint4 cS[RQ_T * 16];  // [c][16 chunks of 8 rows] bf16
+    const int64_t r0 = (int64_t)blockIdx.y * RQ_T, c0 = (int64_t)blockIdx.x * RQ_T;
+    {
+        const int cg = threadIdx.x & 15, rg = threadIdx.x >> 4;
+        const bool col_ok = c0 + 8 * cg < cols;
+        const int rows_left = (int)min((int64_t)8, rows - (r0 + 8 * rg));
+        const uint16_t *xp = x + (r0 + 8 * rg) * cols + c0 + 8 * cg;
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (col_ok && i < rows_left) v[i] = __ldg(reinterpret_cast<const uint4 *>(xp + i * cols));
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {  // columns 2k, 2k+1
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t a = u4_word(v[2 * i], k), bb = u4_word(v[2 * i + 1], k);
+                lo[i] = __byte_perm(a, bb, 0x5410);
+                hi[i] = __byte_perm(a, bb, 0x7632);
+            }
+            const int cl = 8 * cg + 2 * k;
+            cS[rq_chunk(cl, rg)] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            cS[rq_chunk(cl + 1, rg)] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        }
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int task = threadIdx.x; task < RQ_T * 4; task += blockDim.x) {
+        const int c = task >> 2, rb = task & 3;
+        const int64_t oc = c0 + c, orow0 = r0 + rb * 32;
+        if (oc >= cols || orow0 >= rows) continue;
+        uint32_t hw[16];  // 32 bf16 values: rows rb*32 .. rb*32+31
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint4 u = cS[rq_chunk(c, 4 * rb + k)];
+            hw[4 * k] = u.x;
+            hw[4 * k + 1] = u.y;
+            hw[4 * k + 2] = u.z;
+            hw[4 * k + 3] = u.w;
+        }
+        uint32_t m = 0u;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) m = __vmaxu2(m, hw[j] & 0x7FFF7FFFu);  // |bf16| orders as integers
+        const float amax = __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
+        const int e = mx_exponent_448(amax);
+        const float sc = exp2_neg(e);
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float p0, p1, p2, p3;
+            mul2(bf16_lo(hw[2 * i]), bf16_hi(hw[2 * i]), sc, sc, p0, p1);
+            mul2(bf16_lo(hw[2 * i + 1]), bf16_hi(hw[2 * i + 1]), sc, sc, p2, p3);
+            o[i] = cvt_e4m3x2_rn(p0, p1) | (cvt_e4m3x2_rn(p2, p3) << 16);
+        }
+        uint4 *po = reinterpret_cast<uint4 *>(out + oc * rows + orow0);
+        po[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        po[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        out_sc[oc * (rows / 32) + orow0 / 32] = (uint8_t)(e + 127);
+    }
+}
 
 // One output 32-block with a per-group outer scale g: y = cs * (g * 2^-e)
 // from 32 exact f16 values cs = code * S (16 f16x2 words); returns e.
@@ -827,7 +853,7 @@ extern "C" pmn_status pmn_mxfp8_quantize(const void *x, int64_t rows, int64_t co
         mxfp8_quant_rowwise_kernel<<<(unsigned)((nblocks + 255) / 256), 256, 0, s>>>(xb, nblocks, cols / 32, out,
                                                                                      out_scales);
     } else {
-        dim3 grid((unsigned)((cols + 63) / 64), (unsigned)((rows + 127) / 128));
+        dim3 grid((unsigned)((cols + RQ_T - 1) / RQ_T), (unsigned)((rows + RQ_T - 1) / RQ_T));
         mxfp8_quant_transposed_kernel<<<grid, 256, 0, s>>>(xb, rows, cols, out, out_scales);
     }
     return launch_status();
