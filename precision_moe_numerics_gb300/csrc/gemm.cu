@@ -101,8 +101,12 @@ struct Cfg {
     static constexpr int SFT_OFF = A_TILE_BYTES + B_TILE_BYTES + RAW_A + RAW_B;  // re-laid chunks in a stage
     static constexpr int STAGE_RAW = SFT_OFF + SFT_A + SFT_B;
     static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
-    static constexpr int STAGES = TBN == 256 ? 3 : (KIND == KIND_MXFP8 ? PMN_GEMM_STAGES_MXFP8 : PMN_GEMM_STAGES);
-    static constexpr int EPI = TBN == 256 ? 2 : EPI_BUFS;  // epilogue staging buffers per warp
+#ifndef PMN_W256_MX_STAGES  // 256-wide MXFP8 tiles: 4 stages with one epilogue staging buffer per warp
+#define PMN_W256_MX_STAGES 4
+#endif
+    static constexpr int STAGES = TBN == 256 ? (KIND == KIND_MXFP8 ? PMN_W256_MX_STAGES : 3)
+                                             : (KIND == KIND_MXFP8 ? PMN_GEMM_STAGES_MXFP8 : PMN_GEMM_STAGES);
+    static constexpr int EPI = TBN == 256 ? (STAGES == 4 ? 1 : 2) : EPI_BUFS;  // epilogue staging buffers per warp
     static constexpr int ACC = TBN == 256 ? 1 : 2;
     static constexpr uint32_t SF_COL0 = ACC * TBN;  // scale factors live after the accumulators
     static constexpr uint32_t SFA_COLS = 4 * SFT_CHUNKS, SFB_COLS = 4 * SFT_CHUNKS * RB;

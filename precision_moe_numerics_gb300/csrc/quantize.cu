@@ -276,6 +276,28 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
+// L2 cache policies (createpolicy) and 16-byte loads that carry one.
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld_l2_policy(const uint4 *ptr, uint64_t policy)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr), "l"(policy));
+    return v;
+}
+
 __global__ void __launch_bounds__(QG_THREADS, 3) nvfp4_quant_groups_kernel(
     const uint16_t *__restrict__ x, int64_t groups, int64_t blocks_per_group, int64_t nch, int64_t lead,
     int four_over_six, uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, float *__restrict__ outer,
@@ -288,6 +310,9 @@ __global__ void __launch_bounds__(QG_THREADS, 3) nvfp4_quant_groups_kernel(
     uint32_t *ticket = scratch, *done = scratch + QG_PAD, *amax = scratch + QG_PAD + groups;
     const int tid = threadIdx.x;
     const int64_t na = groups * nch, total = 2 * na, paired = na - lead;
+    // L2 priorities: amax reads stay (the coding pass re-reads them about a
+    // group later), coding reads leave
+    const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
     const bool fos = four_over_six != 0;
     if (tid == 0) s_ticket = atomicAdd(ticket, 1u);
     __syncthreads();
@@ -321,7 +346,7 @@ __global__ void __launch_bounds__(QG_THREADS, 3) nvfp4_quant_groups_kernel(
 #pragma unroll 4
                 for (int64_t b = b0 + tid; b < b1; b += QG_THREADS) {
                     const uint4 *q = reinterpret_cast<const uint4 *>(xg + b * 16);
-                    const uint4 v0 = __ldg(q), v1 = __ldg(q + 1);
+                    const uint4 v0 = ld_l2_policy(q, keep), v1 = ld_l2_policy(q + 1, keep);
                     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
                     for (int k = 0; k < 8; ++k) m = __vmaxu2(m, w[k] & 0x7FFF7FFFu);  // per 16-bit half
@@ -349,8 +374,8 @@ __global__ void __launch_bounds__(QG_THREADS, 3) nvfp4_quant_groups_kernel(
                     const int64_t bi = bb + u * QG_THREADS;
                     if (bi < b1) {
                         const uint4 *q = reinterpret_cast<const uint4 *>(xg + bi * 16);
-                        v[u][0] = __ldg(q);
-                        v[u][1] = __ldg(q + 1);
+                        v[u][0] = ld_l2_policy(q, drop);
+                        v[u][1] = ld_l2_policy(q + 1, drop);
                     }
                 }
             };
