@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(256) nvfp4_quant_rows_kernel(
 // B waits (bounded) for its group's A count; no A item ever waits, so the
 // streams progress whatever the number of resident CTAs.
 constexpr int QG_THREADS = 256;
-constexpr int QG_CHUNK = 4096;  // 16-blocks per work item (64 Ki values)
+constexpr int QG_CHUNK = 2048;  // 16-blocks per work item (32 Ki values)
 constexpr int QG_PAD = 64;      // the ticket sits alone in its 256-byte line
 
 // scratch words: [0] ticket, [QG_PAD + g] done count of A(g, *),
@@ -808,8 +808,10 @@ pmn_status launch_quant_groups(const uint16_t *x, int64_t groups, int64_t blocks
         grid = std::max(1, sms * per_sm);
     }
     const int64_t nch = (blocks_per_group + QG_CHUNK - 1) / QG_CHUNK;
-    // one group plus one item per CTA (measured best of 0, 1 and 2 per CTA)
-    const int64_t lead = std::min(groups * nch, nch + (int64_t)grid);
+    // one group plus three quarters of an item per CTA: measured best with
+    // the L2 priorities above (a longer lead pushes re-reads out of L2, a
+    // shorter one makes coding items wait)
+    const int64_t lead = std::min(groups * nch, nch + (int64_t)grid * 3 / 4);
     nvfp4_quant_groups_kernel<<<(unsigned)grid, QG_THREADS, 0, s>>>(x, groups, blocks_per_group, nch, lead,
                                                                      four_over_six, codes, scales, outer, scratch);
     return launch_status();
