@@ -986,14 +986,19 @@ pmn_status launch_gemm_tbn(const GemmMaps &ms, const CUtensorMap &o, const GemmA
 }
 
 // Tile width: 256 columns (N = 256 MMAs, half the operand traffic per
-// output) for M-grouped problems whose N is a multiple of 256; 128 otherwise
-// (K-grouped gradients: short per-expert K, double-buffered accumulators).
+// output) for M-grouped problems whose N is a multiple of 256 and whose
+// epilogue is a plain conversion; 128 otherwise (K-grouped gradients: short
+// per-expert K; the RHT + S2F6 epilogue), with double-buffered accumulators.
 // Cluster size: the largest of 4, 2, 1 (capped by PMN_GEMM_CLUSTER_MAX) that
 // divides the number of N-tiles.
 template <int KIND, int OUT>
 pmn_status launch_gemm(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
 {
-    if (PMN_GEMM_WIDE_M && !args.group_k && args.n % 256 == 0) return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);
+    // 256-wide M-grouped tiles except under the RHT + S2F6 epilogue, whose
+    // conversion is long enough that overlapping it with the next tile's MMAs
+    // (two 128-wide accumulators) beats the halved A traffic
+    if (PMN_GEMM_WIDE_M && OUT != PMN_OUT_RHT_S2F6 && !args.group_k && args.n % 256 == 0)
+        return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);
     return launch_gemm_tbn<KIND, OUT, 128>(ms, o, args, s);
 }
 
