@@ -11,6 +11,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/pmn.h"
 #include "numerics.cuh"
@@ -558,9 +559,6 @@ __device__ __forceinline__ int rq_chunk(int c, int logical)
 {
     return c * 16 + (logical ^ ((c ^ (c >> 3)) & 7) ^ ((logical >> 3) << 1));
 }
-// per-row outer scales, 4 floats of padding per 32 rows so the four row-blocks
-// of a quarter-warp read different banks
-__device__ __forceinline__ int rq_gidx(int r) { return r + ((r >> 5) << 2); }
 
 // transposed MXFP8 (RN): 128 x 128 tile.  Phase 1 as in the requantisation:
 // each thread loads an 8-row x 8-column block (16-byte row pieces), transposes
@@ -635,134 +633,199 @@ __global__ void __launch_bounds__(256) mxfp8_quant_transposed_kernel(const uint1
     }
 }
 
-// One output 32-block with a per-group outer scale g: y = cs * (g * 2^-e)
-// from 32 exact f16 values cs = code * S (16 f16x2 words); returns e.
-__device__ __forceinline__ int rq_group_y(const uint32_t (&hw)[16], float g, float (&y)[32])
+// Two E2M1 codes (byte K of `word`) decoded by the hardware to f16x2 and
+// multiplied by an E4M3 scale held as f16x2: exact, as in e2m1x8_mul_h2.
+template <int K>
+__device__ __forceinline__ uint32_t e2m1x2_byte_mul_h2(uint32_t word, uint32_t scale_h2)
 {
-    uint32_t m[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) m[j] = h2_absmax_xs(hw[2 * j], hw[2 * j + 1]);
-#pragma unroll
-    for (int h = 4; h >= 1; h >>= 1)
-#pragma unroll
-        for (int j = 0; j < h; ++j) m[j] = h2_absmax_xs(m[j], m[j + h]);
-    const uint32_t mm = m[0] & 0x7FFF7FFFu;
-    const float amax_cs = fmaxf(h2_lo_to_f32(mm), h2_hi_to_f32(mm));
-    const int e = mx_exponent_448(__fmul_rn(amax_cs, g));
-    // exact; an all-zero block keeps its signed zeros (g * 2^127 could overflow)
-    const float gp = amax_cs == 0.0f ? 0.0f : __fmul_rn(g, exp2_neg(e));
-#pragma unroll
-    for (int j = 0; j < 16; ++j) mul2(h2_lo_to_f32(hw[j]), h2_hi_to_f32(hw[j]), gp, gp, y[2 * j], y[2 * j + 1]);
-    return e;
+    uint32_t h2, p;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b%2;\n\t}"
+        : "=r"(h2) : "r"(word), "n"(K));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(p) : "r"(h2), "r"(scale_h2));
+    return p;
 }
 
-// E4M3 bytes of one output 32-block (output elements i0 .. i0+31, i0 a
-// multiple of 32): hardware stochastic rounding fed with the Philox words of
-// elements 16j .. 16j+15, or round-to-nearest-even; then its E8M0 byte.
-__device__ __forceinline__ void rq_emit(const float (&y)[32], int e, uint64_t i0, uint64_t seed, uint32_t tag,
-                                        int stochastic, uint8_t *out, uint8_t *sc)
+// Philox4x32-10 for counters whose high word is shared by a whole thread: the
+// first round's product of the tag and the second round's product of the
+// resulting first word depend only on (tag, high word, key), so they are
+// formed once per thread.  Same arithmetic as philox4x32_10.
+struct PhiloxPrefix {
+    uint32_t k0, k1, y1, x2hi, x2lo;  // see philox_from_prefix
+};
+
+__device__ __forceinline__ PhiloxPrefix philox_prefix(uint64_t seed, uint32_t tag, uint32_t jhi)
 {
-    uint32_t o[8];
-    if (stochastic) {
-        const uint4 wa = sr_words16(seed, tag, i0 >> 4);
-        const uint4 wb = sr_words16(seed, tag, (i0 >> 4) + 1);
-        const uint32_t wd[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+    PhiloxPrefix p;
+    p.k0 = (uint32_t)seed;
+    p.k1 = (uint32_t)(seed >> 32);
+    const uint64_t t1 = (uint64_t)0xCD9E8D57u * tag;  // round 1, second product
+    const uint32_t x1 = (uint32_t)(t1 >> 32) ^ jhi ^ p.k0;  // round 1 output word 0
+    p.y1 = (uint32_t)t1;                                  // round 1 output word 1
+    const uint64_t t2 = (uint64_t)0xD2511F53u * x1;       // round 2, first product
+    p.x2hi = (uint32_t)(t2 >> 32);
+    p.x2lo = (uint32_t)t2;
+    return p;
+}
+
+__device__ __forceinline__ uint4 philox_from_prefix(const PhiloxPrefix &p, uint32_t jlo)
+{
+    // round 1: c = (jlo, jhi, tag, 0)
+    const uint64_t a1 = (uint64_t)0xD2511F53u * jlo;
+    const uint32_t z1 = (uint32_t)(a1 >> 32) ^ p.k1, w1 = (uint32_t)a1;
+    // round 2: c = (x1, y1, z1, w1) with keys bumped once
+    const uint32_t k0 = p.k0 + 0x9E3779B9u, k1 = p.k1 + 0xBB67AE85u;
+    const uint64_t b2 = (uint64_t)0xCD9E8D57u * z1;
+    uint4 c = make_uint4((uint32_t)(b2 >> 32) ^ p.y1 ^ k0, (uint32_t)b2, p.x2hi ^ w1 ^ k1, p.x2lo);
+    uint32_t q0 = k0, q1 = k1;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) o[k] = cvt_e4m3x4_rs(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3], wd[k]);
-    } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            o[k] = cvt_e4m3x2_rn(y[4 * k], y[4 * k + 1]) | (cvt_e4m3x2_rn(y[4 * k + 2], y[4 * k + 3]) << 16);
+    for (int r = 2; r < 10; ++r) {
+        q0 += 0x9E3779B9u;
+        q1 += 0xBB67AE85u;
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ q0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ q1, (uint32_t)p0);
     }
-    uint4 *po = reinterpret_cast<uint4 *>(out + i0);
-    po[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    po[1] = make_uint4(o[4], o[5], o[6], o[7]);
-    *sc = (uint8_t)(e + 127);
+    return c;
 }
 
-__global__ void __launch_bounds__(256) requant_transpose_kernel(
+// Requantisation of an NVFP4 tensor [batch, rows, cols] to MXFP8 of its
+// transpose [batch, cols, rows].  CTA = 4 warps = a 128-row x 128-column
+// tile.  Thread = 16 input rows x 8 input columns; lanes l and l ^ 16 hold the
+// two halves of a 32-row block, so each input column's values are half of one
+// output 32-block: its amax takes one shuffle, its 16 elements are one Philox
+// counter (16j .. 16j+15) and its bytes one 16-byte chunk.  The chunks are
+// staged in shared memory ([output row][8 chunks], chunk index XOR bits 3..5 of
+// the output row: conflict-free both ways) and written as whole 128-byte lines
+// after one barrier.  COLS > 0 fixes the row length at compile time so the 16
+// row loads use immediate offsets.
+template <bool PER_ROW, int COLS>
+__global__ void __launch_bounds__(128) requant_transpose_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, const float *__restrict__ outer,
-    int outer_per_row, int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, int stochastic,
+    int64_t rows, int64_t cols_rt, uint64_t seed, uint32_t tag, int stochastic,
     uint8_t *__restrict__ out, uint8_t *__restrict__ out_sc)
 {
-    __shared__ __align__(16) uint4 cS[RQ_T * 16];  // [c][16 chunks of 8 rows] f16
-    __shared__ __align__(16) float gS[RQ_T + RQ_T / 8];  // per-row outer scales (activations)
+    __shared__ __align__(16) uint4 oS[128 * 8];  // [output row][16-row chunk ^ swizzle]
+    __shared__ __align__(4) uint8_t scS[128 * 4];  // [output row][32-row block]: E8M0 bytes
+    const int64_t cols = COLS > 0 ? (int64_t)COLS : cols_rt;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, q = lane & 15, hf = lane >> 4;
     const int64_t b = blockIdx.z;
-    const int64_t r0 = (int64_t)blockIdx.y * RQ_T, c0 = (int64_t)blockIdx.x * RQ_T;
+    const int64_t r0 = (int64_t)blockIdx.y * 128, c0 = (int64_t)blockIdx.x * 128;
+    const int64_t rb0 = r0 + 32 * w;  // the warp's 32-row block
+    const int64_t col0 = c0 + 8 * q;
+    const bool active = rb0 < rows && col0 < cols;  // lanes l, l ^ 16 agree
+    const unsigned act = __ballot_sync(0xFFFFFFFFu, active);
+    if (active) {
+    const int64_t row0 = rb0 + 16 * hf;
     const int64_t cols2 = cols / 2, cols16 = cols / 16;
-    const float g_batch = outer_per_row ? 0.0f : __ldg(outer + b);
-    // ---- phase 1: rows 8rg .. 8rg+7, columns 8cg .. 8cg+7
-    {
-        const int cg = threadIdx.x & 15, rg = threadIdx.x >> 4;
-        const bool col_ok = c0 + 8 * cg < cols;
-        const int64_t src0 = b * rows + r0 + 8 * rg;  // source row of i = 0
-        const uint8_t *cp = codes + src0 * cols2 + (c0 + 8 * cg) / 2;
-        const uint8_t *sp = scales + src0 * cols16 + (c0 + 8 * cg) / 16;
-        const int rows_left = (int)min((int64_t)8, rows - (r0 + 8 * rg));  // valid rows of this group
-        uint32_t h2[8][4];  // row i: f16x2 pairs of columns (0,1) (2,3) (4,5) (6,7)
+    const uint8_t *cp = codes + (b * rows + row0) * cols2 + col0 / 2;
+    const uint8_t *sp = scales + (b * rows + row0) * cols16 + col0 / 16;
+    uint32_t word[16], s2[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint32_t word = 0u, sbyte = 0u;
-            if (col_ok && i < rows_left) {
-                word = __ldg(reinterpret_cast<const uint32_t *>(cp + i * cols2));
-                sbyte = __ldg(sp + i * cols16);
-            }
-            if (outer_per_row && cg == 0) gS[rq_gidx(8 * rg + i)] = i < rows_left ? __ldg(outer + src0 + i) : 0.0f;
-            e2m1x8_mul_h2(word, e4m3_to_h2(sbyte), h2[i]);
+    for (int i = 0; i < 16; ++i) word[i] = __ldg(reinterpret_cast<const uint32_t *>(cp + i * cols2));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s2[i] = e4m3_to_h2(__ldg(sp + i * cols16));
+    float g[PER_ROW ? 16 : 1];
+    if (PER_ROW) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) g[i] = __ldg(outer + b * rows + row0 + i);
+    } else {
+        g[0] = __ldg(outer + b);
+    }
+    // Philox counter of (column col0, rows row0 .. row0+15); column col0 + c adds c * rows / 16
+    const uint64_t j0 = (uint64_t)((b * cols + col0) * rows + row0) >> 4;
+    const uint64_t jstep = (uint64_t)rows >> 4;
+    const uint32_t jhi0 = (uint32_t)(j0 >> 32);
+    const bool one_hi = (uint32_t)((j0 + 7 * jstep) >> 32) == jhi0;
+    const PhiloxPrefix pre = philox_prefix(seed, tag, jhi0);
+    const int chunk = (2 * w + hf) ^ (q & 7);  // output rows 8q .. 8q+7 share bits 3..5
+    auto emit = [&](int c, const float (&y)[16], int e) {
+        const uint64_t j = j0 + (uint64_t)c * jstep;
+        uint32_t o[4];
+        if (stochastic) {
+            const uint4 wd = one_hi ? philox_from_prefix(pre, (uint32_t)j) : sr_words16(seed, tag, j);
+            o[0] = cvt_e4m3x4_rs(y[0], y[1], y[2], y[3], wd.x);
+            o[1] = cvt_e4m3x4_rs(y[4], y[5], y[6], y[7], wd.y);
+            o[2] = cvt_e4m3x4_rs(y[8], y[9], y[10], y[11], wd.z);
+            o[3] = cvt_e4m3x4_rs(y[12], y[13], y[14], y[15], wd.w);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                o[k] = cvt_e4m3x2_rn(y[4 * k], y[4 * k + 1]) | (cvt_e4m3x2_rn(y[4 * k + 2], y[4 * k + 3]) << 16);
         }
-        // transpose: column j gets rows 0..7 as four f16x2
+        oS[(8 * q + c) * 8 + chunk] = make_uint4(o[0], o[1], o[2], o[3]);
+        if (hf == 0) scS[(8 * q + c) * 4 + w] = (uint8_t)(e + 127);
+    };
+    auto column_pair = [&](auto kc) {
+        constexpr int K = decltype(kc)::value;
+        uint32_t cs[16];  // exact code * S of columns 2K (low halves) and 2K + 1 (high halves)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            uint32_t lo[4], hi[4];  // columns 2k and 2k+1
+        for (int i = 0; i < 16; ++i) cs[i] = e2m1x2_byte_mul_h2<K>(word[i], s2[i]);
+        if (!PER_ROW) {
+            uint32_t m[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                lo[i] = __byte_perm(h2[2 * i][k], h2[2 * i + 1][k], 0x5410);
-                hi[i] = __byte_perm(h2[2 * i][k], h2[2 * i + 1][k], 0x7632);
+            for (int i = 0; i < 8; ++i) m[i] = h2_absmax_xs(cs[2 * i], cs[2 * i + 1]);
+#pragma unroll
+            for (int h = 4; h >= 1; h >>= 1)
+#pragma unroll
+                for (int i = 0; i < h; ++i) m[i] = h2_absmax_xs(m[i], m[i + h]);
+            const uint32_t mm = h2_absmax_xs(m[0], __shfl_xor_sync(act, m[0], 16)) & 0x7FFF7FFFu;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const float amax_cs = hf ? h2_hi_to_f32(mm) : h2_lo_to_f32(mm);
+                const int e = mx_exponent_448(__fmul_rn(amax_cs, g[0]));
+                // exact; an all-zero block keeps its signed zeros (g * 2^127 could overflow)
+                const float gp = amax_cs == 0.0f ? 0.0f : __fmul_rn(g[0], exp2_neg(e));
+                float y[16];
+#pragma unroll
+                for (int i = 0; i < 16; i += 2) {
+                    const float a0 = hf ? h2_hi_to_f32(cs[i]) : h2_lo_to_f32(cs[i]);
+                    const float a1 = hf ? h2_hi_to_f32(cs[i + 1]) : h2_lo_to_f32(cs[i + 1]);
+                    mul2(a0, a1, gp, gp, y[i], y[i + 1]);
+                }
+                emit(2 * K + hf, y, e);
             }
-            const int cl = 8 * cg + 2 * k;
-            cS[rq_chunk(cl, rg)] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            cS[rq_chunk(cl + 1, rg)] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        } else {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float y[16], amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 16; i += 2) {
+                    const float a0 = hf ? h2_hi_to_f32(cs[i]) : h2_lo_to_f32(cs[i]);
+                    const float a1 = hf ? h2_hi_to_f32(cs[i + 1]) : h2_lo_to_f32(cs[i + 1]);
+                    mul2(a0, a1, g[i], g[i + 1], y[i], y[i + 1]);
+                    amax = fmaxf(amax, fmaxf(fabsf(y[i]), fabsf(y[i + 1])));
+                }
+                amax = fmaxf(amax, __shfl_xor_sync(act, amax, 16));
+                const int e = mx_exponent_448(amax);
+                const float sc = exp2_neg(e);
+#pragma unroll
+                for (int i = 0; i < 16; i += 2) mul2(y[i], y[i + 1], sc, sc, y[i], y[i + 1]);  // exact
+                emit(2 * K + hf, y, e);
+            }
         }
+    };
+    column_pair(std::integral_constant<int, 0>());
+    column_pair(std::integral_constant<int, 1>());
+    column_pair(std::integral_constant<int, 2>());
+    column_pair(std::integral_constant<int, 3>());
     }
     __syncthreads();
-    // ---- phase 2: 128 output rows x 4 row-blocks = 512 tasks, 2 per thread;
-    // four consecutive lanes cover one 128-byte line of an output row.
-#pragma unroll 1
-    for (int task = threadIdx.x; task < RQ_T * 4; task += blockDim.x) {
-        const int c = task >> 2, rb = task & 3;
-        const int64_t oc = c0 + c, orow0 = r0 + rb * 32;
-        if (oc >= cols || orow0 >= rows) continue;
-        uint32_t hw[16];  // 32 f16 values: rows rb*32 .. rb*32+31
+    // whole lines: 8 consecutive threads write the 128 bytes of one output row
+    const int rows_here = (int)min((int64_t)128, rows - r0), cols_here = (int)min((int64_t)128, cols - c0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint4 u = cS[rq_chunk(c, 4 * rb + k)];
-            hw[4 * k] = u.x;
-            hw[4 * k + 1] = u.y;
-            hw[4 * k + 2] = u.z;
-            hw[4 * k + 3] = u.w;
-        }
-        float y[32];
-        int e;
-        if (!outer_per_row) {
-            e = rq_group_y(hw, g_batch, y);
+    for (int it = 0; it < 8; ++it) {
+        const int idx = it * 128 + threadIdx.x, c = idx >> 3, ch = idx & 7;
+        if (c < cols_here && 16 * ch < rows_here)
+            *reinterpret_cast<uint4 *>(out + (b * cols + c0 + c) * rows + r0 + 16 * ch) = oS[c * 8 + (ch ^ ((c >> 3) & 7))];
+    }
+    if ((int)threadIdx.x < cols_here) {
+        const int c = threadIdx.x;
+        uint8_t *dst = out_sc + (b * cols + c0 + c) * (rows / 32) + r0 / 32;
+        if (rows_here == 128 && ((reinterpret_cast<uintptr_t>(dst) & 3u) == 0)) {
+            *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(scS + 4 * c);
         } else {
-            float amax = 0.0f;
-            const float4 *gp4 = reinterpret_cast<const float4 *>(gS + rq_gidx(rb * 32));
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 g4 = gp4[q];
-                mul2(h2_lo_to_f32(hw[2 * q]), h2_hi_to_f32(hw[2 * q]), g4.x, g4.y, y[4 * q], y[4 * q + 1]);
-                mul2(h2_lo_to_f32(hw[2 * q + 1]), h2_hi_to_f32(hw[2 * q + 1]), g4.z, g4.w, y[4 * q + 2], y[4 * q + 3]);
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(y[4 * q]), fabsf(y[4 * q + 1])),
-                                         fmaxf(fabsf(y[4 * q + 2]), fabsf(y[4 * q + 3]))));
-            }
-            e = mx_exponent_448(amax);
-            const float sc = exp2_neg(e);
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) mul2(y[j], y[j + 1], sc, sc, y[j], y[j + 1]);  // exact
+            for (int k = 0; 32 * k < rows_here; ++k) dst[k] = scS[4 * c + k];
         }
-        const int64_t i0 = (b * cols + oc) * rows + orow0;  // output index, multiple of 32
-        rq_emit(y, e, (uint64_t)i0, seed, tag, stochastic, out, out_sc + (b * cols + oc) * (rows / 32) + orow0 / 32);
     }
 }
 
@@ -953,9 +1016,21 @@ extern "C" pmn_status pmn_requant_transpose_sr_mxfp8(const uint8_t *codes, const
     if (batch == 0 || rows == 0 || cols == 0) return PMN_OK;
     if ((cols / 16) % 4 != 0) return PMN_ERR_INVALID_ARG;  // 4-byte scale words per 64 columns
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    dim3 grid((unsigned)((cols + RQ_T - 1) / RQ_T), (unsigned)((rows + RQ_T - 1) / RQ_T), (unsigned)batch);
-    requant_transpose_kernel<<<grid, 256, 0, s>>>(codes, scales, outer, outer_mode == PMN_OUTER_PER_ROW, rows, cols,
-                                                   seed, tag, rounding == PMN_ROUND_SR, out, out_scales);
+    dim3 grid((unsigned)((cols + 127) / 128), (unsigned)((rows + 127) / 128), (unsigned)batch);
+    const bool per_row = outer_mode == PMN_OUTER_PER_ROW;
+    const int sr = rounding == PMN_ROUND_SR;
+#define PMN_RQ_LAUNCH(PR, C)                                                                                  \
+    requant_transpose_kernel<PR, C><<<grid, 128, 0, s>>>(codes, scales, outer, rows, cols, seed, tag, sr, out, \
+                                                         out_scales)
+    // the expert layer's two row lengths (d_model, d_ff) get compile-time strides
+    if (cols == 4096) {
+        if (per_row) PMN_RQ_LAUNCH(true, 4096); else PMN_RQ_LAUNCH(false, 4096);
+    } else if (cols == 1536) {
+        if (per_row) PMN_RQ_LAUNCH(true, 1536); else PMN_RQ_LAUNCH(false, 1536);
+    } else {
+        if (per_row) PMN_RQ_LAUNCH(true, 0); else PMN_RQ_LAUNCH(false, 0);
+    }
+#undef PMN_RQ_LAUNCH
     return launch_status();
 }
 
