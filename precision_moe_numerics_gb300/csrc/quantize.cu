@@ -688,58 +688,23 @@ __device__ __forceinline__ uint4 philox_from_prefix(const PhiloxPrefix &p, uint3
     return c;
 }
 
-// Requantisation of an NVFP4 tensor [batch, rows, cols] to MXFP8 of its
-// transpose [batch, cols, rows].  CTA = 4 warps = a 128-row x 128-column
-// tile.  Thread = 16 input rows x 8 input columns; lanes l and l ^ 16 hold the
-// two halves of a 32-row block, so each input column's values are half of one
-// output 32-block: its amax takes one shuffle, its 16 elements are one Philox
-// counter (16j .. 16j+15) and its bytes one 16-byte chunk.  The chunks are
-// staged in shared memory ([output row][8 chunks], chunk index XOR bits 3..5 of
-// the output row: conflict-free both ways) and written as whole 128-byte lines
-// after one barrier.  COLS > 0 fixes the row length at compile time so the 16
-// row loads use immediate offsets.
-// Register targets (measured): 5 resident CTAs per SM for the per-group form;
-// the per-row form keeps 16 more outer scales and is left uncapped.
-template <bool PER_ROW, int COLS>
-__global__ void __launch_bounds__(128, PER_ROW ? 1 : 5) requant_transpose_kernel(
-    const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, const float *__restrict__ outer,
-    int64_t rows, int64_t cols_rt, uint64_t seed, uint32_t tag, int stochastic,
-    uint8_t *__restrict__ out, uint8_t *__restrict__ out_sc)
+// Requantisation of one thread's 16 input rows (lanes l and l ^ 16 hold the
+// two halves of a 32-row block) x 8 input columns.  word[i] / s2[i]: the code
+// word (columns 2k, 2k + 1 in byte k) and the E4M3 block scale (as f16x2) of
+// row i; g: the group's outer scale, or the 16 rows' (PER_ROW).  j0: the
+// Philox counter of (first column, first row); jstep = rows / 16 steps to the
+// next column.  Output row orow0 + c (c = 0 .. 7) gets its 16-byte chunk at
+// oS[(orow0 + c) * 8 + chunk] and, from the low lane of the pair, its E8M0
+// byte at scS[(orow0 + c) * 4 + rb].
+template <bool PER_ROW>
+__device__ __forceinline__ void rq_block16x8(const uint32_t (&word)[16], const uint32_t (&s2)[16],
+                                             const float (&g)[PER_ROW ? 16 : 1], unsigned act, uint64_t j0,
+                                             uint64_t jstep, uint64_t seed, uint32_t tag, int stochastic,
+                                             bool low, int orow0, int chunk, int rb, uint4 *oS, uint8_t *scS)
 {
-    __shared__ __align__(16) uint4 oS[128 * 8];  // [output row][16-row chunk ^ swizzle]
-    __shared__ __align__(4) uint8_t scS[128 * 4];  // [output row][32-row block]: E8M0 bytes
-    const int64_t cols = COLS > 0 ? (int64_t)COLS : cols_rt;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, q = lane & 15, hf = lane >> 4;
-    const int64_t b = blockIdx.z;
-    const int64_t r0 = (int64_t)blockIdx.y * 128, c0 = (int64_t)blockIdx.x * 128;
-    const int64_t rb0 = r0 + 32 * w;  // the warp's 32-row block
-    const int64_t col0 = c0 + 8 * q;
-    const bool active = rb0 < rows && col0 < cols;  // lanes l, l ^ 16 agree
-    const unsigned act = __ballot_sync(0xFFFFFFFFu, active);
-    if (active) {
-    const int64_t row0 = rb0 + 16 * hf;
-    const int64_t cols2 = cols / 2, cols16 = cols / 16;
-    const uint8_t *cp = codes + (b * rows + row0) * cols2 + col0 / 2;
-    const uint8_t *sp = scales + (b * rows + row0) * cols16 + col0 / 16;
-    uint32_t word[16], s2[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) word[i] = __ldg(reinterpret_cast<const uint32_t *>(cp + i * cols2));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) s2[i] = e4m3_to_h2(__ldg(sp + i * cols16));
-    float g[PER_ROW ? 16 : 1];
-    if (PER_ROW) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) g[i] = __ldg(outer + b * rows + row0 + i);
-    } else {
-        g[0] = __ldg(outer + b);
-    }
-    // Philox counter of (column col0, rows row0 .. row0+15); column col0 + c adds c * rows / 16
-    const uint64_t j0 = (uint64_t)((b * cols + col0) * rows + row0) >> 4;
-    const uint64_t jstep = (uint64_t)rows >> 4;
     const uint32_t jhi0 = (uint32_t)(j0 >> 32);
     const bool one_hi = (uint32_t)((j0 + 7 * jstep) >> 32) == jhi0;
     const PhiloxPrefix pre = philox_prefix(seed, tag, jhi0);
-    const int chunk = (2 * w + hf) ^ (q & 7);  // output rows 8q .. 8q+7 share bits 3..5
     auto emit = [&](int c, const float (&y)[16], int e) {
         const uint64_t j = j0 + (uint64_t)c * jstep;
         uint32_t o[4];
@@ -754,8 +719,8 @@ __global__ void __launch_bounds__(128, PER_ROW ? 1 : 5) requant_transpose_kernel
             for (int k = 0; k < 4; ++k)
                 o[k] = cvt_e4m3x2_rn(y[4 * k], y[4 * k + 1]) | (cvt_e4m3x2_rn(y[4 * k + 2], y[4 * k + 3]) << 16);
         }
-        oS[(8 * q + c) * 8 + chunk] = make_uint4(o[0], o[1], o[2], o[3]);
-        if (hf == 0) scS[(8 * q + c) * 4 + w] = (uint8_t)(e + 127);
+        oS[(orow0 + c) * 8 + chunk] = make_uint4(o[0], o[1], o[2], o[3]);
+        if (low) scS[(orow0 + c) * 4 + rb] = (uint8_t)(e + 127);
     };
     auto column_pair = [&](auto kc) {
         constexpr int K = decltype(kc)::value;
@@ -810,6 +775,58 @@ __global__ void __launch_bounds__(128, PER_ROW ? 1 : 5) requant_transpose_kernel
     column_pair(std::integral_constant<int, 1>());
     column_pair(std::integral_constant<int, 2>());
     column_pair(std::integral_constant<int, 3>());
+}
+
+// Requantisation of an NVFP4 tensor [batch, rows, cols] to MXFP8 of its
+// transpose [batch, cols, rows].  CTA = 4 warps = a 128-row x 128-column
+// tile.  Thread = 16 input rows x 8 input columns; lanes l and l ^ 16 hold the
+// two halves of a 32-row block, so each input column's values are half of one
+// output 32-block: its amax takes one shuffle, its 16 elements are one Philox
+// counter (16j .. 16j+15) and its bytes one 16-byte chunk.  The chunks are
+// staged in shared memory ([output row][8 chunks], chunk index XOR bits 3..5 of
+// the output row: conflict-free both ways) and written as whole 128-byte lines
+// after one barrier.  COLS > 0 fixes the row length at compile time so the 16
+// row loads use immediate offsets.
+// Register targets (measured): 5 resident CTAs per SM for the per-group form;
+// the per-row form keeps 16 more outer scales and is left uncapped.
+template <bool PER_ROW, int COLS>
+__global__ void __launch_bounds__(128, PER_ROW ? 1 : 5) requant_transpose_kernel(
+    const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, const float *__restrict__ outer,
+    int64_t rows, int64_t cols_rt, uint64_t seed, uint32_t tag, int stochastic,
+    uint8_t *__restrict__ out, uint8_t *__restrict__ out_sc)
+{
+    __shared__ __align__(16) uint4 oS[128 * 8];  // [output row][16-row chunk ^ swizzle]
+    __shared__ __align__(4) uint8_t scS[128 * 4];  // [output row][32-row block]: E8M0 bytes
+    const int64_t cols = COLS > 0 ? (int64_t)COLS : cols_rt;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, q = lane & 15, hf = lane >> 4;
+    const int64_t b = blockIdx.z;
+    const int64_t r0 = (int64_t)blockIdx.y * 128, c0 = (int64_t)blockIdx.x * 128;
+    const int64_t rb0 = r0 + 32 * w;  // the warp's 32-row block
+    const int64_t col0 = c0 + 8 * q;
+    const bool active = rb0 < rows && col0 < cols;  // lanes l, l ^ 16 agree
+    const unsigned act = __ballot_sync(0xFFFFFFFFu, active);
+    if (active) {
+    const int64_t row0 = rb0 + 16 * hf;
+    const int64_t cols2 = cols / 2, cols16 = cols / 16;
+    const uint8_t *cp = codes + (b * rows + row0) * cols2 + col0 / 2;
+    const uint8_t *sp = scales + (b * rows + row0) * cols16 + col0 / 16;
+    uint32_t word[16], s2[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) word[i] = __ldg(reinterpret_cast<const uint32_t *>(cp + i * cols2));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s2[i] = e4m3_to_h2(__ldg(sp + i * cols16));
+    float g[PER_ROW ? 16 : 1];
+    if (PER_ROW) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) g[i] = __ldg(outer + b * rows + row0 + i);
+    } else {
+        g[0] = __ldg(outer + b);
+    }
+    // Philox counter of (column col0, rows row0 .. row0+15); column col0 + c adds c * rows / 16
+    const uint64_t j0 = (uint64_t)((b * cols + col0) * rows + row0) >> 4;
+    // output rows 8q .. 8q+7 share bits 3..5, so the chunk index XOR them spreads a quarter-warp
+    rq_block16x8<PER_ROW>(word, s2, g, act, j0, (uint64_t)rows >> 4, seed, tag, stochastic, hf == 0, 8 * q,
+                          (2 * w + hf) ^ (q & 7), w, oS, scS);
     }
     __syncthreads();
     // whole lines: 8 consecutive threads write the 128 bytes of one output row
