@@ -192,6 +192,7 @@ def main():
     ap.add_argument("--experts", type=int, default=None, help="smaller layer for profiling (default 384)")
     ap.add_argument("--tokens", type=int, default=None, help="tokens routed (default 16384)")
     ap.add_argument("--only", default=None, help="time only this call of the step (profiling)")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped forward measurement")
     args = ap.parse_args()
     rank, world, local = dist_env()
 
@@ -275,6 +276,11 @@ def main():
     if not args.no_e2e and not args.only:
         e2e = run_e2e(L, inp, args, dev, flops_step, world)
 
+    # ------------------------------------------------------------ decode shape
+    dec = None
+    if not args.no_decode and not args.only:
+        dec = run_decode(L, args, dev, W, layer, pmn)
+
     pk = peaks()
     comps = {}
     for name, (fl, by) in alg.items():
@@ -321,7 +327,7 @@ def main():
                     "experts": L.shape.experts, "d_model": L.shape.d_model, "d_ff": L.shape.d_ff,
                     "flops_per_step": flops_step, "l2": "inputs larger than L2 (no flush needed)",
                     "parallelism": "replicas" if world > 1 else "single-gpu"},
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "decode": dec,
                 "gpu_launches": (layer.launches_per_step() if not args.only else
                                  sum(layer.LAUNCHES.get(n, 1) for n in args.only.split(","))) * args.steps,
                 "clocks": clocks,
@@ -329,6 +335,44 @@ def main():
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_decode(L, args, dev, W, layer, pmn, reps=20):
+    """The decode-shaped forward: 64 tokens routed top-8 over the layer's
+    experts (segments of a few rows, not padded), quantised and run through
+    both NVFP4 GEMMs (RHT + S2F6 epilogue on w2) against the step's resident
+    NVFP4 weights of every expert.  CUDA events around `reps` forwards on the
+    launching stream; the hit experts' weights (about 3.1 GB) exceed L2, so
+    every forward streams them from HBM."""
+    import numpy as np
+    import torch
+    r = W.decode_routing(args.seed)
+    xb = W.decode_x(r, args.seed, L.shape.d_model)
+    x = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).view(torch.bfloat16).to(dev)
+    offs = torch.from_numpy(r.offsets.astype(np.int32)).to(dev)
+    fwd = layer.DecodeForward(x, L.w1q3(), L.w2q3(), offs, seed=args.seed, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        fwd.forward()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        fwd.forward()
+    b.record(stream)
+    torch.cuda.synchronize()
+    if pmn.get_device_error() != 0:
+        raise RuntimeError("device error in the decode forward")
+    ms = a.elapsed_time(b) / reps
+    fl, by, wb = layer.decode_algorithmic(r.counts, L.shape.d_model, L.shape.d_ff)
+    pk = peaks()
+    gbs = by / (ms * 1e-3) / 1e9
+    return {"workload": "decode forward: %d tokens, top-%d of %d experts (%d rows, %d experts hit, unpadded), "
+                        "NVFP4 weights resident" % (W.DECODE_TOKENS, W.TOP_K, L.shape.experts, r.real_rows,
+                                                    int((r.counts > 0).sum())),
+            "ms": round(ms, 4), "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 2), "weight_bytes": wb,
+            "algorithmic_bytes": by, "GB/s": round(gbs, 1), "hbm_frac": round(gbs / pk["hbm_gbs"], 3),
+            "bound": "hbm", "reps": reps, "gpu_launches": 4 * reps}
 
 
 def run_e2e(L, inp, args, dev, flops_step, world):

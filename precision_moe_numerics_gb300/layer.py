@@ -136,6 +136,57 @@ class ExpertLayerStep:
             f()
 
 
+class DecodeForward:
+    """The forward pass of a decode batch: a few tokens routed top-k over the
+    experts (segments of a few rows, not padded), against NVFP4 weights of
+    every expert already resident in HBM (e.g. an ExpertLayerStep's w1q3() and
+    w2q3()).  Its time is set by streaming the hit experts' weights."""
+
+    def __init__(self, x, w1q3, w2q3, offsets, seed=0, device="cuda"):
+        T, D = x.shape
+        E, F2 = w1q3[0].shape[0], w1q3[0].shape[1]
+        F = F2 // 2
+        self.x, self.w1q3, self.w2q3, self.offsets, self.seed = x, w1q3, w2q3, offsets, seed
+        u8, f32 = torch.uint8, torch.float32
+
+        def e(*shape, dtype=u8):
+            return torch.empty(shape, dtype=dtype, device=device)
+
+        self.xq = (e(T, D // 2), e(T, D // 16), e(T, dtype=f32))
+        self.y = e(T, F2, dtype=torch.bfloat16)
+        self.hq = (e(T, F // 2), e(T, F // 16), e(T, dtype=f32))
+        self.z = (e(T, D, dtype=torch.int8), e(T, D // 32))
+        self.F = F
+
+    def kernel_calls(self):
+        P = pmn
+        return [
+            ("quant_x", lambda: P.nvfp4_quantize(self.x, four_over_six=True, out=self.xq)),
+            ("gemm1_nvfp4", lambda: P.grouped_gemm_nvfp4(self.xq, self.w1q3, self.offsets, out=self.y)),
+            ("swiglu_quant_h", lambda: P.nvfp4_quantize(self.y, cols=self.F, swiglu=True, four_over_six=True,
+                                                        out=self.hq)),
+            ("gemm2_nvfp4_rht_s2f6", lambda: P.w2_gemm_rht_s2f6(self.hq, self.w2q3, self.offsets, self.seed,
+                                                                out=self.z)),
+        ]
+
+    def forward(self):
+        for _, f in self.kernel_calls():
+            f()
+
+
+def decode_algorithmic(counts, d_model, d_ff):
+    """(flops, algorithmic HBM bytes) of DecodeForward: the hit experts'
+    NVFP4 weights (codes, scales, outer scale) dominate the bytes."""
+    nv = 0.5 + 1 / 16
+    R = int(counts.sum())
+    hit = int((counts > 0).sum())
+    F2 = 2 * d_ff
+    wbytes = hit * ((F2 * d_model + d_model * d_ff) * nv + 8)
+    act = R * d_model * (2 + nv) + R * F2 * 2 * 2 + R * d_ff * nv * 2 + R * d_model * (1 + 1 / 32)
+    flops = 2.0 * R * F2 * d_model + 2.0 * R * d_model * d_ff
+    return flops, wbytes + act, wbytes
+
+
 # launches of library kernels per call name (for the launch count); every
 # call of the step launches one kernel (the scratch clear of the per-group
 # weight quantiser is a memset, not a kernel of the library)

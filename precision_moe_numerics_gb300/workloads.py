@@ -117,6 +117,14 @@ def decode_routing(seed=0):
     return route_topk(logits, TOP_K, pad=1)
 
 
+def decode_x(routing, seed=0, d=D_MODEL):
+    """bf16 bits of the decode batch's routed rows [rows, d]: the tokens ~
+    N(0,1) with 0.1 % entries x30, row i a copy of token row_token[i]."""
+    rng = np.random.default_rng(seed + 5)
+    xt = normal_bf16_host(rng, (DECODE_TOKENS, d), 1.0, 0.001, 30.0)
+    return xt[routing.row_token]
+
+
 # ------------------------------------------------------------------ host cases
 def tiny(seed=0, n=256, outlier_rows=4, outlier_mult=50.0):
     rng = np.random.default_rng(seed)

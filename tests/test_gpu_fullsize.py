@@ -219,3 +219,45 @@ def test_fullsize_step_is_deterministic(run):
     after = (L.z[0], L.dw1[:2], L.dx[:512], L.w1t[0][:2])
     for a, b in zip(before, after):
         assert torch.equal(a, b)
+
+
+def test_decode_forward_against_oracle(run):
+    """Decode batch: 64 tokens, top-8 of the 384 experts, segments of 1-5 rows
+    (not padded), against the step's NVFP4 weights of every expert.  The
+    activation codes and scales are bytes; Y rows of the first, the last and
+    the most-used hit expert within the GEMM tolerance; the combine payload of
+    the most-used one by the step's property."""
+    from precision_moe_numerics_gb300 import layer
+    L = run["L"]
+    E, F2, D = L.w1.shape
+    F = F2 // 2
+    r = W.decode_routing(SEED)
+    xb = W.decode_x(r, SEED, D)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    offs = torch.from_numpy(r.offsets.astype(np.int32)).cuda()
+    dec = layer.DecodeForward(x, L.w1q3(), L.w2q3(), offs, seed=SEED)
+    dec.forward()
+    torch.cuda.synchronize()
+    xc, xs, xg = oracle.nvfp4_quantize(xb, oracle.OUTER_PER_ROW, four_over_six=True)
+    same(hu(dec.xq[0]), xc, "decode X codes")
+    same(hu(dec.xq[1]), xs, "decode X scales")
+    same(hu(dec.xq[2]), xg, "decode X outer")
+    hit = [e for e in range(E) if r.counts[e] > 0]
+    top = int(np.argmax(r.counts))
+    for e in sorted({hit[0], hit[-1], top}):
+        lo, hi = seg(r, e)
+        wc, ws, wg = oracle_w(run, "w1", e)
+        ref = oracle.gemm_nvfp4(xc[lo:hi], xs[lo:hi], xg[lo:hi], wc, ws, wg[0])
+        A = np.abs(oracle.nvfp4_dequant_f64(xc[lo:hi], xs[lo:hi])) * np.abs(xg[lo:hi, None].astype(np.float64))
+        B = np.abs(oracle.nvfp4_dequant_f64(wc, ws)) * abs(float(wg[0]))
+        check_bf16(hb(dec.y[lo:hi]), ref, A @ B.T, "decode Y rows of expert %d" % e)
+    lo, hi = seg(r, top)
+    w1c, w1s, w1g = oracle_w(run, "w1", top)
+    y = oracle.bf16_rne_array(oracle.gemm_nvfp4(xc[lo:hi], xs[lo:hi], xg[lo:hi], w1c, w1s, w1g[0]))
+    h = oracle.swiglu_bf16(y, F)
+    hc, hs, hg = oracle.nvfp4_quantize(h, oracle.OUTER_PER_ROW, four_over_six=True)
+    w2c, w2s, w2g = oracle_w(run, "w2", top)
+    z = oracle.gemm_nvfp4(hc, hs, hg, w2c, w2s, w2g[0])
+    zq = oracle.s2f6_dequant_inverse_rht(hu(dec.z[0][lo:hi]), hu(dec.z[1][lo:hi]), SEED)
+    rel = np.linalg.norm(zq - z) / np.linalg.norm(z)
+    assert rel < 0.02, rel
