@@ -668,6 +668,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // row by row with predicated stores.
         const int q = warp & 3;
         uint8_t *stg = staging + q * C::EPI * STAGE_OUT_BYTES;
+        // fp32 outputs (the weight gradients, written once) are stored with an
+        // L2 evict_last policy: measured 1-2 % faster than the default or
+        // evict_first for dW1 / dW2
+        uint64_t st_policy = 0;
+        if (OUT == PMN_OUT_F32) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(st_policy));
         constexpr int CH_PER_STORE = OUT == PMN_OUT_F32 ? 1 : (OUT == PMN_OUT_BF16 ? 2 : 4);
         uint32_t nstore = 0;
         uint32_t abuf = 0, aphase = 0;
@@ -771,7 +776,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         __syncwarp();
                         if (lane == 0) {
                             const int32_t x = (int32_t)(ti.n0 + 32 * (c - part));
-                            tma_store_2d(&tmO, smem_u32(buf), x, (int32_t)(obase + ti.m0 + 32 * q));
+                            const int32_t y = (int32_t)(obase + ti.m0 + 32 * q);
+                            if (OUT == PMN_OUT_F32) tma_store_2d_hint(&tmO, smem_u32(buf), x, y, st_policy);
+                            else tma_store_2d(&tmO, smem_u32(buf), x, y);
                             bulk_commit_group();
                         }
                         ++nstore;

@@ -111,6 +111,17 @@ __device__ __forceinline__ void cluster_sync()
 }
 
 // Shared -> global tile store (bulk-group completion).
+// As tma_store_2d, with an L2 cache policy for the written lines.
+__device__ __forceinline__ void tma_store_2d_hint(const void *tmap, uint32_t src, int32_t x, int32_t y,
+                                                  uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(src), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int32_t x, int32_t y)
 {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
