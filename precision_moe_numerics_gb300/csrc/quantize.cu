@@ -161,8 +161,17 @@ __device__ __forceinline__ float outer_from_amax(float amax, bool four_over_six)
 // One warp per row; lane handles 16-blocks lane, lane+32, ...  NB = blocks per
 // lane (ceil(cols/16/32)).  The whole row stays in registers, so x is read
 // once.  SWIGLU: h = silu(gate) * up in binary32, rounded to bf16 first.
+// Register targets, measured on rows of d_ff (SwiGLU) and d_model: 4 and 5
+// resident CTAs per SM (7 % and 1.5 % faster than uncapped); wider rows keep
+// their registers.
+#ifndef PMN_QR_MIN_BLOCKS
+#define PMN_QR_MIN_BLOCKS 4
+#endif
+#ifndef PMN_QR2_MIN_BLOCKS
+#define PMN_QR2_MIN_BLOCKS 5
+#endif
 template <int NB, bool SWIGLU>
-__global__ void __launch_bounds__(256) nvfp4_quant_rows_kernel(
+__global__ void __launch_bounds__(256, NB <= 4 ? PMN_QR_MIN_BLOCKS : 1) nvfp4_quant_rows_kernel(
     const uint16_t *__restrict__ x, int64_t rows, int cols, int64_t ldx, int four_over_six,
     uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, float *__restrict__ outer,
     uint16_t *__restrict__ h_out)
@@ -299,7 +308,10 @@ __device__ __forceinline__ uint4 ld_l2_policy(const uint4 *ptr, uint64_t policy)
     return v;
 }
 
-__global__ void __launch_bounds__(QG_THREADS, 3) nvfp4_quant_groups_kernel(
+#ifndef PMN_QG_MIN_BLOCKS  // resident CTAs per SM the register allocation aims for (measured: 4 beats 3
+#define PMN_QG_MIN_BLOCKS 4  // by 4-8 %; 5 spills heavily)
+#endif
+__global__ void __launch_bounds__(QG_THREADS, PMN_QG_MIN_BLOCKS) nvfp4_quant_groups_kernel(
     const uint16_t *__restrict__ x, int64_t groups, int64_t blocks_per_group, int64_t nch, int64_t lead,
     int four_over_six, uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, float *__restrict__ outer,
     uint32_t *scratch)
@@ -441,7 +453,7 @@ __global__ void __launch_bounds__(QG_THREADS, 3) nvfp4_quant_groups_kernel(
 // registers -- once for its amax, then block by block for the codes (the
 // second read hits L1/L2) -- so more warps fit per SM to hide the 4/6 scoring.
 template <int NB>
-__global__ void __launch_bounds__(256) nvfp4_quant_rows2_kernel(const uint16_t *__restrict__ x, int64_t rows,
+__global__ void __launch_bounds__(256, NB <= 8 ? PMN_QR2_MIN_BLOCKS : 1) nvfp4_quant_rows2_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                                 int cols, int64_t ldx, int four_over_six,
                                                                 uint8_t *__restrict__ codes,
                                                                 uint8_t *__restrict__ scales, float *__restrict__ outer)
@@ -893,7 +905,10 @@ pmn_status launch_quant_groups(const uint16_t *x, int64_t groups, int64_t blocks
     // one group plus three quarters of an item per CTA: measured best with
     // the L2 priorities above (a longer lead pushes re-reads out of L2, a
     // shorter one makes coding items wait)
-    const int64_t lead = std::min(groups * nch, nch + (int64_t)grid * 3 / 4);
+#ifndef PMN_QG_LEAD_Q  // the lead beyond one group, in quarters of an item per CTA
+#define PMN_QG_LEAD_Q 3
+#endif
+    const int64_t lead = std::min(groups * nch, nch + (int64_t)grid * PMN_QG_LEAD_Q / 4);
     nvfp4_quant_groups_kernel<<<(unsigned)grid, QG_THREADS, 0, s>>>(x, groups, blocks_per_group, nch, lead,
                                                                      four_over_six, codes, scales, outer, scratch);
     return launch_status();
