@@ -259,7 +259,10 @@ __global__ void __launch_bounds__(256, NB <= 4 ? PMN_QR_MIN_BLOCKS : 1) nvfp4_qu
 // B waits (bounded) for its group's A count; no A item ever waits, so the
 // streams progress whatever the number of resident CTAs.
 constexpr int QG_THREADS = 256;
-constexpr int QG_CHUNK = 2048;  // 16-blocks per work item (32 Ki values)
+#ifndef PMN_QG_CHUNK
+#define PMN_QG_CHUNK 2048
+#endif
+constexpr int QG_CHUNK = PMN_QG_CHUNK;  // 16-blocks per work item (32 Ki values)
 constexpr int QG_PAD = 64;      // the ticket sits alone in its 256-byte line
 
 // scratch words: [0] ticket, [QG_PAD + g] done count of A(g, *),
@@ -577,7 +580,10 @@ __device__ __forceinline__ int rq_chunk(int c, int logical)
 // it in registers and stores 16-byte chunks (8 rows of one column) into the
 // swizzled tile.  Phase 2: task (c, rb) forms the 32-block of output row c;
 // four consecutive lanes write one 128-byte line of the output row.
-__global__ void __launch_bounds__(256) mxfp8_quant_transposed_kernel(const uint16_t *__restrict__ x,
+#ifndef PMN_MXT_MIN_BLOCKS  // resident CTAs per SM the register allocation aims for (measured: 5
+#define PMN_MXT_MIN_BLOCKS 5  // is 6 % faster than the uncapped 4; 6 spills)
+#endif
+__global__ void __launch_bounds__(256, PMN_MXT_MIN_BLOCKS) mxfp8_quant_transposed_kernel(const uint16_t *__restrict__ x,
                                                                      int64_t rows, int64_t cols,
                                                                      uint8_t *__restrict__ out,
                                                                      uint8_t *__restrict__ out_sc)
