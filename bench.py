@@ -51,23 +51,32 @@ def dist_env():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms from before the
+    warm-up; summary() keeps the samples taken between mark_start() and
+    mark_end() (host wall clock, the timed region)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *a):
         self.out = ""
@@ -80,20 +89,26 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
 
     def summary(self):
+        import datetime
         rows = []
         for line in (self.out or "").strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
+        if self.t0 is not None and self.t1 is not None:
+            inside = [r for r in rows if self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
+            if inside:
+                rows = inside
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+        reasons = sorted({names[i] for _, _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": max(r[2] for r in rows),
                 "reasons": reasons, "samples": len(rows)}
 
 
@@ -183,7 +198,7 @@ def pick_sample_experts(r, k):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
@@ -235,21 +250,22 @@ def main():
         alg = {n: alg[n] for n in only}
     flops_step = sum(v[0] for v in alg.values())
 
-    for _ in range(args.warmup):
-        for _, f in calls:
-            f()
-    torch.cuda.synchronize()
-    if pmn.get_device_error() != 0:
-        raise RuntimeError("device error during warm-up")
+    with ClockSampler(local) as clk:  # sampling from before the warm-up; the timed region is marked
+        for _ in range(args.warmup):
+            for _, f in calls:
+                f()
+        torch.cuda.synchronize()
+        if pmn.get_device_error() != 0:
+            raise RuntimeError("device error during warm-up")
 
-    stream = torch.cuda.current_stream()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+        stream = torch.cuda.current_stream()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        clk.mark_start()
         t_start.record(stream)
         for s in range(args.steps):
             ev[s][0].record(stream)
@@ -258,6 +274,7 @@ def main():
                 ev[s][i + 1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
     if world > 1:
         dist.barrier()
     ms_total = t_start.elapsed_time(t_end)
