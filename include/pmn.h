@@ -211,6 +211,12 @@ PMN_API pmn_status pmn_grouped_gemm_nvfp4(const uint8_t *a_codes, const uint8_t 
  * sigma in {+-1}^32 is bit j of Philox4x32-10 word 0 at counter (0, 0, 5, 0)
  * with key (seed lo, seed hi), bit set -> -1, the same for every block.
  *  out      int8 [total_rows, n];  out_scales uint8 [total_rows, n/32].
+ *  debug_acc  NULL, or float32 [total_rows, n], 16-byte aligned: receives
+ *           the epilogue's input x (the accumulator times both outer
+ *           scales) for the rows of the expert segments, so that the
+ *           fused epilogue can be checked byte for byte against
+ *           pmn_rht_s2f6_quantize or a reference of it.  The pages have no
+ *           counterpart; it costs one fp32 write of the output when set.
  * Other arguments as pmn_grouped_gemm_nvfp4.
  */
 PMN_API pmn_status pmn_w2_gemm_rht_s2f6(const uint8_t *a_codes, const uint8_t *a_scales,
@@ -218,7 +224,7 @@ PMN_API pmn_status pmn_w2_gemm_rht_s2f6(const uint8_t *a_codes, const uint8_t *a
                                 const uint8_t *b_scales, const float *b_outer,
                                 const int32_t *offsets, int num_experts, int64_t total_rows,
                                 int64_t n, int64_t k, uint64_t seed, int8_t *out,
-                                uint8_t *out_scales, void *stream);
+                                uint8_t *out_scales, float *debug_acc, void *stream);
 
 /*
  * The combine quantisation alone on a float32 tensor [NVLink] (the same

@@ -132,6 +132,7 @@ struct GemmArgs {
     void *out;
     uint8_t *out_sc;
     uint64_t seed;
+    float *debug_acc;        // RHT + S2F6 only, optional: the scaled fp32 accumulator [m, n]
 };
 
 struct Tile {
@@ -743,6 +744,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) o[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                 } else {
+                    if (p.debug_acc != nullptr && valid) {  // the epilogue's input, before the transform
+                        float4 *d4 = reinterpret_cast<float4 *>(p.debug_acc + orow * p.n + ti.n0 + 32 * c);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    }
                     uint32_t qv[8];
                     const uint32_t sb = rht32_s2f6(v, sigma, qv);
                     o[0] = make_uint4(qv[0], qv[1], qv[2], qv[3]);
@@ -1012,9 +1018,11 @@ pmn_status launch_gemm(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs 
 pmn_status nvfp4_common(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_outer,
                         const uint8_t *b_codes, const uint8_t *b_scales, const float *b_outer,
                         const int32_t *offsets, int num_experts, int64_t total_rows, int64_t n, int64_t k,
-                        int out_kind, void *out, uint8_t *out_sc, uint64_t seed, void *stream)
+                        int out_kind, void *out, uint8_t *out_sc, uint64_t seed, void *stream,
+                        float *debug_acc = nullptr)
 {
     if (num_experts <= 0 || num_experts > MAX_GROUPS || total_rows < 0 || n <= 0 || k <= 0) return PMN_ERR_INVALID_ARG;
+    if (debug_acc && (out_kind != PMN_OUT_RHT_S2F6 || !aligned16(debug_acc))) return PMN_ERR_INVALID_ARG;
     if (n % BN_MIN != 0 || k % 256 != 0 || total_rows >= (int64_t(1) << 31)) return PMN_ERR_INVALID_ARG;
     if (!a_codes || !a_scales || !a_outer || !b_codes || !b_scales || !b_outer || !offsets || !out)
         return PMN_ERR_INVALID_ARG;
@@ -1042,6 +1050,7 @@ pmn_status nvfp4_common(const uint8_t *a_codes, const uint8_t *a_scales, const f
     args.out = out;
     args.out_sc = out_sc;
     args.seed = seed;
+    args.debug_acc = debug_acc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (out_kind) {
         case PMN_OUT_BF16: return launch_gemm<KIND_NVFP4, PMN_OUT_BF16>(ms, mo, args, s);
@@ -1105,10 +1114,11 @@ extern "C" pmn_status pmn_grouped_gemm_nvfp4(const uint8_t *a_codes, const uint8
 extern "C" pmn_status pmn_w2_gemm_rht_s2f6(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_outer,
                                            const uint8_t *b_codes, const uint8_t *b_scales, const float *b_outer,
                                            const int32_t *offsets, int num_experts, int64_t total_rows, int64_t n,
-                                           int64_t k, uint64_t seed, int8_t *out, uint8_t *out_scales, void *stream)
+                                           int64_t k, uint64_t seed, int8_t *out, uint8_t *out_scales,
+                                           float *debug_acc, void *stream)
 {
     return nvfp4_common(a_codes, a_scales, a_outer, b_codes, b_scales, b_outer, offsets, num_experts, total_rows, n,
-                        k, PMN_OUT_RHT_S2F6, out, out_scales, seed, stream);
+                        k, PMN_OUT_RHT_S2F6, out, out_scales, seed, stream, debug_acc);
 }
 
 extern "C" pmn_status pmn_gemm_mxfp8(const uint8_t *a, const uint8_t *a_scales, const uint8_t *b,

@@ -38,7 +38,7 @@ SIGNATURES = {
     "pmn_requant_transpose_sr_mxfp8": ([_P, _P, _P, _I, _I64, _I64, _I64, _U64, _U32, _I, _P, _P, _P], _I),
     "pmn_mxfp8_quantize": ([_P, _I64, _I64, _I, _P, _P, _P], _I),
     "pmn_grouped_gemm_nvfp4": ([_P, _P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P], _I),
-    "pmn_w2_gemm_rht_s2f6": ([_P, _P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _U64, _P, _P, _P], _I),
+    "pmn_w2_gemm_rht_s2f6": ([_P, _P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _U64, _P, _P, _P, _P], _I),
     "pmn_rht_s2f6_quantize": ([_P, _I64, _I64, _U64, _P, _P, _P], _I),
     "pmn_gemm_mxfp8": ([_P, _P, _P, _P, _P, _I, _I, _I64, _I64, _I64, _I, _P, _P], _I),
 }
@@ -210,7 +210,9 @@ def grouped_gemm_nvfp4(a, b, offsets, out_dtype=torch.bfloat16, out=None, stream
     return out
 
 
-def w2_gemm_rht_s2f6(a, b, offsets, seed, out=None, stream=None):
+def w2_gemm_rht_s2f6(a, b, offsets, seed, out=None, debug_acc=None, stream=None):
+    """(q int8 [T, N], scales u8 [T, N/32]); debug_acc: optional float32 [T, N] that receives the
+    epilogue's input (the scaled accumulator) on the expert segments' rows."""
     ac, asc, ao = a
     bc, bsc, bo = b
     _dev(offsets, torch.int32)
@@ -222,8 +224,11 @@ def w2_gemm_rht_s2f6(a, b, offsets, seed, out=None, stream=None):
         sc = torch.empty((T, N // 32), dtype=torch.uint8, device=ac.device)
     else:
         q, sc = out
+    if debug_acc is not None:
+        _dev(debug_acc, torch.float32)
     st = lib().pmn_w2_gemm_rht_s2f6(_ptr(ac), _ptr(asc), _ptr(ao), _ptr(bc), _ptr(bsc), _ptr(bo), _ptr(offsets), E,
-                                    T, N, K, seed, _ptr(q), _ptr(sc), _stream(stream))
+                                    T, N, K, seed, _ptr(q), _ptr(sc),
+                                    _ptr(debug_acc) if debug_acc is not None else None, _stream(stream))
     _check(st, "w2_gemm_rht_s2f6")
     return q, sc
 

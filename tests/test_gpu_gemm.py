@@ -4,9 +4,12 @@ Tolerances (stated for the expert-layer path): float32 outputs within
 relative Frobenius error 1e-5 and elementwise |err| <= 1e-3 * (|A| |B|)[m, n]
 (outer scales included); bf16 outputs additionally within one bf16 step
 (2^-8 relative) of the binary64 value.  The fused RHT + S2F6 epilogue is
-checked after decoding: codes within one step of the oracle's combine
-quantisation of the binary64 product, scales equal except where the block
-maximum sits on a power-of-two boundary.
+checked two ways: its input (the scaled fp32 accumulator, read back through
+the optional debug output) within the float32 tolerance of the binary64
+product, and its bytes equal to the oracle's combine quantisation of that
+same input; also after decoding, against the combine quantisation of the
+binary64 product (codes within one step, scales equal except where the block
+maximum sits on a power-of-two boundary).
 """
 import numpy as np
 import pytest
@@ -128,11 +131,18 @@ def test_w2_gemm_rht_s2f6(pmn):
     bc, bsc, bg = w2q[0].reshape(E, d, f // 2), w2q[1].reshape(E, d, f // 16), w2q[2]
     offs = r.offsets.astype(np.int32)
     seed = 42
+    acc = torch.zeros((r.rows, d), dtype=torch.float32, device="cuda")
     q, sc = pmn.w2_gemm_rht_s2f6((dev(hq[0]), dev(hq[1]), dev(hq[2])), (dev(bc), dev(bsc), dev(bg)), dev(offs),
-                                 seed)
+                                 seed, debug_acc=acc)
     z = oracle.grouped_gemm_nvfp4(hq[0], hq[1], hq[2], bc, bsc, bg, r.offsets)
+    q, sc, acc = q.cpu().numpy(), sc.cpu().numpy(), acc.cpu().numpy()
+    # the epilogue's input is the GEMM result within the float32 tolerance ...
+    check_f32(acc, z, abs_product(hq[0], hq[1], hq[2], bc, bsc, bg, r.offsets), "w2 accumulator")
+    # ... and its bytes are the combine quantisation of exactly that input
+    aq, asc = oracle.rht_s2f6(acc, seed)
+    assert np.array_equal(sc, asc), "fused S2F6 scales differ from the oracle's on the same input"
+    assert np.array_equal(q, aq), "fused S2F6 codes differ from the oracle's on the same input"
     rq, rsc = oracle.rht_s2f6(z.astype(np.float32), seed)
-    q, sc = q.cpu().numpy(), sc.cpu().numpy()
     same_e = sc == rsc
     assert same_e.mean() > 0.99
     dq = np.abs(q.astype(np.int32) - rq.astype(np.int32)).reshape(q.shape[0], -1, 32)
