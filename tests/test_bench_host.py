@@ -1,0 +1,74 @@
+"""Host-side logic of bench.py (no GPU): the clock sampler keeps only the
+samples taken inside the timed region and reports throttle reasons; the DRAM
+traffic table counts an entry only while the kernel source is unchanged; the
+decode forward's algorithmic bytes are the hit experts' weights plus the
+activations."""
+import datetime
+import importlib.util
+import os
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def load_bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def smi_line(t, mhz, power_cap="Not Active", thermal="Not Active"):
+    ts = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    return "%s, 0, %d, 2070, 450.00, 0x0, Not Active, Not Active, %s, %s" % (ts, mhz, thermal, power_cap)
+
+
+def test_clock_sampler_keeps_the_timed_region():
+    b = load_bench()
+    c = b.ClockSampler(0)
+    now = time.time()
+    c.out = "\n".join([smi_line(now - 2.0, 900, thermal="Active"),   # warm-up, before the region
+                       smi_line(now + 0.10, 2070),
+                       smi_line(now + 0.15, 2040, power_cap="Active"),
+                       smi_line(now + 0.20, 2070),
+                       smi_line(now + 3.00, 600)])                       # after the region
+    c.t0, c.t1 = now, now + 0.25
+    s = c.summary()
+    assert s["samples"] == 3
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_without_samples():
+    b = load_bench()
+    c = b.ClockSampler(0)
+    c.out = ""
+    assert c.summary()["reasons"] == ["unsampled"]
+
+
+def test_traffic_table_parses_and_hashes_sources():
+    b = load_bench()
+    table = b.traffic_table()
+    assert "gemm_dw1_mxfp8" in table
+    nbytes, sha = table["gemm_dw1_mxfp8"]
+    assert nbytes > 1e10 and len(sha) == 12
+    # the hash covers the kernel's sources: GEMM and quantiser calls hash different files
+    assert b.source_sha("gemm_dw1_mxfp8") != b.source_sha("quant_w1")
+    assert b.source_sha("gemm_dw1_mxfp8") == b.source_sha("gemm1_nvfp4")
+
+
+def test_decode_accounting():
+    from precision_moe_numerics_gb300 import layer
+    from precision_moe_numerics_gb300 import workloads as W
+    r = W.decode_routing(0)
+    assert r.real_rows == W.DECODE_TOKENS * W.TOP_K and r.rows == r.real_rows  # segments not padded
+    hit = int((r.counts > 0).sum())
+    fl, by, wb = layer.decode_algorithmic(r.counts, W.D_MODEL, W.D_FF)
+    nv = 0.5 + 1 / 16
+    assert wb == hit * ((2 * W.D_FF * W.D_MODEL + W.D_MODEL * W.D_FF) * nv + 8)
+    assert by > wb
+    assert fl == 2.0 * r.real_rows * 2 * W.D_FF * W.D_MODEL + 2.0 * r.real_rows * W.D_MODEL * W.D_FF
+    x = W.decode_x(r, 0)
+    assert x.shape == (r.rows, W.D_MODEL) and x.dtype == np.uint16
