@@ -76,6 +76,7 @@ def lib():
         L.orc_rht32.argtypes = [P, u32, P]
         L.orc_rht_s2f6.argtypes = [P, i64, i64, u64, P, P]
         L.orc_s2f6_dequant_inverse_rht.argtypes = [P, P, i64, i64, u64, P]
+        L.orc_combine_receive.argtypes = [P, P, i64, i64, u64, P, P, i64, i64, P]
         L.orc_bf16_rne_array.argtypes = [P, i64, P]
         _lib = L
     return _lib
@@ -285,6 +286,23 @@ def s2f6_dequant_inverse_rht(q, sc, seed):
     rows, cols = q.shape
     out = np.zeros((rows, cols), np.float64)
     lib().orc_s2f6_dequant_inverse_rht(_p(q), _p(sc), rows, cols, seed, _p(out))
+    return out
+
+
+def combine_receive(q, sc, seed, row_index, gates):
+    """Receive side of the combine [NVLink]: out[t] = sum_i gates[t, i] *
+    (routed row row_index[t, i] decoded and transformed back), binary64
+    [tokens, cols]; a negative index adds nothing."""
+    q = _c(q, np.int8)
+    sc = _c(sc, np.uint8)
+    idx = _c(row_index, np.int64)
+    g = _c(gates, np.float32)
+    rows, cols = q.shape
+    tokens, k = idx.shape
+    assert g.shape == (tokens, k) and cols % 32 == 0 and sc.shape == (rows, cols // 32)
+    assert np.all(idx < rows)
+    out = np.zeros((tokens, cols), np.float64)
+    lib().orc_combine_receive(_p(q), _p(sc), rows, cols, seed, _p(idx), _p(g), tokens, k, _p(out))
     return out
 
 

@@ -30,6 +30,7 @@
  * (worked examples from the pages, closed forms, library codecs, brute force).
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -599,6 +600,36 @@ ORC_API void orc_s2f6_dequant_inverse_rht(const int8_t *q, const uint8_t *sc, in
 }
 
 /* Element-wise orc_bf16_rne over an array (binary64 in, bfloat16 bits out). */
+/* Receive side of the combine, gathered back into token order [NVLink]: each
+ * token t sums, over its k expert choices i = 0 .. k-1 in order,
+ *   gate[t, i] * R(row_index[t, i])
+ * where R(r) is routed row r decoded and transformed back as in
+ * orc_s2f6_dequant_inverse_rht.  Binary64 throughout; out double [tokens, cols].
+ * Reading: the pages send each expert output back to the token's GPU and do
+ * not say how the k results are merged; the plainest reading is the weighted
+ * sum of an MoE combine, with the router's gate weights passed in as inputs.
+ * A negative row index is a dropped choice and adds nothing. */
+ORC_API void orc_combine_receive(const int8_t *q, const uint8_t *sc, int64_t rows, int64_t cols,
+                                 uint64_t seed, const int64_t *row_index, const float *gates,
+                                 int64_t tokens, int64_t k, double *out)
+{
+    (void)rows;
+    #pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < tokens; ++t) {
+        double *y = out + t * cols;
+        double *row = (double *)malloc((size_t)cols * sizeof(double));
+        for (int64_t c = 0; c < cols; ++c) y[c] = 0.0;
+        for (int64_t i = 0; i < k; ++i) {
+            int64_t r = row_index[t * k + i];
+            if (r < 0) continue;
+            orc_s2f6_dequant_inverse_rht(q + r * cols, sc + r * (cols / 32), 1, cols, seed, row);
+            double g = (double)gates[t * k + i];
+            for (int64_t c = 0; c < cols; ++c) y[c] += g * row[c];
+        }
+        free(row);
+    }
+}
+
 ORC_API void orc_bf16_rne_array(const double *v, int64_t n, uint16_t *out)
 {
     #pragma omp parallel for schedule(static)

@@ -74,6 +74,7 @@ class Routing:
     counts: np.ndarray       # int64 [E]
     row_token: np.ndarray    # int64 [rows]
     topk: np.ndarray         # int64 [tokens, k]
+    gates: np.ndarray = None  # float32 [tokens, k]: softmax over the k chosen logits
 
     @property
     def rows(self):
@@ -82,6 +83,18 @@ class Routing:
     @property
     def real_rows(self):
         return int(self.counts.sum())
+
+    def token_rows(self):
+        """int32 [tokens, k]: the routed row that holds token t's i-th choice
+        (the inverse of row_token, in the order of topk)."""
+        tokens, k = self.topk.shape
+        r = np.nonzero(self.row_token >= 0)[0]
+        t = self.row_token[r]
+        e = np.searchsorted(self.offsets, r, side="right") - 1
+        slot = (self.topk[t] == e[:, None]).argmax(axis=1)
+        out = np.full((tokens, k), -1, np.int64)
+        out[t, slot] = r
+        return out.astype(np.int32)
 
 
 def route_topk(logits, k=TOP_K, pad=PAD):
@@ -102,7 +115,10 @@ def route_topk(logits, k=TOP_K, pad=PAD):
     for e, t in zip(flat_e[srt], flat_t[srt]):
         row_token[fill[e]] = t
         fill[e] += 1
-    return Routing(offsets, counts, row_token, order.astype(np.int64))
+    sel = np.take_along_axis(logits, order, axis=1).astype(np.float64)
+    ex = np.exp(sel - sel[:, :1])
+    gates = (ex / ex.sum(axis=1, keepdims=True)).astype(np.float32)
+    return Routing(offsets, counts, row_token, order.astype(np.int64), gates)
 
 
 def moe_routing(seed=0, tokens=MOE_TOKENS, experts=N_EXPERTS, k=TOP_K, pad=PAD):

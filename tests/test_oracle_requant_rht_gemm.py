@@ -174,6 +174,85 @@ def test_s2f6_scale_rule_and_round_trip():
     assert np.all(q[3, :32] == 0) and sc[3, 0] == 0
 
 
+def _receive_by_matrices(q, sc, seed, row_index, gates):
+    """The receive side restated with explicit matrices: decoded block z =
+    k / 64 * 2^(b - 127); back-transformed block = D_sigma (H / sqrt(32)) z
+    with H the explicit Sylvester matrix; token rows = sum of gate * row."""
+    rows, cols = q.shape
+    sigma = oracle.rht_sign_word(seed)
+    D = np.diag([-1.0 if (sigma >> j) & 1 else 1.0 for j in range(32)])
+    M = D @ _sylvester(32).astype(np.float64) / np.sqrt(32.0)
+    z = q.astype(np.float64).reshape(rows, cols // 32, 32) / 64.0 * np.exp2(sc.astype(np.float64) - 127.0)[:, :, None]
+    back = np.einsum("ij,rbj->rbi", M, z).reshape(rows, cols)
+    out = np.zeros((row_index.shape[0], cols))
+    for t in range(row_index.shape[0]):
+        for i in range(row_index.shape[1]):
+            if row_index[t, i] >= 0:
+                out[t] += float(gates[t, i]) * back[row_index[t, i]]
+    return out
+
+
+def test_combine_receive_vs_explicit_matrices():
+    rng = np.random.default_rng(11)
+    rows, cols, tokens, k = 12, 96, 7, 3
+    q = rng.integers(-128, 128, (rows, cols)).astype(np.int8)
+    q[0, :32] = -128
+    q[1, 32:64] = 127
+    sc = rng.integers(110, 141, (rows, cols // 32)).astype(np.uint8)
+    idx = rng.integers(0, rows, (tokens, k))
+    idx[2, 1] = -1          # a dropped choice
+    idx[4, :] = -1          # a token with no choice left
+    gates = rng.uniform(0.0, 1.0, (tokens, k)).astype(np.float32)
+    for seed in (0, 7):
+        got = oracle.combine_receive(q, sc, seed, idx, gates)
+        want = _receive_by_matrices(q, sc, seed, idx, gates)
+        scale = np.abs(want).max()
+        assert np.abs(got - want).max() <= 1e-13 * scale
+        assert np.all(got[4] == 0.0)
+    # the sign word matters: another seed's signs give another result
+    assert not np.allclose(oracle.combine_receive(q, sc, 0, idx, gates), oracle.combine_receive(q, sc, 7, idx, gates))
+    # no token: empty result
+    assert oracle.combine_receive(q, sc, 0, np.zeros((0, k), np.int64), np.zeros((0, k), np.float32)).shape == (0, cols)
+
+
+def test_combine_receive_inverts_the_combine_quantisation():
+    """Routed copies of each token row go through the forward combine
+    quantisation and come back: with gates summing to 1 the token row is
+    recovered to within the S2F6 rounding, half a step 2^(e-6) per
+    transformed coordinate, i.e. sqrt(32) * 2^(e-7) in 2-norm per block
+    (the transform is orthogonal), weighted by the gates."""
+    rng = np.random.default_rng(12)
+    tokens, experts, k, cols, seed = 40, 6, 3, 128, 5
+    routing = W.route_topk(rng.standard_normal((tokens, experts)).astype(np.float32), k, pad=32)
+    x = (rng.standard_normal((tokens, cols)) * 10.0 ** rng.uniform(-2, 2, (tokens, 1))).astype(np.float32)
+    xr = np.zeros((routing.rows, cols), np.float32)
+    real = routing.row_token >= 0
+    xr[real] = x[routing.row_token[real]]
+    q, sc = oracle.rht_s2f6(xr, seed)
+    idx = routing.token_rows()
+    np.testing.assert_allclose(routing.gates.sum(axis=1), 1.0, rtol=1e-6)
+    got = oracle.combine_receive(q, sc, seed, idx, routing.gates)
+    for t in range(tokens):
+        for b in range(cols // 32):
+            sl = slice(32 * b, 32 * b + 32)
+            e = sc[idx[t], b].astype(np.float64) - 127.0
+            bound = float(np.sum(routing.gates[t] * np.sqrt(32.0) * np.exp2(e - 7.0))) * 1.001
+            bound += 1e-6 * np.linalg.norm(x[t, sl])   # binary32 butterflies of the forward side
+            assert np.linalg.norm(got[t, sl] - x[t, sl] * routing.gates[t].astype(np.float64).sum()) <= bound
+
+
+def test_routing_token_rows_inverts_row_token():
+    r = W.route_topk(np.random.default_rng(13).standard_normal((50, 9)).astype(np.float32), 3, pad=32)
+    idx = r.token_rows()
+    assert idx.dtype == np.int32 and idx.shape == (50, 3)
+    for t in range(50):
+        for i in range(3):
+            row = idx[t, i]
+            assert r.row_token[row] == t
+            assert r.offsets[r.topk[t, i]] <= row < r.offsets[r.topk[t, i] + 1]
+    assert np.all(np.diff(r.gates, axis=1) <= 0) and np.all(r.gates > 0)
+
+
 # ------------------------------------------------------------------ GEMMs
 def _exact_nvfp4_matrix(codes, scales):
     rows, cols = codes.shape[0], codes.shape[1] * 2
