@@ -207,7 +207,9 @@ def main():
     ap.add_argument("--experts", type=int, default=None, help="smaller layer for profiling (default 384)")
     ap.add_argument("--tokens", type=int, default=None, help="tokens routed (default 16384)")
     ap.add_argument("--only", default=None, help="time only this call of the step (profiling)")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped forward measurement")
+    ap.add_argument("--combine-only", action="store_true",
+                    help="profiling: time only the combine receive, on a seeded payload (--steps calls)")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped forward and combine-receive measurements")
     args = ap.parse_args()
     rank, world, local = dist_env()
 
@@ -227,6 +229,16 @@ def main():
     from precision_moe_numerics_gb300 import build, layer, pmn
     from precision_moe_numerics_gb300 import workloads as W
     build.build()
+
+    if args.combine_only:  # profiling: the combine receive alone on a seeded payload (< 1 GB on the device)
+        r = W.moe_routing(args.seed)
+        rows = ((r.rows + 511) // 512) * 512
+        q, sc = W.combine_payload(rows, W.D_MODEL, args.seed)
+        z = (torch.from_numpy(q).to(dev), torch.from_numpy(sc).to(dev))
+        res = run_combine(z, r, args, dev, pmn, reps=args.steps)
+        if rank == 0:
+            print(json.dumps({"combine_receive": res}))
+        return
 
     kw = {}
     if args.experts:
@@ -298,6 +310,10 @@ def main():
     if not args.no_decode and not args.only:
         dec = run_decode(L, args, dev, W, layer, pmn)
 
+    comb = None
+    if not args.no_decode and not args.only:
+        comb = run_combine(L.z, r, args, dev, pmn)
+
     pk = peaks()
     comps = {}
     for name, (fl, by) in alg.items():
@@ -344,7 +360,7 @@ def main():
                     "experts": L.shape.experts, "d_model": L.shape.d_model, "d_ff": L.shape.d_ff,
                     "flops_per_step": flops_step, "l2": "inputs larger than L2 (no flush needed)",
                     "parallelism": "replicas" if world > 1 else "single-gpu"},
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "decode": dec,
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "decode": dec, "combine_receive": comb,
                 "gpu_launches": (layer.launches_per_step() if not args.only else
                                  sum(layer.LAUNCHES.get(n, 1) for n in args.only.split(","))) * args.steps,
                 "clocks": clocks,
@@ -390,6 +406,46 @@ def run_decode(L, args, dev, W, layer, pmn, reps=20):
             "ms": round(ms, 4), "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 2), "weight_bytes": wb,
             "algorithmic_bytes": by, "GB/s": round(gbs, 1), "hbm_frac": round(gbs / pk["hbm_gbs"], 3),
             "bound": "hbm", "reps": reps, "gpu_launches": 4 * reps}
+
+
+def run_combine(payload, r, args, dev, pmn, reps=20):
+    """The combine's receive side at the step's size: the layer's S2F6
+    payload (all routed rows) decoded, transformed back and summed with the
+    gates into 16384 bf16 token rows.  CUDA events around `reps` calls on the
+    launching stream; the payload (~0.6 GB) exceeds L2."""
+    import numpy as np
+    import torch
+    idx = torch.from_numpy(r.token_rows()).to(dev)
+    gates = torch.from_numpy(r.gates).to(dev)
+    tokens, k = idx.shape
+    d = payload[0].shape[1]
+    out = torch.empty((tokens, d), dtype=torch.bfloat16, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        pmn.combine_receive_s2f6(payload, args.seed, idx, gates, out=out)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        pmn.combine_receive_s2f6(payload, args.seed, idx, gates, out=out)
+    b.record(stream)
+    torch.cuda.synchronize()
+    if pmn.get_device_error() != 0:
+        raise RuntimeError("device error in the combine receive")
+    ms = a.elapsed_time(b) / reps
+    by = combine_algorithmic(tokens, k, d)
+    gbs = by / (ms * 1e-3) / 1e9
+    return {"workload": "combine receive: %d tokens x top-%d S2F6 rows of %d (+ E8M0 per 32) -> bf16 token rows"
+                        % (tokens, k, d),
+            "ms": round(ms, 4), "algorithmic_bytes": by, "GB/s": round(gbs, 1),
+            "hbm_frac": round(gbs / peaks()["hbm_gbs"], 3), "bound": "hbm", "reps": reps, "gpu_launches": reps}
+
+
+def combine_algorithmic(tokens, k, d):
+    """Bytes the combine receive must move: each routed row's S2F6 bytes and
+    scales read once, the index and gate of every choice, the bf16 token rows
+    written."""
+    return tokens * k * (d + d // 32 + 8) + tokens * d * 2
 
 
 def run_e2e(L, inp, args, dev, flops_step, world):

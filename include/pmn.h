@@ -236,6 +236,35 @@ PMN_API pmn_status pmn_rht_s2f6_quantize(const float *x, int64_t rows, int64_t c
                                  int8_t *out, uint8_t *out_scales, void *stream);
 
 /*
+ * Receive side of the combine, back in token order [NVLink]: the pages call
+ * the combine transform orthogonal and exactly invertible; each token sums
+ * its k expert results, weighted by the router's gates:
+ *   out[t, :] = sum_i gates[t, i] * R(row_index[t, i])
+ *   R(r), per 32-block: sigma . H (k / 64 * 2^(b - 127)) / sqrt(32)
+ * with (k, b) the S2F6 bytes and E8M0 scale of routed row r, H the 32-point
+ * Sylvester Hadamard matrix and sigma the sign word of pmn_w2_gemm_rht_s2f6
+ * for the same seed.  Computed in float32: the choices are summed before
+ * the transform (u = sum_i (gate_i 2^(e_i - 6)) k_i by fma, in order i = 0 ..
+ * k-1), then one FWHT32, RN(1/sqrt(32)), the signs.  How the k results are
+ * merged is not on the pages; the weighted sum of an MoE combine is taken.
+ *  q        int8 [rows, cols], scales uint8 [rows, cols/32]: the combine
+ *           payload (rows in the routed, expert-sorted order), cols % 32 == 0.
+ *  row_index  DEVICE int32 [tokens, k] (4-byte aligned): the routed row of
+ *           token t's i-th choice; negative = a dropped choice (adds
+ *           nothing); an index >= rows adds nothing and latches
+ *           PMN_DEVERR_BAD_OFFSETS.
+ *  gates    DEVICE float32 [tokens, k] (4-byte aligned).
+ *  k        1 .. 64.
+ *  out_kind PMN_OUT_BF16 (round to nearest even from float32) or
+ *           PMN_OUT_F32;  out [tokens, cols].
+ * tokens == 0 or cols == 0 returns PMN_OK before the pointers are checked.
+ */
+PMN_API pmn_status pmn_combine_receive_s2f6(const int8_t *q, const uint8_t *scales, int64_t rows,
+                                    int64_t cols, uint64_t seed, const int32_t *row_index,
+                                    const float *gates, int64_t tokens, int k, int out_kind,
+                                    void *out, void *stream);
+
+/*
  * Grouped MXFP8 GEMM for the backward pass [SR] (E4M3 operands with E8M0
  * scales per 32 along the contraction, float32 accumulation):
  *   C[m, n] = sum_k A[m, k] * B[n, k]

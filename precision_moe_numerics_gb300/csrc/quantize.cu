@@ -3,6 +3,7 @@
 //   pmn_mxfp8_quantize              bf16 -> MXFP8 (RN), both orientations
 //   pmn_requant_transpose_sr_mxfp8  dequant -> transpose -> SR MXFP8  [SR]
 //   pmn_rht_s2f6_quantize           RHT-32 + S2F6 combine quantisation [NVLink]
+//   pmn_combine_receive_s2f6        S2F6 decode + inverse RHT-32 + top-k sum [NVLink]
 // Sections cited are those of the page "Thinking Machines ... Inkling 2
 // Small ... native 4-bit forward" (arex-research.com).
 #include <cuda_bf16.h>
@@ -892,6 +893,172 @@ __global__ void __launch_bounds__(256) rht_s2f6_kernel(const float *__restrict__
     out_sc[t] = (uint8_t)sb;
 }
 
+// ------------------------------------------------------------------ combine receive
+// Receive side of the combine [NVLink], back in token order.  The back
+// transform is linear, so the k choices are summed first and transformed once:
+//   u = sum_i (gate_i * 2^(e_i - 6)) * k_i     (float32 fma, choices in order)
+//   y = sigma . (FWHT32(u) * RN(1/sqrt(32)))
+// which equals sum_i gate_i * sigma . H (k_i 2^(e_i - 6)) / sqrt(32) up to
+// float32 rounding.  An S2F6 byte enters as float32 exactly: the byte plus 128
+// becomes the low mantissa byte of 2^23, and 2^23 + 128 is subtracted.
+// Thread = half of one 32-value block (values 16 h .. 16 h + 15, h = lane & 1):
+// the butterfly stages of stride 1 .. 8 run in registers, the stride-16 stage
+// pairs lanes l and l ^ 1 through one shuffle per value.  Packed float32x2
+// arithmetic for the conversion, the sum and the in-lane butterflies.
+__device__ __forceinline__ void add2(float a0, float a1, float b0, float b1, float &c0, float &c1)
+{
+    asm("{\n\t.reg .b64 a, b, c;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 c, a, b;\n\tmov.b64 {%0, %1}, c;\n\t}"
+        : "=f"(c0), "=f"(c1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void sub2(float a0, float a1, float b0, float b1, float &c0, float &c1)
+{
+    asm("{\n\t.reg .b64 a, b, c;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "sub.rn.f32x2 c, a, b;\n\tmov.b64 {%0, %1}, c;\n\t}"
+        : "=f"(c0), "=f"(c1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void fma2(float a0, float a1, float b0, float b1, float &c0, float &c1)
+{
+    asm("{\n\t.reg .b64 a, b, c;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%0, %1};\n\t"
+        "fma.rn.f32x2 c, a, b, c;\n\tmov.b64 {%0, %1}, c;\n\t}"
+        : "+f"(c0), "+f"(c1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// u[0..3] += s * (4 S2F6 bytes of w)
+__device__ __forceinline__ void s2f6_word_fma(uint32_t w, float s, float *u)
+{
+    const uint32_t x = w ^ 0x80808080u;  // k + 128 per byte
+    const float c = 8388736.0f;          // 2^23 + 128
+    float f[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) f[j] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540u + j));
+    sub2(f[0], f[1], c, c, f[0], f[1]);
+    sub2(f[2], f[3], c, c, f[2], f[3]);
+    fma2(f[0], f[1], s, s, u[0], u[1]);
+    fma2(f[2], f[3], s, s, u[2], u[3]);
+}
+
+__device__ __forceinline__ void s2f6_half_fma(const uint4 &w, float s, float (&u)[16])
+{
+    s2f6_word_fma(w.x, s, u);
+    s2f6_word_fma(w.y, s, u + 4);
+    s2f6_word_fma(w.z, s, u + 8);
+    s2f6_word_fma(w.w, s, u + 12);
+}
+
+// KF > 0: the number of choices at compile time (all loads issued before the
+// arithmetic); KF == 0: k_rt choices, one at a time.  A negative row index is
+// a dropped choice; an index >= rows latches PMN_DEVERR_BAD_OFFSETS and is
+// dropped too.
+template <int KF, bool BF16>
+__global__ void __launch_bounds__(256, 3) combine_receive_kernel(
+    const int8_t *__restrict__ q, const uint8_t *__restrict__ sc, int64_t rows, int64_t nb, uint64_t seed,
+    const int32_t *__restrict__ row_index, const float *__restrict__ gates, int64_t tokens, int k_rt,
+    void *__restrict__ out)
+{
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // every lane stays for the stride-16 shuffle; lanes past the end load and store nothing
+    const bool active = gid < tokens * nb * 2;
+    const int hf = threadIdx.x & 1;
+    const int64_t tb = active ? gid >> 1 : 0, t = tb / nb, b = tb - t * nb;
+    const int64_t cols = nb * 32;
+    const int k = KF > 0 ? KF : k_rt;
+    const int32_t *ri = row_index + t * k;
+    const float *gi = gates + t * k;
+    float u[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) u[j] = 0.0f;
+    auto row_ok = [&](int32_t r) {
+        if (r >= rows) atomicOr(&g_pmn_quant_error, PMN_DEVERR_BAD_OFFSETS);
+        return r >= 0 && r < rows;
+    };
+    // gate * 2^(e - 6) with e = byte - 127: exact unless it falls below the normal range
+    auto row_scale = [&](float g, uint32_t e8) { return ldexpf(g, (int)e8 - 133); };
+    const int64_t off = 32 * b + 16 * hf;
+    if (active) {
+        if (KF > 0) {
+            constexpr int N = KF > 0 ? KF : 1;
+            int32_t r[N];
+            float g[N];
+            uint4 w[N];
+            uint32_t e8[N];
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                r[i] = __ldg(ri + i);
+                g[i] = __ldg(gi + i);
+            }
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                w[i] = make_uint4(0u, 0u, 0u, 0u);  // S2F6 zeros
+                e8[i] = 0u;
+                if (row_ok(r[i])) {
+                    w[i] = __ldg(reinterpret_cast<const uint4 *>(q + (int64_t)r[i] * cols + off));
+                    e8[i] = __ldg(sc + (int64_t)r[i] * nb + b);
+                } else {
+                    g[i] = 0.0f;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < N; ++i) s2f6_half_fma(w[i], row_scale(g[i], e8[i]), u);
+        } else {
+            for (int i = 0; i < k; ++i) {
+                const int32_t r = __ldg(ri + i);
+                if (!row_ok(r)) continue;
+                const uint4 w = __ldg(reinterpret_cast<const uint4 *>(q + (int64_t)r * cols + off));
+                s2f6_half_fma(w, row_scale(__ldg(gi + i), __ldg(sc + (int64_t)r * nb + b)), u);
+            }
+        }
+    }
+    // strides 1, 2, 4, 8 in registers
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {  // stride 1: (u[i], u[i+1])
+        const float a = u[i], c = u[i + 1];
+        u[i] = __fadd_rn(a, c);
+        u[i + 1] = __fsub_rn(a, c);
+    }
+#pragma unroll
+    for (int h = 2; h < 16; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            if ((i & h) == 0) {
+                float s0, s1, d0, d1;
+                add2(u[i], u[i + 1], u[i + h], u[i + h + 1], s0, s1);
+                sub2(u[i], u[i + 1], u[i + h], u[i + h + 1], d0, d1);
+                u[i] = s0;
+                u[i + 1] = s1;
+                u[i + h] = d0;
+                u[i + h + 1] = d1;
+            }
+        }
+    }
+    // stride 16 across the lane pair: low half a + b, high half a - b (one rounding each)
+    const float sgn = hf ? -1.0f : 1.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) u[j] = __fmaf_rn(sgn, u[j], __shfl_xor_sync(0xFFFFFFFFu, u[j], 1));
+    const uint32_t sg = rht_sigma(seed) >> (16 * hf);
+    const float rs = __uint_as_float(0x3E3504F3u);  // RN(1/sqrt(32))
+#pragma unroll
+    for (int j = 0; j < 16; ++j) u[j] = __uint_as_float(__float_as_uint(__fmul_rn(u[j], rs)) ^ (((sg >> j) & 1u) << 31));
+    if (!active) return;
+    if (BF16) {
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(u[2 * j], u[2 * j + 1]);
+            o[j] = *reinterpret_cast<const uint32_t *>(&h2);
+        }
+        uint4 *po = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + t * cols + off);
+        po[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        po[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    } else {
+        float4 *po = reinterpret_cast<float4 *>(static_cast<float *>(out) + t * cols + off);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) po[v] = make_float4(u[4 * v], u[4 * v + 1], u[4 * v + 2], u[4 * v + 3]);
+    }
+}
+
 // Clears the scratch, then runs the per-group kernel on as many CTAs as fit.
 pmn_status launch_quant_groups(const uint16_t *x, int64_t groups, int64_t blocks_per_group, int four_over_six,
                                uint8_t *codes, uint8_t *scales, float *outer, uint32_t *scratch, cudaStream_t s)
@@ -1083,5 +1250,31 @@ extern "C" pmn_status pmn_rht_s2f6_quantize(const float *x, int64_t rows, int64_
     if (nblocks == 0) return PMN_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     rht_s2f6_kernel<<<(unsigned)((nblocks + 255) / 256), 256, 0, s>>>(x, nblocks, seed, out, out_scales);
+    return launch_status();
+}
+
+extern "C" pmn_status pmn_combine_receive_s2f6(const int8_t *q, const uint8_t *scales, int64_t rows, int64_t cols,
+                                               uint64_t seed, const int32_t *row_index, const float *gates,
+                                               int64_t tokens, int k, int out_kind, void *out, void *stream)
+{
+    if (rows < 0 || cols < 0 || tokens < 0 || cols % 32 != 0 || k < 1 || k > 64) return PMN_ERR_INVALID_ARG;
+    if (out_kind != PMN_OUT_BF16 && out_kind != PMN_OUT_F32) return PMN_ERR_INVALID_ARG;
+    if (tokens == 0 || cols == 0) return PMN_OK;  // nothing to read or write (empty buffers may be NULL)
+    if (!q || !scales || !row_index || !gates || !out) return PMN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || ((uintptr_t)row_index & 3u) || ((uintptr_t)gates & 3u))
+        return PMN_ERR_INVALID_ARG;
+    const int64_t nb = cols / 32, nthreads = tokens * nb * 2, grid = (nthreads + 255) / 256;
+    if (grid > 0x7FFFFFFF) return PMN_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+#define PMN_CR_LAUNCH(KF, BF)                                                                           \
+    combine_receive_kernel<KF, BF><<<(unsigned)grid, 256, 0, s>>>(q, scales, rows, nb, seed, row_index, gates, \
+                                                                  tokens, k, out)
+    const bool bf = out_kind == PMN_OUT_BF16;
+    if (k == 8) {  // the layer's top-8
+        if (bf) PMN_CR_LAUNCH(8, true); else PMN_CR_LAUNCH(8, false);
+    } else {
+        if (bf) PMN_CR_LAUNCH(0, true); else PMN_CR_LAUNCH(0, false);
+    }
+#undef PMN_CR_LAUNCH
     return launch_status();
 }

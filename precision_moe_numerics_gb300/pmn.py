@@ -40,6 +40,7 @@ SIGNATURES = {
     "pmn_grouped_gemm_nvfp4": ([_P, _P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P], _I),
     "pmn_w2_gemm_rht_s2f6": ([_P, _P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _U64, _P, _P, _P, _P], _I),
     "pmn_rht_s2f6_quantize": ([_P, _I64, _I64, _U64, _P, _P, _P], _I),
+    "pmn_combine_receive_s2f6": ([_P, _P, _I64, _I64, _U64, _P, _P, _I64, _I, _I, _P, _P], _I),
     "pmn_gemm_mxfp8": ([_P, _P, _P, _P, _P, _I, _I, _I64, _I64, _I64, _I, _P, _P], _I),
 }
 
@@ -189,6 +190,28 @@ def rht_s2f6_quantize(x, seed, out=None, stream=None):
     _check(lib().pmn_rht_s2f6_quantize(_ptr(x), rows, cols, seed, _ptr(q), _ptr(sc), _stream(stream)),
            "rht_s2f6_quantize")
     return q, sc
+
+
+def combine_receive_s2f6(payload, seed, row_index, gates, out_dtype=torch.bfloat16, out=None, stream=None):
+    """payload = (int8 [rows, cols], E8M0 uint8 [rows, cols/32]) in routed
+    order; row_index int32 [tokens, k], gates float32 [tokens, k] -> the
+    token rows [tokens, cols] (bf16 or float32)."""
+    q, sc = payload
+    _dev(q, torch.int8)
+    _dev(sc, torch.uint8)
+    _dev(row_index, torch.int32)
+    _dev(gates, torch.float32)
+    rows, cols = q.shape
+    tokens, k = row_index.shape
+    if tuple(gates.shape) != (tokens, k) or tuple(sc.shape) != (rows, cols // 32):
+        raise PmnError("combine_receive_s2f6: shape mismatch")
+    kind = {torch.bfloat16: OUT_BF16, torch.float32: OUT_F32}[out_dtype]
+    if out is None:
+        out = torch.empty((tokens, cols), dtype=out_dtype, device=q.device)
+    _check(lib().pmn_combine_receive_s2f6(_ptr(q), _ptr(sc), rows, cols, seed, _ptr(row_index), _ptr(gates),
+                                          tokens, k, kind, _ptr(out), _stream(stream)),
+           "combine_receive_s2f6")
+    return out
 
 
 # ------------------------------------------------------------------ GEMMs

@@ -141,6 +141,17 @@ def decode_x(routing, seed=0, d=D_MODEL):
     return xt[routing.row_token]
 
 
+def combine_payload(rows, d=D_MODEL, seed=0):
+    """A seeded combine payload in the shape the w2 epilogue emits: int8
+    S2F6 bytes [rows, d] (k ~ round(N(0, 42^2)) clipped to +-127, so a block's
+    largest |k| is near the top of the range, as the epilogue's scale rule
+    makes it) and E8M0 bytes [rows, d/32] between 2^-9 and 2^2."""
+    rng = np.random.default_rng(seed + 6)
+    q = np.clip(np.rint(rng.standard_normal((rows, d), dtype=np.float32) * 42.0), -127, 127).astype(np.int8)
+    sc = rng.integers(118, 130, (rows, d // 32)).astype(np.uint8)
+    return q, sc
+
+
 # ------------------------------------------------------------------ host cases
 def tiny(seed=0, n=256, outlier_rows=4, outlier_mult=50.0):
     rng = np.random.default_rng(seed)

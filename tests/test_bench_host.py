@@ -72,3 +72,13 @@ def test_decode_accounting():
     assert fl == 2.0 * r.real_rows * 2 * W.D_FF * W.D_MODEL + 2.0 * r.real_rows * W.D_MODEL * W.D_FF
     x = W.decode_x(r, 0)
     assert x.shape == (r.rows, W.D_MODEL) and x.dtype == np.uint16
+
+
+def test_combine_accounting():
+    b = load_bench()
+    # 16384 tokens x top-8 rows of 4096 S2F6 bytes + 128 scale bytes, index + gate each, bf16 out
+    assert b.combine_algorithmic(16384, 8, 4096) == 16384 * 8 * (4096 + 128 + 8) + 16384 * 4096 * 2
+    from precision_moe_numerics_gb300 import workloads as W
+    q, sc = W.combine_payload(64, 256, 0)
+    assert q.dtype == np.int8 and q.shape == (64, 256) and np.abs(q.astype(int)).max() <= 127
+    assert sc.dtype == np.uint8 and sc.shape == (64, 8) and 118 <= sc.min() and sc.max() < 130
