@@ -958,11 +958,12 @@ __global__ void __launch_bounds__(256, 3) combine_receive_kernel(
     const int32_t *__restrict__ row_index, const float *__restrict__ gates, int64_t tokens, int k_rt,
     void *__restrict__ out)
 {
-    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    // every lane stays for the stride-16 shuffle; lanes past the end load and store nothing
-    const bool active = gid < tokens * nb * 2;
+    // CTA (t, y): token t, blocks 128 y .. 128 y + 127 of its row
+    const int64_t t = blockIdx.x;
+    const int64_t b = (int64_t)blockIdx.y * (blockDim.x / 2) + (threadIdx.x >> 1);
     const int hf = threadIdx.x & 1;
-    const int64_t tb = active ? gid >> 1 : 0, t = tb / nb, b = tb - t * nb;
+    // every lane stays for the stride-16 shuffle; lanes past the row's end load and store nothing
+    const bool active = b < nb;
     const int64_t cols = nb * 32;
     const int k = KF > 0 ? KF : k_rt;
     const int32_t *ri = row_index + t * k;
@@ -974,8 +975,14 @@ __global__ void __launch_bounds__(256, 3) combine_receive_kernel(
         if (r >= rows) atomicOr(&g_pmn_quant_error, PMN_DEVERR_BAD_OFFSETS);
         return r >= 0 && r < rows;
     };
-    // gate * 2^(e - 6) with e = byte - 127: exact unless it falls below the normal range
-    auto row_scale = [&](float g, uint32_t e8) { return ldexpf(g, (int)e8 - 133); };
+    // gate * 2^(e - 6) with e = byte - 127, as (g * 2^min(byte - 7, 0)) * 2^max(byte - 133, -126):
+    // both factors are normal powers of two, so one rounding at most (below the normal range)
+    auto row_scale = [&](float g, uint32_t e8) {
+        const int e = (int)e8;
+        const float lo = __uint_as_float((uint32_t)(min(e, 7) + 120) << 23);
+        const float hi = __uint_as_float((uint32_t)max(e - 6, 1) << 23);
+        return __fmul_rn(__fmul_rn(g, lo), hi);
+    };
     const int64_t off = 32 * b + 16 * hf;
     if (active) {
         if (KF > 0) {
@@ -1263,11 +1270,12 @@ extern "C" pmn_status pmn_combine_receive_s2f6(const int8_t *q, const uint8_t *s
     if (!q || !scales || !row_index || !gates || !out) return PMN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(out) || ((uintptr_t)row_index & 3u) || ((uintptr_t)gates & 3u))
         return PMN_ERR_INVALID_ARG;
-    const int64_t nb = cols / 32, nthreads = tokens * nb * 2, grid = (nthreads + 255) / 256;
-    if (grid > 0x7FFFFFFF) return PMN_ERR_INVALID_ARG;
+    const int64_t nb = cols / 32, chunks = (2 * nb + 255) / 256;  // 128 blocks per CTA
+    if (tokens > 0x7FFFFFFF || chunks > 65535) return PMN_ERR_INVALID_ARG;
+    const dim3 grid((unsigned)tokens, (unsigned)chunks);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 #define PMN_CR_LAUNCH(KF, BF)                                                                           \
-    combine_receive_kernel<KF, BF><<<(unsigned)grid, 256, 0, s>>>(q, scales, rows, nb, seed, row_index, gates, \
+    combine_receive_kernel<KF, BF><<<grid, 256, 0, s>>>(q, scales, rows, nb, seed, row_index, gates, \
                                                                   tokens, k, out)
     const bool bf = out_kind == PMN_OUT_BF16;
     if (k == 8) {  // the layer's top-8
