@@ -968,6 +968,12 @@ __global__ void __launch_bounds__(256, 3) combine_receive_kernel(
     const int k = KF > 0 ? KF : k_rt;
     const int32_t *ri = row_index + t * k;
     const float *gi = gates + t * k;
+    // the sign-scaled normalisation sigma_j * RN(1/sqrt(32)) of the 32 positions, once per CTA
+    __shared__ __align__(16) float sgn_rs[32];
+    if (threadIdx.x < 32) {
+        const uint32_t sigma = rht_sigma(seed);
+        sgn_rs[threadIdx.x] = __uint_as_float(0x3E3504F3u ^ (((sigma >> threadIdx.x) & 1u) << 31));
+    }
     float u[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) u[j] = 0.0f;
@@ -991,10 +997,20 @@ __global__ void __launch_bounds__(256, 3) combine_receive_kernel(
             float g[N];
             uint4 w[N];
             uint32_t e8[N];
+            if (N % 4 == 0 && ((reinterpret_cast<uintptr_t>(ri) | reinterpret_cast<uintptr_t>(gi)) & 15u) == 0) {
 #pragma unroll
-            for (int i = 0; i < N; ++i) {
-                r[i] = __ldg(ri + i);
-                g[i] = __ldg(gi + i);
+                for (int i = 0; i < N; i += 4) {  // 16-byte loads of the choices' indices and gates
+                    const int4 rv = __ldg(reinterpret_cast<const int4 *>(ri + i));
+                    const float4 gv = __ldg(reinterpret_cast<const float4 *>(gi + i));
+                    r[i] = rv.x, r[i + 1] = rv.y, r[i + 2] = rv.z, r[i + 3] = rv.w;
+                    g[i] = gv.x, g[i + 1] = gv.y, g[i + 2] = gv.z, g[i + 3] = gv.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < N; ++i) {
+                    r[i] = __ldg(ri + i);
+                    g[i] = __ldg(gi + i);
+                }
             }
 #pragma unroll
             for (int i = 0; i < N; ++i) {
@@ -1042,12 +1058,19 @@ __global__ void __launch_bounds__(256, 3) combine_receive_kernel(
     }
     // stride 16 across the lane pair: low half a + b, high half a - b (one rounding each)
     const float sgn = hf ? -1.0f : 1.0f;
+    float p[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) u[j] = __fmaf_rn(sgn, u[j], __shfl_xor_sync(0xFFFFFFFFu, u[j], 1));
-    const uint32_t sg = rht_sigma(seed) >> (16 * hf);
-    const float rs = __uint_as_float(0x3E3504F3u);  // RN(1/sqrt(32))
+    for (int j = 0; j < 16; ++j) p[j] = __shfl_xor_sync(0xFFFFFFFFu, u[j], 1);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) u[j] = __uint_as_float(__float_as_uint(__fmul_rn(u[j], rs)) ^ (((sg >> j) & 1u) << 31));
+    for (int j = 0; j < 16; j += 2) fma2(sgn, sgn, u[j], u[j + 1], p[j], p[j + 1]);
+    __syncthreads();  // sgn_rs written
+    const float4 *cr = reinterpret_cast<const float4 *>(sgn_rs + 16 * hf);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {  // times sigma_j RN(1/sqrt(32)): the sign is exact
+        const float4 c = cr[v];
+        mul2(p[4 * v], p[4 * v + 1], c.x, c.y, u[4 * v], u[4 * v + 1]);
+        mul2(p[4 * v + 2], p[4 * v + 3], c.z, c.w, u[4 * v + 2], u[4 * v + 3]);
+    }
     if (!active) return;
     if (BF16) {
         uint32_t o[8];
