@@ -209,7 +209,7 @@ def main():
     ap.add_argument("--only", default=None, help="time only this call of the step (profiling)")
     ap.add_argument("--combine-only", action="store_true",
                     help="profiling: time only the combine receive, on a seeded payload (--steps calls)")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped forward and combine-receive measurements")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped forward, combine-receive and MXFP8-forward measurements")
     args = ap.parse_args()
     rank, world, local = dist_env()
 
@@ -310,9 +310,10 @@ def main():
     if not args.no_decode and not args.only:
         dec = run_decode(L, args, dev, W, layer, pmn)
 
-    comb = None
+    comb = mxf = None
     if not args.no_decode and not args.only:
         comb = run_combine(L.z, r, args, dev, pmn)
+        mxf = run_mxfp8_forward(inp, r, offsets, args, layer, pmn)
 
     pk = peaks()
     comps = {}
@@ -360,7 +361,7 @@ def main():
                     "experts": L.shape.experts, "d_model": L.shape.d_model, "d_ff": L.shape.d_ff,
                     "flops_per_step": flops_step, "l2": "inputs larger than L2 (no flush needed)",
                     "parallelism": "replicas" if world > 1 else "single-gpu"},
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "decode": dec, "combine_receive": comb,
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "decode": dec, "combine_receive": comb, "mxfp8_forward": mxf,
                 "gpu_launches": (layer.launches_per_step() if not args.only else
                                  sum(layer.LAUNCHES.get(n, 1) for n in args.only.split(","))) * args.steps,
                 "clocks": clocks,
@@ -439,6 +440,46 @@ def run_combine(payload, r, args, dev, pmn, reps=20):
                         % (tokens, k, d),
             "ms": round(ms, 4), "algorithmic_bytes": by, "GB/s": round(gbs, 1),
             "hbm_frac": round(gbs / peaks()["hbm_gbs"], 3), "bound": "hbm", "reps": reps, "gpu_launches": reps}
+
+
+def run_mxfp8_forward(inp, r, offsets, args, layer, pmn, reps=10):
+    """The layer's forward in MXFP8 (the precision of the last 16.6 % of
+    layers): MXFP8 quantisation of W1, W2 (every call, as in a training step)
+    and X, the grouped FP8 GEMMs, SwiGLU + MXFP8 of h.  CUDA events around
+    `reps` forwards on the launching stream; weights (14.5 GB bf16) and
+    activations exceed L2."""
+    import torch
+    fw = layer.MXFP8Forward(inp["x"], inp["w1"], inp["w2"], offsets, device=inp["x"].device)
+    calls = fw.kernel_calls()
+    for _ in range(max(args.warmup, 3)):
+        fw.forward()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(reps)]
+    for i in range(reps):
+        for j, (_, f) in enumerate(calls):
+            ev[i][j].record(stream)
+            f()
+        ev[i][-1].record(stream)
+    torch.cuda.synchronize()
+    if pmn.get_device_error() != 0:
+        raise RuntimeError("device error in the MXFP8 forward")
+    ms = sum(ev[i][0].elapsed_time(ev[i][-1]) for i in range(reps)) / reps
+    per = {name: round(sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(reps)) / reps, 4)
+           for j, (name, _) in enumerate(calls)}
+    E, F2, D = inp["w1"].shape
+    fl, by = layer.mxfp8_forward_algorithmic(r.real_rows, E, D, F2 // 2)
+    pk = peaks()
+    fp8_peak = pk["bf16_tflops_sustained"] * NOMINAL_TC_RATIO["fp8"]
+    gemm_ms = per["mx_gemm1"] + per["mx_gemm2"]
+    del fw
+    return {"workload": "MXFP8 forward of the layer (last 16.6 %% of layers): %d experts, %d routed rows, "
+                        "d_model %d, d_ff %d; weights quantised every call" % (E, r.real_rows, D, F2 // 2),
+            "ms": round(ms, 4), "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 1), "flops": fl, "algorithmic_bytes": by,
+            "GB/s": round(by / (ms * 1e-3) / 1e9, 1), "hbm_frac": round(by / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3),
+            "gemm_TFLOP/s": round(fl / (gemm_ms * 1e-3) / 1e12, 1),
+            "gemm_tc_frac": round(fl / (gemm_ms * 1e-3) / 1e12 / fp8_peak, 3),
+            "calls_ms": per, "reps": reps, "gpu_launches": len(calls) * reps}
 
 
 def combine_algorithmic(tokens, k, d):

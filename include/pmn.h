@@ -181,6 +181,20 @@ PMN_API pmn_status pmn_mxfp8_quantize(const void *x, int64_t rows, int64_t cols,
                               uint8_t *out, uint8_t *out_scales, void *stream);
 
 /*
+ * SwiGLU followed by MXFP8 quantisation (round to nearest even, E8M0 per 32
+ * along the row) of h, for the forward of the last 16.6 % of layers, which
+ * the pages keep in MXFP8 instead of NVFP4 [Cost]:
+ *   h = bf16(silu(gate) * up), formed in float32 as in PMN_IN_BF16_SWIGLU;
+ *   out = MXFP8(h) as pmn_mxfp8_quantize (transpose 0).
+ *  y        bf16 [rows, 2 f]: gate = columns [0, f), up = columns [f, 2 f).
+ *  f        multiple of 32;  rows * f / 32 < 2^32.
+ *  out      uint8 [rows, f] (E4M3);  out_scales uint8 [rows, f / 32].
+ *  h_out    optional bf16 [rows, f]: the h that was quantised (NULL to skip).
+ */
+PMN_API pmn_status pmn_mxfp8_quantize_swiglu(const void *y, int64_t rows, int64_t f, uint8_t *out,
+                                     uint8_t *out_scales, void *h_out, void *stream);
+
+/*
  * Grouped NVFP4 expert GEMM for the forward pass [Layers], [Cost]:
  *   Z[m, n] = (sum_k A[m, k] * B_e[n, k]) * a_outer[m] * b_outer[e]
  * for the rows m of expert e, offsets[e] <= m < offsets[e+1].  A and B are

@@ -1,6 +1,7 @@
 // quantize.cu -- HBM-bound quantisation kernels of the MoE expert-layer path:
 //   pmn_nvfp4_quantize              NVFP4 with outer scales and 4/6   [SR], [Cost]
 //   pmn_mxfp8_quantize              bf16 -> MXFP8 (RN), both orientations
+//   pmn_mxfp8_quantize_swiglu       SwiGLU -> MXFP8 (RN) of h, the MXFP8 forward [Cost]
 //   pmn_requant_transpose_sr_mxfp8  dequant -> transpose -> SR MXFP8  [SR]
 //   pmn_rht_s2f6_quantize           RHT-32 + S2F6 combine quantisation [NVLink]
 //   pmn_combine_receive_s2f6        S2F6 decode + inverse RHT-32 + top-k sum [NVLink]
@@ -547,6 +548,62 @@ __global__ void __launch_bounds__(256) mxfp8_quant_rowwise_kernel(const uint16_t
     (void)bpr;
 }
 
+// SwiGLU, then MXFP8 (round to nearest) of h, for the MXFP8 forward of the
+// last layers [Cost]: y bf16 [rows, 2 f] holds gate | up; thread = one
+// 32-block of h.  h = silu(gate) * up in binary32 (the same operations as the
+// NVFP4 SwiGLU path), rounded to bf16, then quantised as the rowwise kernel
+// above.  rows * f / 32 < 2^32 (checked by the caller).
+__global__ void __launch_bounds__(256) mxfp8_swiglu_rowwise_kernel(const uint16_t *__restrict__ y, uint32_t nblocks,
+                                                                   uint32_t bpr, uint8_t *__restrict__ out,
+                                                                   uint8_t *__restrict__ out_sc,
+                                                                   uint16_t *__restrict__ h_out)
+{
+    const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= nblocks) return;
+    const uint32_t row = t / bpr, b = t - row * bpr;
+    const int64_t f = (int64_t)bpr * 32;
+    const uint4 *pg = reinterpret_cast<const uint4 *>(y + (int64_t)row * 2 * f + 32 * (int64_t)b);
+    const uint4 *pu = reinterpret_cast<const uint4 *>(y + (int64_t)row * 2 * f + f + 32 * (int64_t)b);
+    uint4 gv[4], uv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        gv[i] = __ldg(pg + i);
+        uv[i] = __ldg(pu + i);
+    }
+    const uint32_t *gw = reinterpret_cast<const uint32_t *>(gv);
+    const uint32_t *uw = reinterpret_cast<const uint32_t *>(uv);
+    uint32_t hw[16];
+    uint32_t m = 0u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float a0 = bf16_lo(gw[i]), a1 = bf16_hi(gw[i]);
+        const float h0 = __fmul_rn(__fdiv_rn(a0, __fadd_rn(1.0f, expf(-a0))), bf16_lo(uw[i]));
+        const float h1 = __fmul_rn(__fdiv_rn(a1, __fadd_rn(1.0f, expf(-a1))), bf16_hi(uw[i]));
+        hw[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(h0)) |
+                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(h1)) << 16);
+        m = __vmaxu2(m, hw[i] & 0x7FFF7FFFu);  // |bf16| orders as integers
+    }
+    const float amax = __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
+    const int e = mx_exponent_448(amax);
+    const float sc = exp2_neg(e);  // y * 2^-e is exact
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t lo = cvt_e4m3x2_rn(__fmul_rn(bf16_lo(hw[2 * i]), sc), __fmul_rn(bf16_hi(hw[2 * i]), sc));
+        const uint32_t hi =
+            cvt_e4m3x2_rn(__fmul_rn(bf16_lo(hw[2 * i + 1]), sc), __fmul_rn(bf16_hi(hw[2 * i + 1]), sc));
+        o[i] = lo | (hi << 16);
+    }
+    uint4 *po = reinterpret_cast<uint4 *>(out + (int64_t)t * 32);
+    po[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    po[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    out_sc[t] = (uint8_t)(e + 127);
+    if (h_out) {
+        uint4 *ph = reinterpret_cast<uint4 *>(h_out + (int64_t)t * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ph[i] = make_uint4(hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]);
+    }
+}
 
 // ------------------------------------------------------------------ requant [SR]
 // One CTA per tile of 128 input rows x 128 input cols.
@@ -1236,6 +1293,22 @@ extern "C" pmn_status pmn_mxfp8_quantize(const void *x, int64_t rows, int64_t co
         dim3 grid((unsigned)((cols + RQ_T - 1) / RQ_T), (unsigned)((rows + RQ_T - 1) / RQ_T));
         mxfp8_quant_transposed_kernel<<<grid, 256, 0, s>>>(xb, rows, cols, out, out_scales);
     }
+    return launch_status();
+}
+
+extern "C" pmn_status pmn_mxfp8_quantize_swiglu(const void *y, int64_t rows, int64_t f, uint8_t *out,
+                                                uint8_t *out_scales, void *h_out, void *stream)
+{
+    if (rows < 0 || f < 0 || f % 32 != 0) return PMN_ERR_INVALID_ARG;
+    if (rows == 0 || f == 0) return PMN_OK;
+    if (!y || !out || !out_scales || !aligned16(y) || !aligned16(out)) return PMN_ERR_INVALID_ARG;
+    if (h_out && !aligned16(h_out)) return PMN_ERR_INVALID_ARG;
+    const int64_t nblocks = rows * (f / 32);
+    if (nblocks > 0xFFFFFF00LL) return PMN_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    mxfp8_swiglu_rowwise_kernel<<<(unsigned)((nblocks + 255) / 256), 256, 0, s>>>(
+        reinterpret_cast<const uint16_t *>(y), (uint32_t)nblocks, (uint32_t)(f / 32), out, out_scales,
+        reinterpret_cast<uint16_t *>(h_out));
     return launch_status();
 }
 

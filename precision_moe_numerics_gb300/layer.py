@@ -174,6 +174,66 @@ class DecodeForward:
             f()
 
 
+class MXFP8Forward:
+    """The expert layer's forward in MXFP8, the precision the pages keep for
+    the last 16.6 % of layers [Cost]: X, W1 and W2 quantised to MXFP8 with
+    round to nearest (E8M0 per 32 along the contraction), both grouped GEMMs
+    on the block-scaled FP8 tensor cores with bf16 outputs, and SwiGLU +
+    MXFP8 of h between them.  The weights are quantised on every call, as in
+    a training step.  x: bf16 [rows, D] routed rows; w1 bf16 [E, 2F, D];
+    w2 bf16 [E, D, F]; offsets: device int32 [E+1]."""
+
+    def __init__(self, x, w1, w2, offsets, device="cuda"):
+        T, D = x.shape
+        E, F2, _ = w1.shape
+        F = F2 // 2
+        self.x, self.w1, self.w2, self.offsets = x, w1, w2, offsets
+        self.E, self.D, self.F = E, D, F
+        u8, bf16 = torch.uint8, torch.bfloat16
+
+        def e(*shape, dtype=u8):
+            return torch.empty(shape, dtype=dtype, device=device)
+
+        self.w1q = (e(E * F2, D), e(E * F2, D // 32))
+        self.w2q = (e(E * D, F), e(E * D, F // 32))
+        self.xq = (e(T, D), e(T, D // 32))
+        self.y = e(T, F2, dtype=bf16)
+        self.hq = (e(T, F), e(T, F // 32))
+        self.z = e(T, D, dtype=bf16)
+
+    def kernel_calls(self):
+        P = pmn
+        E, D, F = self.E, self.D, self.F
+        return [
+            ("mx_quant_w1", lambda: P.mxfp8_quantize(self.w1.view(E * 2 * F, D), out=self.w1q)),
+            ("mx_quant_w2", lambda: P.mxfp8_quantize(self.w2.view(E * D, F), out=self.w2q)),
+            ("mx_quant_x", lambda: P.mxfp8_quantize(self.x, out=self.xq)),
+            ("mx_gemm1", lambda: P.gemm_mxfp8(self.xq[0], self.xq[1], self.w1q[0].view(E, 2 * F, D),
+                                              self.w1q[1].view(E, 2 * F, D // 32), self.offsets, P.GROUP_M,
+                                              torch.bfloat16, out=self.y)),
+            ("mx_swiglu_quant_h", lambda: P.mxfp8_quantize_swiglu(self.y, out=self.hq)),
+            ("mx_gemm2", lambda: P.gemm_mxfp8(self.hq[0], self.hq[1], self.w2q[0].view(E, D, F),
+                                              self.w2q[1].view(E, D, F // 32), self.offsets, P.GROUP_M,
+                                              torch.bfloat16, out=self.z)),
+        ]
+
+    def forward(self):
+        for _, f in self.kernel_calls():
+            f()
+
+
+def mxfp8_forward_algorithmic(real_rows, experts, d_model, d_ff):
+    """(flops, algorithmic HBM bytes) of MXFP8Forward on the real routed rows:
+    bf16 weights and X read once, their MXFP8 copies written and read once,
+    Y and h round trips, the bf16 output written."""
+    mx = 1 + 1 / 32
+    R, E, D, F2 = real_rows, experts, d_model, 2 * d_ff
+    w = E * (F2 * D + D * d_ff)
+    by = w * (2 + 2 * mx) + R * D * (2 + 2 * mx) + R * F2 * 2 * 2 + R * d_ff * 2 * mx + R * D * 2
+    flops = 2.0 * R * F2 * D + 2.0 * R * D * d_ff
+    return flops, by
+
+
 def decode_algorithmic(counts, d_model, d_ff):
     """(flops, algorithmic HBM bytes) of DecodeForward: the hit experts'
     NVFP4 weights (codes, scales, outer scale) dominate the bytes."""

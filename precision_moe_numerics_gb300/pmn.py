@@ -37,6 +37,7 @@ SIGNATURES = {
     "pmn_nvfp4_quantize_per_group_noalloc": ([_P, _I64, _I64, _I64, _I, _P, _P, _P, _P], _I),
     "pmn_requant_transpose_sr_mxfp8": ([_P, _P, _P, _I, _I64, _I64, _I64, _U64, _U32, _I, _P, _P, _P], _I),
     "pmn_mxfp8_quantize": ([_P, _I64, _I64, _I, _P, _P, _P], _I),
+    "pmn_mxfp8_quantize_swiglu": ([_P, _I64, _I64, _P, _P, _P, _P], _I),
     "pmn_grouped_gemm_nvfp4": ([_P, _P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P], _I),
     "pmn_w2_gemm_rht_s2f6": ([_P, _P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _U64, _P, _P, _P, _P], _I),
     "pmn_rht_s2f6_quantize": ([_P, _I64, _I64, _U64, _P, _P, _P], _I),
@@ -177,6 +178,23 @@ def mxfp8_quantize(x, transpose=False, out=None, stream=None):
     _check(lib().pmn_mxfp8_quantize(_ptr(x), rows, cols, int(transpose), _ptr(q), _ptr(sc), _stream(stream)),
            "mxfp8_quantize")
     return q, sc
+
+
+def mxfp8_quantize_swiglu(y, want_h=False, out=None, stream=None):
+    """bf16 y [rows, 2f] (gate | up) -> MXFP8 (RN) of h = silu(gate) * up
+    (u8 values [rows, f], u8 E8M0 scales [rows, f/32][, bf16 h])."""
+    _dev(y, torch.bfloat16)
+    rows, f2 = y.shape
+    f = f2 // 2
+    if out is None:
+        q = torch.empty((rows, f), dtype=torch.uint8, device=y.device)
+        sc = torch.empty((rows, f // 32), dtype=torch.uint8, device=y.device)
+    else:
+        q, sc = out
+    h = torch.empty((rows, f), dtype=torch.bfloat16, device=y.device) if want_h else None
+    _check(lib().pmn_mxfp8_quantize_swiglu(_ptr(y), rows, f, _ptr(q), _ptr(sc), _ptr(h), _stream(stream)),
+           "mxfp8_quantize_swiglu")
+    return (q, sc, h) if want_h else (q, sc)
 
 
 def rht_s2f6_quantize(x, seed, out=None, stream=None):

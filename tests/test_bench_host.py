@@ -82,3 +82,11 @@ def test_combine_accounting():
     q, sc = W.combine_payload(64, 256, 0)
     assert q.dtype == np.int8 and q.shape == (64, 256) and np.abs(q.astype(int)).max() <= 127
     assert sc.dtype == np.uint8 and sc.shape == (64, 8) and 118 <= sc.min() and sc.max() < 130
+
+
+def test_mxfp8_forward_accounting():
+    from precision_moe_numerics_gb300 import layer
+    fl, by = layer.mxfp8_forward_algorithmic(131072, 384, 4096, 1536)
+    assert fl == 2.0 * 131072 * 3072 * 4096 + 2.0 * 131072 * 4096 * 1536
+    w = 384 * (3072 * 4096 + 4096 * 1536)        # weight elements: bf16 read, MXFP8 written and read
+    assert by > w * (2 + 2 * 1.03125) and by < w * (2 + 2 * 1.03125) * 1.25
