@@ -28,7 +28,8 @@ def test_header_declares_the_path():
     syms = declared_symbols()
     for name in ["pmn_nvfp4_quantize", "pmn_requant_transpose_sr_mxfp8", "pmn_grouped_gemm_nvfp4",
                  "pmn_gemm_mxfp8", "pmn_w2_gemm_rht_s2f6", "pmn_mxfp8_quantize", "pmn_rht_s2f6_quantize",
-                 "pmn_get_device_error", "pmn_status_string", "pmn_version"]:
+                 "pmn_get_device_error", "pmn_status_string", "pmn_version", "pmn_combine_receive_s2f6",
+                 "pmn_mxfp8_quantize_swiglu"]:
         assert name in syms
 
 
@@ -57,8 +58,26 @@ def test_host_argument_checks_need_no_gpu(libpath):
                                     null) == pmn.ERR_INVALID_ARG
     assert L.pmn_gemm_mxfp8(null, null, null, null, null, 1, 5, 128, 128, 512, 0, null, null) == pmn.ERR_INVALID_ARG
     assert L.pmn_rht_s2f6_quantize(null, 1, 31, 0, null, null, null) == pmn.ERR_INVALID_ARG
-    # more groups than the fixed scratch holds: rejected before any pointer is used
     fake = 1 << 20
+    # combine receive: cols % 32, k out of 1 .. 64, unknown output kind, misaligned output
+    assert L.pmn_combine_receive_s2f6(fake, fake, 64, 48, 0, fake, fake, 4, 8, pmn.OUT_BF16, fake,
+                                      null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_combine_receive_s2f6(fake, fake, 64, 64, 0, fake, fake, 4, 65, pmn.OUT_BF16, fake,
+                                      null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_combine_receive_s2f6(fake, fake, 64, 64, 0, fake, fake, 4, 0, pmn.OUT_BF16, fake,
+                                      null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_combine_receive_s2f6(fake, fake, 64, 64, 0, fake, fake, 4, 8, 7, fake, null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_combine_receive_s2f6(fake, fake, 64, 64, 0, fake, fake, 4, 8, pmn.OUT_F32, fake + 4,
+                                      null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_combine_receive_s2f6(null, null, 64, 64, 0, null, null, 4, 8, pmn.OUT_F32, null,
+                                      null) == pmn.ERR_INVALID_ARG
+    # no token: nothing to do, NULL buffers allowed
+    assert L.pmn_combine_receive_s2f6(null, null, 64, 64, 0, null, null, 0, 8, pmn.OUT_F32, null, null) == pmn.OK
+    # SwiGLU + MXFP8: f % 32, misaligned input
+    assert L.pmn_mxfp8_quantize_swiglu(fake, 4, 48, fake, fake, null, null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_mxfp8_quantize_swiglu(fake + 2, 4, 64, fake, fake, null, null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_mxfp8_quantize_swiglu(null, 0, 64, null, null, null, null) == pmn.OK
+    # more groups than the fixed scratch holds: rejected before any pointer is used
     assert L.pmn_nvfp4_quantize_per_group_noalloc(fake, 1025 * 16, 64, 16, 0, fake, fake, fake,
                                                   null) == pmn.ERR_INVALID_ARG
 
