@@ -69,6 +69,7 @@ def lib():
         L.orc_requant_transpose_mxfp8_window.argtypes = [P, P, P, i32, i64, i64, i64, u64, u32, i32, P, P,
                                                          i64, i64, i64]
         L.orc_mxfp8_quantize.argtypes = [P, i64, i64, i32, P, P]
+        L.orc_requant_transpose_nvfp4.argtypes = [P, P, P, i32, i64, i64, i64, u64, u32, i32, P, P, P, i64]
         L.orc_mxfp8_dequant_f64.argtypes = [P, P, i64, i64, P]
         L.orc_rht_sign_word.argtypes = [u64]
         L.orc_rht_sign_word.restype = u32
@@ -242,6 +243,25 @@ def requant_transpose_mxfp8(codes, scales, outer, outer_per_row, batch, rows, co
                                              _p(out), _p(out_sc), b_begin, rows if rows_total is None else rows_total,
                                              r_begin)
     return out, out_sc
+
+
+def requant_transpose_nvfp4(codes, scales, outer, outer_per_row, batch, rows, cols, seed, tag,
+                            stochastic=True, b_begin=0):
+    """NVFP4 [batch, rows, cols] -> dequant -> transpose -> NVFP4 [batch, cols,
+    rows] with stochastic (or nearest) rounding: (codes [batch, cols, rows/2],
+    E4M3 scales [batch, cols, rows/16], outer [batch]).  b_begin: index of
+    the first entry in the full tensor (random bits follow the full index)."""
+    codes = _c(codes, np.uint8).reshape(batch * rows, cols // 2)
+    scales = _c(scales, np.uint8).reshape(batch * rows, cols // 16)
+    outer = _c(outer, np.float32)
+    assert rows % 16 == 0 and cols % 16 == 0
+    out = np.zeros((batch, cols, rows // 2), np.uint8)
+    out_sc = np.zeros((batch, cols, rows // 16), np.uint8)
+    out_g = np.zeros(batch, np.float32)
+    lib().orc_requant_transpose_nvfp4(_p(codes), _p(scales), _p(outer), 0 if outer_per_row else 1, batch, rows,
+                                      cols, seed, tag, 0 if stochastic else 1, _p(out), _p(out_sc), _p(out_g),
+                                      b_begin)
+    return out, out_sc, out_g
 
 
 def mxfp8_quantize(x_bf16_bits, transpose=False):

@@ -473,6 +473,91 @@ ORC_API void orc_requant_transpose_mxfp8_window(const uint8_t *codes, const uint
             }
 }
 
+/* Dequantise -> transpose -> requantise to NVFP4 with stochastic rounding:
+ * the FP4 backward the pages name as future work, the same [SR] steps as the
+ * MXFP8 requantisation above with the NVFP4 format of the forward pass.
+ * Input as orc_requant_transpose_mxfp8; d = (code * S) * g in binary32.
+ * Output per batch entry: codes [cols, rows/2] (element 2i in the low
+ * nibble), E4M3 scales [cols, rows/16] (16-blocks along the original rows),
+ * binary32 outer scale out_outer[b].
+ * Reading (outer scale; the pages give none for the transposed tensor): the
+ * entry's largest block scale times its outer scale, sd = dec(S) * g
+ * (binary32), over every input block of the entry, divided by 448:
+ * g' = max sd / 448 (binary32), g' = 1 when every scale is zero.  So every
+ * |d| <= 6 * dec(S) * g fits under 6 * 448 * g', and zero (padding) blocks do
+ * not count.
+ * Reading (block scale; unbiased SR needs values that do not clip, as the
+ * MXFP8 exponent rule): s = amax / RN(6 * g'), S' = the smallest E4M3 value
+ * >= s (saturating at 448); sd' = dec(S') * g'; r = 1 / sd' (0 if sd' = 0);
+ * y = d * r (all binary32); code = SR_E2M1(y) with orc_sr_bits16(seed, tag,
+ * i), i the element's row-major index in the output [batch, cols, rows] of
+ * the full tensor (b_begin shifts the entries), or RNE_E2M1(y) (rounding 1).
+ * The sign is kept, as in the forward codes. */
+static double ru_e4m3(double s)
+{
+    if (s <= 0.0) return 0.0;
+    if (s >= 448.0) return 448.0;
+    int L = ilog2_floor(s);
+    if (L < -6) L = -6;
+    double ulp = ldexp(1.0, L - 3);
+    return ceil(s / ulp) * ulp; /* exact: ulp is a power of two */
+}
+
+ORC_API void orc_requant_transpose_nvfp4(const uint8_t *codes, const uint8_t *scales, const float *outer,
+                                         int outer_mode, int64_t batch, int64_t rows, int64_t cols,
+                                         uint64_t seed, uint32_t tag, int rounding, uint8_t *out_codes,
+                                         uint8_t *out_sc, float *out_outer, int64_t b_begin)
+{
+    for (int64_t b = 0; b < batch; ++b) {
+        float m = 0.0f;
+        for (int64_t r = 0; r < rows; ++r) {
+            int64_t src = b * rows + r;
+            float g = outer_mode == 0 ? outer[src] : outer[b];
+            for (int64_t k = 0; k < cols / 16; ++k) {
+                float sd = (float)orc_e4m3_value(scales[src * (cols / 16) + k]) * g;
+                if (sd > m) m = sd;
+            }
+        }
+        out_outer[b] = m == 0.0f ? 1.0f : m / 448.0f;
+    }
+    #pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t c = 0; c < cols; ++c) {
+            const float gp = out_outer[b];
+            const float six_g = 6.0f * gp;
+            for (int64_t rb = 0; rb < rows / 16; ++rb) {
+                float d[16];
+                float amax = 0.0f;
+                for (int j = 0; j < 16; ++j) {
+                    int64_t src = b * rows + rb * 16 + j;
+                    float g = outer_mode == 0 ? outer[src] : outer[b];
+                    uint32_t byte = codes[src * (cols / 2) + c / 2];
+                    uint32_t code = (c & 1) ? (byte >> 4) : (byte & 15u);
+                    d[j] = deq_nvfp4(code, scales[src * (cols / 16) + c / 16], g);
+                    amax = fmaxf(amax, fabsf(d[j]));
+                }
+                float s = amax / six_g;
+                uint32_t S = e4m3_encode_mag(ru_e4m3((double)s));
+                float sd = (float)orc_e4m3_value(S) * gp;
+                float r = sd == 0.0f ? 0.0f : 1.0f / sd;
+                int64_t orow = (b * cols + c) * rows;
+                int64_t grow = ((b_begin + b) * cols + c) * rows;
+                for (int j = 0; j < 16; j += 2) {
+                    uint32_t q[2];
+                    for (int t = 0; t < 2; ++t) {
+                        float y = d[j + t] * r;
+                        if (rounding == 0)
+                            q[t] = orc_e2m1_sr((double)y, orc_sr_bits16(seed, tag, (uint64_t)(grow + rb * 16 + j + t)));
+                        else
+                            q[t] = orc_e2m1_rne(y);
+                    }
+                    out_codes[(orow + rb * 16 + j) / 2] = (uint8_t)(q[0] | (q[1] << 4));
+                }
+                out_sc[(b * cols + c) * (rows / 16) + rb] = (uint8_t)S;
+            }
+        }
+}
+
 /* bf16 -> MXFP8 with round to nearest even (used for dY).  Reading: the pages
  * ask for SR on the saved forward tensors only; gradients take RN.
  * transpose 0: out [rows, cols], scales [rows, cols/32] (blocks along cols).
