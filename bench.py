@@ -209,7 +209,7 @@ def main():
     ap.add_argument("--only", default=None, help="time only this call of the step (profiling)")
     ap.add_argument("--combine-only", action="store_true",
                     help="profiling: time only the combine receive, on a seeded payload (--steps calls)")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode-shaped forward, combine-receive and MXFP8-forward measurements")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode, combine-receive, MXFP8-forward and FP4-requant measurements")
     args = ap.parse_args()
     rank, world, local = dist_env()
 
@@ -310,10 +310,11 @@ def main():
     if not args.no_decode and not args.only:
         dec = run_decode(L, args, dev, W, layer, pmn)
 
-    comb = mxf = None
+    comb = mxf = fp4b = None
     if not args.no_decode and not args.only:
         comb = run_combine(L.z, r, args, dev, pmn)
         mxf = run_mxfp8_forward(inp, r, offsets, args, layer, pmn)
+        fp4b = run_fp4_requant(L, args, pmn)
 
     pk = peaks()
     comps = {}
@@ -361,7 +362,7 @@ def main():
                     "experts": L.shape.experts, "d_model": L.shape.d_model, "d_ff": L.shape.d_ff,
                     "flops_per_step": flops_step, "l2": "inputs larger than L2 (no flush needed)",
                     "parallelism": "replicas" if world > 1 else "single-gpu"},
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "decode": dec, "combine_receive": comb, "mxfp8_forward": mxf,
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "decode": dec, "combine_receive": comb, "mxfp8_forward": mxf, "fp4_backward_requant": fp4b,
                 "gpu_launches": (layer.launches_per_step() if not args.only else
                                  sum(layer.LAUNCHES.get(n, 1) for n in args.only.split(","))) * args.steps,
                 "clocks": clocks,
@@ -480,6 +481,62 @@ def run_mxfp8_forward(inp, r, offsets, args, layer, pmn, reps=10):
             "gemm_TFLOP/s": round(fl / (gemm_ms * 1e-3) / 1e12, 1),
             "gemm_tc_frac": round(fl / (gemm_ms * 1e-3) / 1e12 / fp8_peak, 3),
             "calls_ms": per, "reps": reps, "gpu_launches": len(calls) * reps}
+
+
+def run_fp4_requant(L, args, pmn, reps=10):
+    """The FP4 backward's requantisations at the step's size: the step's saved
+    NVFP4 X, H (per token) and W1, W2 (per expert) dequantised, transposed and
+    requantised to NVFP4 with stochastic rounding, as the step's MXFP8
+    requantisations do.  CUDA events per call over `reps` passes on the
+    launching stream; every tensor exceeds L2 or streams past it."""
+    import torch
+    E, F2, D = L.w1.shape
+    F, T = F2 // 2, L.shape.rows
+    outs = {}
+
+    def buf(batch, rows, cols):
+        return (torch.empty((batch, cols, rows // 2), dtype=torch.uint8, device=L.x.device),
+                torch.empty((batch, cols, rows // 16), dtype=torch.uint8, device=L.x.device),
+                torch.empty((batch,), dtype=torch.float32, device=L.x.device))
+
+    calls = [("fp4_requant_x", (L.xq, True, 1, T, D, pmn.TAG_X)), ("fp4_requant_h", (L.hq, True, 1, T, F, pmn.TAG_H)),
+             ("fp4_requant_w1", (L.w1q, False, E, F2, D, pmn.TAG_W1)),
+             ("fp4_requant_w2", (L.w2q, False, E, D, F, pmn.TAG_W2))]
+    for name, (src, per_row, batch, rows, cols, tag) in calls:
+        outs[name] = buf(batch, rows, cols)
+
+    def run(name, src, per_row, batch, rows, cols, tag):
+        pmn.requant_transpose_sr_nvfp4(src[0], src[1], src[2], per_row, batch, rows, cols, args.seed, tag,
+                                       out=outs[name])
+
+    for _ in range(max(args.warmup, 3)):
+        for name, a in calls:
+            run(name, *a)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(reps)]
+    for i in range(reps):
+        for j, (name, a) in enumerate(calls):
+            ev[i][j].record(stream)
+            run(name, *a)
+        ev[i][-1].record(stream)
+    torch.cuda.synchronize()
+    if pmn.get_device_error() != 0:
+        raise RuntimeError("device error in the FP4 requantisation")
+    nv = 0.5 + 1 / 16
+    R = L.shape.real_rows
+    elems = {"fp4_requant_x": R * D, "fp4_requant_h": R * F, "fp4_requant_w1": E * F2 * D,
+             "fp4_requant_w2": E * D * F}
+    pk = peaks()
+    res = {}
+    for j, (name, _) in enumerate(calls):
+        ms = sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(reps)) / reps
+        by = elems[name] * 2 * nv
+        res[name] = {"ms": round(ms, 4), "GB/s": round(by / (ms * 1e-3) / 1e9, 1),
+                     "hbm_frac": round(by / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3)}
+    del outs
+    return {"workload": "NVFP4 -> transposed NVFP4 with stochastic rounding (FP4 backward) of the step's "
+                        "saved X, H, W1, W2", "calls": res, "reps": reps, "gpu_launches": 3 * len(calls) * reps}
 
 
 def combine_algorithmic(tokens, k, d):

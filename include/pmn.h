@@ -172,6 +172,33 @@ PMN_API pmn_status pmn_requant_transpose_sr_mxfp8(const uint8_t *codes, const ui
                                           void *stream);
 
 /*
+ * Dequantise -> transpose -> requantise to NVFP4 with stochastic rounding:
+ * the FP4 backward that the pages name as future work, the [SR] steps with
+ * the forward's NVFP4 format.  d = (code * S) * g in float32 as above;
+ * entry b of the output gets one float32 outer scale
+ *   g'_b = (max over the entry's input blocks of dec(S) * g) / 448
+ * (1 if every scale is zero; zero padding blocks do not count), so every
+ * value fits; per 16 values along the ORIGINAL rows the E4M3 scale is the
+ * smallest E4M3 value >= amax / (6 g') (saturating at 448: no value clips,
+ * which keeps stochastic rounding unbiased); y = d * (1 / (dec(S') g'))
+ * (float32), and the E2M1 code is y rounded stochastically with 16 random
+ * bits per element (the rule, counters and bit layout of
+ * pmn_requant_transpose_sr_mxfp8) or to nearest even (PMN_ROUND_RN).
+ *  codes, scales, outer, outer_mode, batch, rows, cols, seed, tag, rounding
+ *           as pmn_requant_transpose_sr_mxfp8 (rows % 32 == 0, cols % 64 == 0).
+ *  out      uint8 [batch, cols, rows/2] (element 2i in the low nibble);
+ *  out_scales uint8 [batch, cols, rows/16] (E4M3);
+ *  out_outer float32 [batch] (4-byte aligned); used as scratch during the call.
+ * Launches a scale reduction, the requantisation and a finalisation (three
+ * kernels and one memset on `stream`).
+ */
+PMN_API pmn_status pmn_requant_transpose_sr_nvfp4(const uint8_t *codes, const uint8_t *scales,
+                                          const float *outer, int outer_mode, int64_t batch,
+                                          int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,
+                                          int rounding, uint8_t *out, uint8_t *out_scales,
+                                          float *out_outer, void *stream);
+
+/*
  * bf16 -> MXFP8 with round-to-nearest-even (the gradient dY; the pages ask
  * for SR on the saved forward tensors only).  Same scale rule as above.
  *  transpose 0: out [rows, cols], out_scales [rows, cols/32] (cols % 32 == 0)

@@ -3,6 +3,7 @@
 //   pmn_mxfp8_quantize              bf16 -> MXFP8 (RN), both orientations
 //   pmn_mxfp8_quantize_swiglu       SwiGLU -> MXFP8 (RN) of h, the MXFP8 forward [Cost]
 //   pmn_requant_transpose_sr_mxfp8  dequant -> transpose -> SR MXFP8  [SR]
+//   pmn_requant_transpose_sr_nvfp4  dequant -> transpose -> SR NVFP4 (FP4 backward) [SR]
 //   pmn_rht_s2f6_quantize           RHT-32 + S2F6 combine quantisation [NVLink]
 //   pmn_combine_receive_s2f6        S2F6 decode + inverse RHT-32 + top-k sum [NVLink]
 // Sections cited are those of the page "Thinking Machines ... Inkling 2
@@ -924,6 +925,147 @@ __global__ void __launch_bounds__(128, PER_ROW ? 1 : 5) requant_transpose_kernel
     }
 }
 
+// ------------------------------------------------------------------ requant to NVFP4 (FP4 backward)
+// The FP4 backward the pages name as future work: the [SR] steps (dequantise,
+// transpose, requantise with stochastic rounding) with the NVFP4 format.
+// Outer scale of the transposed entry b: g' = (max over its input blocks of
+// dec(S) * g) / 448, 1 if every scale is zero.  Block scale: the smallest
+// E4M3 value >= amax / RN(6 g'), so no value clips; codes by stochastic
+// rounding of y = d * RN(1 / RN(dec(S') g')) onto E2M1 with 16 random bits
+// (the rule and bit layout of the MXFP8 requantisation), or nearest even.
+
+// Largest dec(S) * g of each entry, as float bits (non-negative floats order
+// as integers, so atomicMax is order-independent).  Thread = one 4-byte word
+// of scales; grid (ceil(rows * spr / 4 / 256), batch).
+__global__ void __launch_bounds__(256) nvfp4_scale_max_kernel(const uint8_t *__restrict__ scales,
+                                                              const float *__restrict__ outer, int per_row,
+                                                              uint32_t rows, uint32_t wpr,
+                                                              uint32_t *__restrict__ gmax)
+{
+    const int64_t b = blockIdx.y;
+    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    float m = 0.0f;
+    if (i < rows * wpr) {
+        const uint32_t r = i / wpr;
+        const float g = per_row ? __ldg(outer + b * rows + r) : __ldg(outer + b);
+        const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(scales) + (b * rows) * wpr + i);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m = fmaxf(m, __fmul_rn(e4m3_to_f32((w >> (8 * k)) & 0xFFu), g));
+    }
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0 && m > 0.0f) atomicMax(gmax + b, __float_as_uint(m));
+}
+
+__device__ __forceinline__ float nvfp4_outer_from_max(uint32_t bits)
+{
+    return bits == 0u ? 1.0f : __fdiv_rn(__uint_as_float(bits), 448.0f);
+}
+
+__global__ void nvfp4_outer_finalize_kernel(float *out_outer, int64_t batch)
+{
+    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < batch) out_outer[b] = nvfp4_outer_from_max(__float_as_uint(out_outer[b]));
+}
+
+// Stochastic rounding of y onto E2M1 (sign kept): with ulp the grid step at
+// |y| (0.5 below 2, 1 below 4, 2 above), t = |y| / ulp, the 16 leading
+// fraction bits f16 = floor((t - floor t) 2^16) and a carry from rb16 + f16
+// round up; 6 saturates.  Every step is exact in binary32.
+__device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t rb16)
+{
+    const float a = fabsf(y);
+    const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
+    const float t = a * inv;
+    const float fl = floorf(t);
+    const uint32_t f16 = (uint32_t)((t - fl) * 65536.0f);
+    const uint32_t k = (uint32_t)fl + ((rb16 + f16) >> 16);
+    const uint32_t code = a < 2.0f ? k : (a < 4.0f ? k + 2u : min(k + 4u, 7u));
+    return code | (signbit(y) ? 8u : 0u);
+}
+
+// 16 random bits of element e (0..15) of a Philox block: word e / 4; low or
+// high half; odd elements bit-reversed.
+__device__ __forceinline__ uint32_t sr_bits_of(const uint4 &wd, int e)
+{
+    const uint32_t w = (e >> 2) == 0 ? wd.x : (e >> 2) == 1 ? wd.y : (e >> 2) == 2 ? wd.z : wd.w;
+    const uint32_t h = (e & 2) ? (w >> 16) : (w & 0xFFFFu);
+    return (e & 1) ? (__brev(h) >> 16) : h;
+}
+
+// Thread = 16 input rows x 8 input columns, as requant_transpose_kernel: the
+// 16 rows of one column are exactly one output 16-block and one Philox
+// counter.  CTA = 4 warps = 128 rows x 128 columns.
+template <bool PER_ROW>
+__global__ void __launch_bounds__(128) requant_transpose_nvfp4_kernel(
+    const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, const float *__restrict__ outer,
+    int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, int stochastic, const uint32_t *__restrict__ gmax,
+    uint8_t *__restrict__ out, uint8_t *__restrict__ out_sc)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, q = lane & 15, hf = lane >> 4;
+    const int64_t b = blockIdx.z;
+    const int64_t row0 = (int64_t)blockIdx.y * 128 + 32 * w + 16 * hf;
+    const int64_t col0 = (int64_t)blockIdx.x * 128 + 8 * q;
+    if (row0 >= rows || col0 >= cols) return;
+    const int64_t cols2 = cols / 2, cols16 = cols / 16;
+    const uint8_t *cp = codes + (b * rows + row0) * cols2 + col0 / 2;
+    const uint8_t *sp = scales + (b * rows + row0) * cols16 + col0 / 16;
+    uint32_t word[16], s2[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) word[i] = __ldg(reinterpret_cast<const uint32_t *>(cp + i * cols2));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s2[i] = e4m3_to_h2(__ldg(sp + i * cols16));
+    float g[PER_ROW ? 16 : 1];
+    if (PER_ROW) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) g[i] = __ldg(outer + b * rows + row0 + i);
+    } else {
+        g[0] = __ldg(outer + b);
+    }
+    const float gp = nvfp4_outer_from_max(__ldg(gmax + b));
+    const float six_g = __fmul_rn(6.0f, gp);
+    const uint64_t j0 = (uint64_t)((b * cols + col0) * rows + row0) >> 4;
+    const uint64_t jstep = (uint64_t)rows >> 4;
+    auto column_pair = [&](auto kc) {
+        constexpr int K = decltype(kc)::value;
+        uint32_t cs[16];  // exact code * S of columns 2K (low halves) and 2K + 1 (high halves)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) cs[i] = e2m1x2_byte_mul_h2<K>(word[i], s2[i]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = 2 * K + h;
+            float d[16], amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                d[i] = __fmul_rn(h ? h2_hi_to_f32(cs[i]) : h2_lo_to_f32(cs[i]), g[PER_ROW ? i : 0]);
+                amax = fmaxf(amax, fabsf(d[i]));
+            }
+            const float s = __fdiv_rn(amax, six_g);
+            uint32_t S = cvt_e4m3(s);
+            if (e4m3_to_f32(S) < s && S < 0x7Eu) ++S;  // round the scale up: no value clips
+            const float sd = __fmul_rn(e4m3_to_f32(S), gp);
+            const float r = sd == 0.0f ? 0.0f : __frcp_rn(sd);
+            uint32_t packed[2] = {0u, 0u};
+            if (stochastic) {
+                const uint4 wd = sr_words16(seed, tag, j0 + (uint64_t)c * jstep);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    packed[i >> 3] |= e2m1_sr(__fmul_rn(d[i], r), sr_bits_of(wd, i)) << (4 * (i & 7));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; i += 2)
+                    packed[i >> 3] |= cvt_e2m1x2(__fmul_rn(d[i], r), __fmul_rn(d[i + 1], r)) << (4 * (i & 7));
+            }
+            const int64_t oc = b * cols + col0 + c;
+            *reinterpret_cast<uint2 *>(out + oc * (rows / 2) + row0 / 2) = make_uint2(packed[0], packed[1]);
+            out_sc[oc * (rows / 16) + row0 / 16] = (uint8_t)S;
+        }
+    };
+    column_pair(std::integral_constant<int, 0>());
+    column_pair(std::integral_constant<int, 1>());
+    column_pair(std::integral_constant<int, 2>());
+    column_pair(std::integral_constant<int, 3>());
+}
+
 // ------------------------------------------------------------------ RHT + S2F6
 __global__ void __launch_bounds__(256) rht_s2f6_kernel(const float *__restrict__ x, int64_t nblocks,
                                                        uint64_t seed, int8_t *__restrict__ out,
@@ -1341,6 +1483,42 @@ extern "C" pmn_status pmn_requant_transpose_sr_mxfp8(const uint8_t *codes, const
         if (per_row) PMN_RQ_LAUNCH(true, 0); else PMN_RQ_LAUNCH(false, 0);
     }
 #undef PMN_RQ_LAUNCH
+    return launch_status();
+}
+
+extern "C" pmn_status pmn_requant_transpose_sr_nvfp4(const uint8_t *codes, const uint8_t *scales,
+                                                     const float *outer, int outer_mode, int64_t batch,
+                                                     int64_t rows, int64_t cols, uint64_t seed, uint32_t tag,
+                                                     int rounding, uint8_t *out, uint8_t *out_scales,
+                                                     float *out_outer, void *stream)
+{
+    if (batch < 0 || rows < 0 || cols < 0 || rows % 32 != 0 || cols % 64 != 0) return PMN_ERR_INVALID_ARG;
+    if (outer_mode != PMN_OUTER_PER_ROW && outer_mode != PMN_OUTER_PER_GROUP) return PMN_ERR_INVALID_ARG;
+    if (rounding != PMN_ROUND_SR && rounding != PMN_ROUND_RN) return PMN_ERR_INVALID_ARG;
+    if (batch == 0) return PMN_OK;
+    if (!codes || !scales || !outer || !out || !out_scales || !out_outer) return PMN_ERR_INVALID_ARG;
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(out) || ((uintptr_t)outer & 3u) ||
+        ((uintptr_t)out_outer & 3u))
+        return PMN_ERR_INVALID_ARG;
+    if (batch > 65535 || rows * (cols / 64) >= 0xFFFFFF00LL) return PMN_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t *gmax = reinterpret_cast<uint32_t *>(out_outer);  // the largest dec(S) * g, then g'
+    if (cudaMemsetAsync(gmax, 0, (size_t)batch * sizeof(uint32_t), s) != cudaSuccess) return PMN_ERR_CUDA;
+    const bool per_row = outer_mode == PMN_OUTER_PER_ROW;
+    if (rows > 0 && cols > 0) {
+        const uint32_t wpr = (uint32_t)(cols / 64), nw = (uint32_t)rows * wpr;
+        nvfp4_scale_max_kernel<<<dim3((nw + 255) / 256, (unsigned)batch), 256, 0, s>>>(scales, outer, per_row,
+                                                                                        (uint32_t)rows, wpr, gmax);
+        dim3 grid((unsigned)((cols + 127) / 128), (unsigned)((rows + 127) / 128), (unsigned)batch);
+        const int sr = rounding == PMN_ROUND_SR;
+        if (per_row)
+            requant_transpose_nvfp4_kernel<true><<<grid, 128, 0, s>>>(codes, scales, outer, rows, cols, seed, tag,
+                                                                      sr, gmax, out, out_scales);
+        else
+            requant_transpose_nvfp4_kernel<false><<<grid, 128, 0, s>>>(codes, scales, outer, rows, cols, seed, tag,
+                                                                       sr, gmax, out, out_scales);
+    }
+    nvfp4_outer_finalize_kernel<<<(unsigned)((batch + 255) / 256), 256, 0, s>>>(out_outer, batch);
     return launch_status();
 }
 

@@ -36,6 +36,7 @@ SIGNATURES = {
     "pmn_nvfp4_quantize": ([_P, _I64, _I64, _I64, _I, _I, _I64, _I, _P, _P, _P, _P, _P], _I),
     "pmn_nvfp4_quantize_per_group_noalloc": ([_P, _I64, _I64, _I64, _I, _P, _P, _P, _P], _I),
     "pmn_requant_transpose_sr_mxfp8": ([_P, _P, _P, _I, _I64, _I64, _I64, _U64, _U32, _I, _P, _P, _P], _I),
+    "pmn_requant_transpose_sr_nvfp4": ([_P, _P, _P, _I, _I64, _I64, _I64, _U64, _U32, _I, _P, _P, _P, _P], _I),
     "pmn_mxfp8_quantize": ([_P, _I64, _I64, _I, _P, _P, _P], _I),
     "pmn_mxfp8_quantize_swiglu": ([_P, _I64, _I64, _P, _P, _P, _P], _I),
     "pmn_grouped_gemm_nvfp4": ([_P, _P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P], _I),
@@ -163,6 +164,28 @@ def requant_transpose_sr_mxfp8(codes, scales, outer, outer_per_row, batch, rows,
                                               _ptr(sc), _stream(stream))
     _check(st, "requant_transpose_sr_mxfp8")
     return q, sc
+
+
+def requant_transpose_sr_nvfp4(codes, scales, outer, outer_per_row, batch, rows, cols, seed, tag,
+                               stochastic=True, out=None, stream=None):
+    """NVFP4 [batch, rows, cols] -> NVFP4 of the transpose with stochastic
+    rounding (u8 codes [batch, cols, rows/2], u8 E4M3 [batch, cols, rows/16],
+    f32 outer [batch]): the FP4 backward's requantisation."""
+    _dev(codes, torch.uint8)
+    _dev(scales, torch.uint8)
+    _dev(outer, torch.float32)
+    if out is None:
+        q = torch.empty((batch, cols, rows // 2), dtype=torch.uint8, device=codes.device)
+        sc = torch.empty((batch, cols, rows // 16), dtype=torch.uint8, device=codes.device)
+        g = torch.empty((batch,), dtype=torch.float32, device=codes.device)
+    else:
+        q, sc, g = out
+    st = lib().pmn_requant_transpose_sr_nvfp4(_ptr(codes), _ptr(scales), _ptr(outer),
+                                              OUTER_PER_ROW if outer_per_row else OUTER_PER_GROUP, batch, rows,
+                                              cols, seed, tag, ROUND_SR if stochastic else ROUND_RN, _ptr(q),
+                                              _ptr(sc), _ptr(g), _stream(stream))
+    _check(st, "requant_transpose_sr_nvfp4")
+    return q, sc, g
 
 
 def mxfp8_quantize(x, transpose=False, out=None, stream=None):

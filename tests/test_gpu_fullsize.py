@@ -125,6 +125,25 @@ def test_fullsize_requant_weights_and_activations(run):
     same(hu(L.xt[1][0][:, lo // 32:hi // 32]), qs[0], "X^T scales")
 
 
+def test_fullsize_requant_nvfp4_weights(run):
+    """The FP4 backward's requantisation of all 384 experts' w1 in one call;
+    two experts compared byte for byte with the oracle's requantisation of
+    its own NVFP4 of the same bf16 weights (random bits by the full index)."""
+    from precision_moe_numerics_gb300 import pmn
+    L = run["L"]
+    E, F2, D = L.w1.shape
+    q, qs, qg = pmn.requant_transpose_sr_nvfp4(L.w1q[0], L.w1q[1], L.w1q[2], False, E, F2, D, SEED, oracle.TAG_W1)
+    torch.cuda.synchronize()
+    assert pmn.get_device_error() == 0
+    for e in run["experts"][:2]:
+        c, s, g = oracle_w(run, "w1", e)
+        rc, rs, rg = oracle.requant_transpose_nvfp4(c, s, g, False, 1, F2, D, SEED, oracle.TAG_W1, b_begin=e)
+        same(hu(q[e]), rc[0], "W1^T NVFP4 codes")
+        same(hu(qs[e]), rs[0], "W1^T NVFP4 scales")
+        same(hu(qg[e:e + 1]), rg, "W1^T NVFP4 outer")
+    del q, qs, qg
+
+
 def test_fullsize_gradient_quantisation(run):
     L, r = run["L"], run["r"]
     lo, hi = seg(r, run["experts"][1])
