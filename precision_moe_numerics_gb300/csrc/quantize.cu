@@ -968,17 +968,17 @@ __global__ void nvfp4_outer_finalize_kernel(float *out_outer, int64_t batch)
 }
 
 // Stochastic rounding of y onto E2M1 (sign kept): with ulp the grid step at
-// |y| (0.5 below 2, 1 below 4, 2 above), t = |y| / ulp, the 16 leading
-// fraction bits f16 = floor((t - floor t) 2^16) and a carry from rb16 + f16
-// round up; 6 saturates.  Every step is exact in binary32.
+// |y| (0.5 below 2, 1 below 4, 2 above) and t = |y| / ulp, the grid index is
+// floor(t) plus the carry of rb16 + the 16 leading fraction bits, i.e.
+// (floor(t 2^16) + rb16) >> 16; 6 saturates.  t 2^16 < 2^19 is exact, and
+// adding 2^23 rounded toward zero leaves floor(t 2^16) in the low mantissa
+// bits, so no float-to-integer conversion is needed.
 __device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t rb16)
 {
-    const float a = fabsf(y);
-    const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
-    const float t = a * inv;
-    const float fl = floorf(t);
-    const uint32_t f16 = (uint32_t)((t - fl) * 65536.0f);
-    const uint32_t k = (uint32_t)fl + ((rb16 + f16) >> 16);
+    const float a = fminf(fabsf(y), 7.0f);  // every value >= 6 gives code 7
+    const float sc = a < 2.0f ? 131072.0f : (a < 4.0f ? 65536.0f : 32768.0f);  // 2^16 / ulp
+    const uint32_t u = __float_as_uint(__fadd_rz(__fmul_rn(a, sc), 8388608.0f)) - 0x4B000000u;
+    const uint32_t k = (u + rb16) >> 16;
     const uint32_t code = a < 2.0f ? k : (a < 4.0f ? k + 2u : min(k + 4u, 7u));
     return code | (signbit(y) ? 8u : 0u);
 }
@@ -996,7 +996,7 @@ __device__ __forceinline__ uint32_t sr_bits_of(const uint4 &wd, int e)
 // 16 rows of one column are exactly one output 16-block and one Philox
 // counter.  CTA = 4 warps = 128 rows x 128 columns.
 template <bool PER_ROW>
-__global__ void __launch_bounds__(128) requant_transpose_nvfp4_kernel(
+__global__ void __launch_bounds__(128, 4) requant_transpose_nvfp4_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, const float *__restrict__ outer,
     int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, int stochastic, const uint32_t *__restrict__ gmax,
     uint8_t *__restrict__ out, uint8_t *__restrict__ out_sc)
@@ -1025,6 +1025,9 @@ __global__ void __launch_bounds__(128) requant_transpose_nvfp4_kernel(
     const float six_g = __fmul_rn(6.0f, gp);
     const uint64_t j0 = (uint64_t)((b * cols + col0) * rows + row0) >> 4;
     const uint64_t jstep = (uint64_t)rows >> 4;
+    const uint32_t jhi0 = (uint32_t)(j0 >> 32);
+    const bool one_hi = (uint32_t)((j0 + 7 * jstep) >> 32) == jhi0;
+    const PhiloxPrefix pre = philox_prefix(seed, tag, jhi0);
     auto column_pair = [&](auto kc) {
         constexpr int K = decltype(kc)::value;
         uint32_t cs[16];  // exact code * S of columns 2K (low halves) and 2K + 1 (high halves)
@@ -1046,7 +1049,8 @@ __global__ void __launch_bounds__(128) requant_transpose_nvfp4_kernel(
             const float r = sd == 0.0f ? 0.0f : __frcp_rn(sd);
             uint32_t packed[2] = {0u, 0u};
             if (stochastic) {
-                const uint4 wd = sr_words16(seed, tag, j0 + (uint64_t)c * jstep);
+                const uint64_t j = j0 + (uint64_t)c * jstep;
+                const uint4 wd = one_hi ? philox_from_prefix(pre, (uint32_t)j) : sr_words16(seed, tag, j);
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     packed[i >> 3] |= e2m1_sr(__fmul_rn(d[i], r), sr_bits_of(wd, i)) << (4 * (i & 7));
