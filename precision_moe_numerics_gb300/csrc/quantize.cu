@@ -983,6 +983,26 @@ __device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t rb16)
     return code | (signbit(y) ? 8u : 0u);
 }
 
+// Hardware stochastic rounding of four values to E2M1 (nibble i = element i,
+// sign kept).  The convert applies the same add-and-carry rule as e2m1_sr but
+// reads its random bits in another order than the E4M3 one: element 0 takes
+// bytes 2 and 0 of rbits as one 16-bit value, element 2 bytes 3 and 1,
+// elements 1 and 3 the same values bit-reversed (measured over 4 M inputs).
+// Swapping bytes 1 and 2 of a Philox word therefore gives every element the
+// 16 bits that sr_bits_of assigns it.  PMN_FP4_HW_SR=0 selects the integer
+// rounding e2m1_sr instead (the same bytes).
+#ifndef PMN_FP4_HW_SR
+#define PMN_FP4_HW_SR 1
+#endif
+__device__ __forceinline__ uint32_t cvt_e2m1x4_rs(float e0, float e1, float e2, float e3, uint32_t word)
+{
+    uint16_t r;
+    asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
+        : "=h"(r)
+        : "f"(e3), "f"(e2), "f"(e1), "f"(e0), "r"(__byte_perm(word, 0u, 0x3120u)));
+    return r;
+}
+
 // 16 random bits of element e (0..15) of a Philox block: word e / 4; low or
 // high half; odd elements bit-reversed.
 __device__ __forceinline__ uint32_t sr_bits_of(const uint4 &wd, int e)
@@ -1051,9 +1071,18 @@ __global__ void __launch_bounds__(128, 4) requant_transpose_nvfp4_kernel(
             if (stochastic) {
                 const uint64_t j = j0 + (uint64_t)c * jstep;
                 const uint4 wd = one_hi ? philox_from_prefix(pre, (uint32_t)j) : sr_words16(seed, tag, j);
+#if PMN_FP4_HW_SR
+                const uint32_t wv[4] = {wd.x, wd.y, wd.z, wd.w};
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    packed[q4 >> 1] |= cvt_e2m1x4_rs(__fmul_rn(d[4 * q4], r), __fmul_rn(d[4 * q4 + 1], r),
+                                                     __fmul_rn(d[4 * q4 + 2], r), __fmul_rn(d[4 * q4 + 3], r),
+                                                     wv[q4]) << (16 * (q4 & 1));
+#else
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     packed[i >> 3] |= e2m1_sr(__fmul_rn(d[i], r), sr_bits_of(wd, i)) << (4 * (i & 7));
+#endif
             } else {
 #pragma unroll
                 for (int i = 0; i < 16; i += 2)
