@@ -29,7 +29,7 @@ def test_header_declares_the_path():
     for name in ["pmn_nvfp4_quantize", "pmn_requant_transpose_sr_mxfp8", "pmn_grouped_gemm_nvfp4",
                  "pmn_gemm_mxfp8", "pmn_w2_gemm_rht_s2f6", "pmn_mxfp8_quantize", "pmn_rht_s2f6_quantize",
                  "pmn_get_device_error", "pmn_status_string", "pmn_version", "pmn_combine_receive_s2f6",
-                 "pmn_mxfp8_quantize_swiglu"]:
+                 "pmn_mxfp8_quantize_swiglu", "pmn_requant_transpose_sr_nvfp4"]:
         assert name in syms
 
 
@@ -77,6 +77,17 @@ def test_host_argument_checks_need_no_gpu(libpath):
     assert L.pmn_mxfp8_quantize_swiglu(fake, 4, 48, fake, fake, null, null) == pmn.ERR_INVALID_ARG
     assert L.pmn_mxfp8_quantize_swiglu(fake + 2, 4, 64, fake, fake, null, null) == pmn.ERR_INVALID_ARG
     assert L.pmn_mxfp8_quantize_swiglu(null, 0, 64, null, null, null, null) == pmn.OK
+    # FP4 backward requantisation: rows % 32, cols % 64, unknown rounding, misaligned outer output
+    assert L.pmn_requant_transpose_sr_nvfp4(fake, fake, fake, 0, 1, 48, 64, 0, 1, 0, fake, fake, fake,
+                                            null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_requant_transpose_sr_nvfp4(fake, fake, fake, 0, 1, 64, 96, 0, 1, 0, fake, fake, fake,
+                                            null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_requant_transpose_sr_nvfp4(fake, fake, fake, 0, 1, 64, 64, 0, 1, 5, fake, fake, fake,
+                                            null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_requant_transpose_sr_nvfp4(fake, fake, fake, 0, 1, 64, 64, 0, 1, 0, fake, fake, fake + 2,
+                                            null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_requant_transpose_sr_nvfp4(null, null, null, 0, 0, 64, 64, 0, 1, 0, null, null, null,
+                                            null) == pmn.OK          # no entry: nothing to do
     # more groups than the fixed scratch holds: rejected before any pointer is used
     assert L.pmn_nvfp4_quantize_per_group_noalloc(fake, 1025 * 16, 64, 16, 0, fake, fake, fake,
                                                   null) == pmn.ERR_INVALID_ARG
