@@ -294,11 +294,8 @@ def main():
         raise RuntimeError("device error during the timed region")
     per_call_ms = {name: sum(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)) / args.steps
                    for i, (name, _) in enumerate(calls)}
-    t = torch.tensor([ms_total], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_step = t.item() / args.steps
-    value = flops_step * world / (ms_step * 1e-3) / 1e12
+    ms_step = max_over_ranks(ms_total, world, dist, dev) / args.steps
+    value = whole_job_value(flops_step, world, ms_step)
 
     # ------------------------------------------------------------ end to end
     e2e = None
@@ -408,6 +405,21 @@ def run_decode(L, args, dev, W, layer, pmn, reps=20):
             "ms": round(ms, 4), "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 2), "weight_bytes": wb,
             "algorithmic_bytes": by, "GB/s": round(gbs, 1), "hbm_frac": round(gbs / pk["hbm_gbs"], 3),
             "bound": "hbm", "reps": reps, "gpu_launches": 4 * reps}
+
+
+def max_over_ranks(ms_total, world, dist, device):
+    """The timed region's length (ms), the maximum over the ranks: each rank
+    times its own replica, and the job takes as long as the slowest."""
+    import torch
+    t = torch.tensor([float(ms_total)], device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def whole_job_value(flops_per_rank_step, world, ms_step):
+    """Whole-job TFLOP/s: every rank's FLOPs over the slowest rank's step time."""
+    return flops_per_rank_step * world / (ms_step * 1e-3) / 1e12
 
 
 def run_combine(payload, r, args, dev, pmn, reps=20):
