@@ -402,6 +402,17 @@ def swiglu_bf16(y_bf16_bits, f):
     return bf16_rne_array(h)
 
 
+def swiglu_bf16_from_f64(y, f):
+    """h = silu(gate) * up from binary64 gate | up values [rows, 2F] (a GEMM's
+    exact result, not rounded to bf16 first), rounded once to bfloat16.
+    Reading, for an epilogue that forms h from the GEMM's accumulator: the
+    unfused path rounds Y to bf16 before the SwiGLU, the fused one does not."""
+    yf = _c(y, np.float64)
+    a = yf[:, :f]
+    b = yf[:, f:2 * f]
+    return bf16_rne_array(a * b / (1.0 + np.exp(-a)))
+
+
 def bf16_rne_array(v):
     """Round binary64 values to bfloat16 bits (nearest even), element by element."""
     v = _c(v, np.float64)

@@ -345,6 +345,22 @@ def test_swiglu_vs_torch_silu():
     assert torch.all((got - ref).abs() <= ulp)
 
 
+def test_swiglu_from_f64_vs_torch_and_bf16_inputs():
+    """SwiGLU on binary64 GEMM outputs: against torch's silu in float64 (one
+    bf16 rounding), and equal to the bf16-input form when the inputs are
+    themselves bf16 values."""
+    rng = np.random.default_rng(10)
+    y = rng.standard_normal((16, 96)) * 3.0
+    h = oracle.swiglu_bf16_from_f64(y, 48)
+    yt = torch.from_numpy(y)
+    ref = torch.nn.functional.silu(yt[:, :48]) * yt[:, 48:]
+    got = torch.from_numpy(W.bf16_bits_to_f32(h).astype(np.float64))
+    assert torch.all((got - ref).abs() <= ref.abs() * 2.0 ** -8 + 1e-30)
+    yb = W.normal_bf16_host(rng, (16, 96), 2.0)
+    assert np.array_equal(oracle.swiglu_bf16_from_f64(W.bf16_bits_to_f32(yb).astype(np.float64), 48),
+                          oracle.swiglu_bf16(yb, 48))
+
+
 def test_requant_window_equals_slice_of_full():
     """The windowed form (used for sampled checks at full size) equals the
     matching slice of the whole-tensor computation, random bits included."""
