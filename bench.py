@@ -351,20 +351,16 @@ def main():
 
     clocks = clk.summary()
     if rank == 0:
-        line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4+mxfp8",
-                "data": "synthetic", "config": {
-                    "workload": WORKLOAD, "routed_rows": r.real_rows, "padded_rows": r.rows,
-                    "experts": L.shape.experts, "d_model": L.shape.d_model, "d_ff": L.shape.d_ff,
-                    "flops_per_step": flops_step, "l2": "inputs larger than L2 (no flush needed)",
-                    "parallelism": "replicas" if world > 1 else "single-gpu"},
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "decode": dec, "combine_receive": comb, "mxfp8_forward": mxf, "fp4_backward_requant": fp4b,
-                "gpu_launches": (layer.launches_per_step() if not args.only else
-                                 sum(layer.LAUNCHES.get(n, 1) for n in args.only.split(","))) * args.steps,
-                "clocks": clocks,
-                "components": comps}
-        print(json.dumps(line))
+        launches = (layer.launches_per_step() if not args.only else
+                    sum(layer.LAUNCHES.get(n, 1) for n in args.only.split(","))) * args.steps
+        config = {"workload": WORKLOAD, "routed_rows": r.real_rows, "padded_rows": r.rows,
+                  "experts": L.shape.experts, "d_model": L.shape.d_model, "d_ff": L.shape.d_ff,
+                  "flops_per_step": flops_step, "l2": "inputs larger than L2 (no flush needed)",
+                  "parallelism": "replicas" if world > 1 else "single-gpu"}
+        extra = {"decode": dec, "combine_receive": comb, "mxfp8_forward": mxf, "fp4_backward_requant": fp4b,
+                 "components": comps}
+        print(json.dumps(result_line(value, world, args.steps, args.warmup, ms_step, config, roof, cpu, e2e,
+                                     launches, clocks, extra)))
     if world > 1:
         dist.destroy_process_group()
 
@@ -405,6 +401,18 @@ def run_decode(L, args, dev, W, layer, pmn, reps=20):
             "ms": round(ms, 4), "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 2), "weight_bytes": wb,
             "algorithmic_bytes": by, "GB/s": round(gbs, 1), "hbm_frac": round(gbs / pk["hbm_gbs"], 3),
             "bound": "hbm", "reps": reps, "gpu_launches": 4 * reps}
+
+
+def result_line(value, world, steps, warmup, ms_step, config, roofline, cpu, e2e, launches, clocks, extra):
+    """The one JSON line of the default run: the contract's keys, then the
+    measurements made beside the step."""
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": steps, "warmup": warmup, "ms_per_step": round(ms_step, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4+mxfp8",
+            "data": "synthetic", "config": config, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks}
+    line.update(extra)
+    return line
 
 
 def max_over_ranks(ms_total, world, dist, device):

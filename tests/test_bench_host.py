@@ -90,3 +90,23 @@ def test_mxfp8_forward_accounting():
     assert fl == 2.0 * 131072 * 3072 * 4096 + 2.0 * 131072 * 4096 * 1536
     w = 384 * (3072 * 4096 + 4096 * 1536)        # weight elements: bf16 read, MXFP8 written and read
     assert by > w * (2 + 2 * 1.03125) and by < w * (2 + 2 * 1.03125) * 1.25
+
+
+def test_result_line_carries_the_contract_keys():
+    import json
+    b = load_bench()
+    roof = {"bound": "hbm", "achieved": 5300.0, "peak": 6680.8, "unit": "GB/s", "frac": 0.79, "traffic": 1.9e10}
+    cpu = {"value": 0.09, "unit": "TFLOP/s", "cores": 16, "kind": "oracle", "sample": "34 experts"}
+    e2e = {"value": 650.0, "unit": "TFLOP/s", "h2d_bytes_per_step": 1, "d2h_bytes_per_step": 2}
+    clocks = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    line = b.result_line(747.2, 1, 30, 3, 19.87, {"workload": "w"}, roof, cpu, e2e, 540, clocks,
+                         {"decode": None, "components": {}})
+    json.dumps(line)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e",
+                "gpu_launches", "clocks"):
+        assert key in line, key
+    assert line["value"] == 747.2 and line["higher_is_better"] is True and line["scaling"] == "weak"
+    assert line["data"] == "synthetic" and line["gpu_launches"] == 540 and "workload" in line["config"]
+    assert set(roof) <= set(line["roofline"]) and line["cpu_baseline"]["kind"] == "oracle"
+    assert "decode" in line and "components" in line
