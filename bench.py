@@ -2,8 +2,9 @@
 
 One step = one pass of the whole path over one batch: NVFP4 quantisation of
 the bf16 master weights (per expert) and of the routed activations (per token,
-4/6), the grouped NVFP4 w1 GEMM, SwiGLU + NVFP4 quantisation of h, the grouped
-NVFP4 w2 GEMM with the fused RHT-32 + S2F6 combine quantisation, the
+4/6), the grouped NVFP4 w1 GEMM with SwiGLU in its epilogue and the NVFP4
+quantisation of h, the grouped NVFP4 w2 GEMM with the fused RHT-32 + S2F6
+combine quantisation, the
 dequantise -> transpose -> SR -> MXFP8 requantisation of X, H, W1 and W2, the
 MXFP8 quantisation of dY and dY1 (both orientations) and the four grouped
 MXFP8 gradient GEMMs (dX, dW1, dH, dW2).  Workload: 384 experts, top-8 routing
@@ -166,7 +167,7 @@ def oracle_sample(inputs, experts, seed=0):
         w2q = oracle.nvfp4_quantize(w2, oracle.OUTER_PER_GROUP, group_offsets=[0, D])
         xq = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW, four_over_six=True)
         y = oracle.grouped_gemm_nvfp4(xq[0], xq[1], xq[2], w1q[0][None], w1q[1][None], w1q[2], [0, n])
-        h = oracle.swiglu_bf16(oracle.bf16_rne_array(y), F)
+        h = oracle.swiglu_bf16_from_f64(y, F)
         hq = oracle.nvfp4_quantize(h, oracle.OUTER_PER_ROW, four_over_six=True)
         z = oracle.grouped_gemm_nvfp4(hq[0], hq[1], hq[2], w2q[0][None], w2q[1][None], w2q[2], [0, n])
         oracle.rht_s2f6(z.astype(np.float32), seed)
@@ -209,7 +210,10 @@ def main():
     ap.add_argument("--only", default=None, help="time only this call of the step (profiling)")
     ap.add_argument("--combine-only", action="store_true",
                     help="profiling: time only the combine receive, on a seeded payload (--steps calls)")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode, combine-receive, MXFP8-forward and FP4-requant measurements")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode, combine-receive, MXFP8-forward, "
+                    "FP4-requant and single-expert measurements")
+    ap.add_argument("--single-expert-only", action="store_true",
+                    help="profiling: only the single-expert forward (T = 4096), printed as one JSON object")
     args = ap.parse_args()
     rank, world, local = dist_env()
 
@@ -229,6 +233,12 @@ def main():
     from precision_moe_numerics_gb300 import build, layer, pmn
     from precision_moe_numerics_gb300 import workloads as W
     build.build()
+
+    if args.single_expert_only:  # profiling: the single-expert forward alone (< 1 GB on the device)
+        res = run_single_expert(args, dev, W, pmn, reps=args.steps)
+        if rank == 0:
+            print(json.dumps({"single_expert": res}))
+        return
 
     if args.combine_only:  # profiling: the combine receive alone on a seeded payload (< 1 GB on the device)
         r = W.moe_routing(args.seed)
@@ -307,11 +317,12 @@ def main():
     if not args.no_decode and not args.only:
         dec = run_decode(L, args, dev, W, layer, pmn)
 
-    comb = mxf = fp4b = None
+    comb = mxf = fp4b = single = None
     if not args.no_decode and not args.only:
         comb = run_combine(L.z, r, args, dev, pmn)
         mxf = run_mxfp8_forward(inp, r, offsets, args, layer, pmn)
         fp4b = run_fp4_requant(L, args, pmn)
+        single = run_single_expert(args, dev, W, pmn)
 
     pk = peaks()
     comps = {}
@@ -358,7 +369,7 @@ def main():
                   "flops_per_step": flops_step, "l2": "inputs larger than L2 (no flush needed)",
                   "parallelism": "replicas" if world > 1 else "single-gpu"}
         extra = {"decode": dec, "combine_receive": comb, "mxfp8_forward": mxf, "fp4_backward_requant": fp4b,
-                 "components": comps}
+                 "single_expert": single, "components": comps}
         print(json.dumps(result_line(value, world, args.steps, args.warmup, ms_step, config, roof, cpu, e2e,
                                      launches, clocks, extra)))
     if world > 1:
@@ -400,7 +411,86 @@ def run_decode(L, args, dev, W, layer, pmn, reps=20):
                                                     int((r.counts > 0).sum())),
             "ms": round(ms, 4), "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 2), "weight_bytes": wb,
             "algorithmic_bytes": by, "GB/s": round(gbs, 1), "hbm_frac": round(gbs / pk["hbm_gbs"], 3),
-            "bound": "hbm", "reps": reps, "gpu_launches": 4 * reps}
+            "bound": "hbm", "reps": reps,
+            "gpu_launches": sum(layer.LAUNCHES.get(n, 1) for n, _ in fwd.kernel_calls()) * reps}
+
+
+def run_single_expert(args, dev, W, pmn, reps=20):
+    """The single-expert forward: T = 4096 tokens (N(0,1), 0.1 % of entries
+    x30) through one expert (w1 [3072, 4096], w2 [4096, 1536], N(0, 0.02)).
+    Each call of the forward is timed alone with CUDA events on the launching
+    stream, `reps` times, with L2 flushed (a 256 MB write) before every timed
+    call, since the operands (17 MB of NVFP4) fit in L2.  The w1 GEMM at this
+    shape is tensor-bound (arithmetic intensity ~2500 FLOP/B): its TFLOP/s
+    against the FP4 tensor peak is the measure of the block-scaled MMA
+    pipeline."""
+    import numpy as np
+    import torch
+    d = W.expert(args.seed)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    x, w1, w2 = bf(d["x"]), bf(d["w1"]), bf(d["w2"])
+    T, D = x.shape
+    F = w2.shape[1]
+    u8, f32 = torch.uint8, torch.float32
+    e = lambda *shape, dtype=u8: torch.empty(shape, dtype=dtype, device=dev)
+    xq = (e(T, D // 2), e(T, D // 16), e(T, dtype=f32))
+    w1q = (e(2 * F, D // 2), e(2 * F, D // 16), e(1, dtype=f32))
+    w2q = (e(D, F // 2), e(D, F // 16), e(1, dtype=f32))
+    hq = (e(T, F // 2), e(T, F // 16), e(T, dtype=f32))
+    h = e(T, F, dtype=torch.bfloat16)
+    y = e(T, 2 * F, dtype=torch.bfloat16)
+    z = e(T, D, dtype=torch.bfloat16)
+    ws = e(pmn.nvfp4_quantize_workspace_bytes(pmn.OUTER_PER_GROUP, D, D))
+    offs = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    w1q3 = lambda: (w1q[0].view(1, 2 * F, D // 2), w1q[1].view(1, 2 * F, D // 16), w1q[2])
+    w2q3 = lambda: (w2q[0].view(1, D, F // 2), w2q[1].view(1, D, F // 16), w2q[2])
+    g1, g2 = 2.0 * T * 2 * F * D, 2.0 * T * D * F
+    nv = 0.5 + 1 / 16
+    calls = [
+        ("quant_x", lambda: pmn.nvfp4_quantize(x, four_over_six=True, out=xq), 0, T * D * (2 + nv)),
+        ("quant_w1", lambda: pmn.nvfp4_quantize(w1, outer_mode=pmn.OUTER_PER_GROUP, rows_per_group=2 * F, out=w1q,
+                                                workspace=ws), 0, 2 * F * D * (2 + nv)),
+        ("quant_w2", lambda: pmn.nvfp4_quantize(w2, outer_mode=pmn.OUTER_PER_GROUP, rows_per_group=D, out=w2q,
+                                                workspace=ws), 0, D * F * (2 + nv)),
+        ("gemm1_swiglu_only", lambda: pmn.grouped_gemm_nvfp4(xq, w1q3(), offs, swiglu=True, out=h), g1,
+         (T * D + 2 * F * D) * nv + T * F * 2),
+        ("gemm1_swiglu_nvfp4", lambda: pmn.w1_gemm_swiglu_nvfp4(xq, w1q3(), offs, True, out=hq, h=h), g1,
+         (T * D + 2 * F * D) * nv + T * F * 2 * 2 + T * F * nv),
+        ("gemm1_bf16", lambda: pmn.grouped_gemm_nvfp4(xq, w1q3(), offs, out=y), g1,
+         (T * D + 2 * F * D) * nv + T * 2 * F * 2),
+        ("gemm2_bf16", lambda: pmn.grouped_gemm_nvfp4(hq, w2q3(), offs, out=z), g2, (T * F + D * F) * nv + T * D * 2),
+    ]
+    flush = torch.empty(256 << 20, dtype=u8, device=dev)
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+    fp4_peak = pk["bf16_tflops_sustained"] * NOMINAL_TC_RATIO["fp4"]
+    out = {}
+    for name, f, fl, by in calls:
+        for _ in range(3):
+            f()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            f()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in ev) / reps
+        c = {"ms": round(ms, 4), "GB/s": round(by / (ms * 1e-3) / 1e9, 1),
+             "hbm_frac": round(by / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 3)}
+        if fl:
+            c["TFLOP/s"] = round(fl / (ms * 1e-3) / 1e12, 1)
+            c["tc_frac"] = round(fl / (ms * 1e-3) / 1e12 / fp4_peak, 3)
+        out[name] = c
+    if pmn.get_device_error() != 0:
+        raise RuntimeError("device error in the single-expert forward")
+    fwd_ms = out["quant_x"]["ms"] + out["gemm1_swiglu_nvfp4"]["ms"] + out["gemm2_bf16"]["ms"]
+    return {"workload": "single expert forward: T=%d tokens, d_model %d, d_ff %d (w1 [%d, %d], w2 [%d, %d]); "
+                        "X NVFP4 4/6 per token, weights NVFP4 per expert (quantised once, resident)"
+                        % (T, D, F, 2 * F, D, D, F),
+            "l2": "flushed (256 MB write) before every timed call",
+            "forward_ms": round(fwd_ms, 4), "forward_TFLOP/s": round((g1 + g2) / (fwd_ms * 1e-3) / 1e12, 1),
+            "fp4_peak_tflops": round(fp4_peak, 1), "reps": reps, "calls": out}
 
 
 def result_line(value, world, steps, warmup, ms_step, config, roofline, cpu, e2e, launches, clocks, extra):

@@ -14,10 +14,10 @@
  *
  * Conventions for every call
  *  - All tensor arguments are DEVICE pointers owned by the caller; the library
- *    never synchronises the device inside a call and allocates nothing but
- *    the small stream-ordered scratch named below.  Work is
- *    enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy
- *    default stream) and returns immediately.
+ *    never synchronises the device inside a call and allocates nothing: where
+ *    a kernel needs scratch, the caller passes a workspace whose size a
+ *    query returns.  Work is enqueued on `stream` (a cudaStream_t passed as
+ *    void*; NULL = legacy default stream) and returns immediately.
  *  - Layouts are row-major and dense unless a leading dimension is given.
  *    NVFP4 tensor [R, C]: codes uint8 [R, C/2] (element 2i in the low nibble,
  *    2i+1 in the high nibble), scales uint8 [R, C/16] (E4M3), outer float32.
@@ -68,6 +68,7 @@ typedef int pmn_status;
 #define PMN_OUT_BF16 0
 #define PMN_OUT_F32 1
 #define PMN_OUT_RHT_S2F6 2
+#define PMN_OUT_SWIGLU_BF16 3
 /* grouping of pmn_gemm_mxfp8 */
 #define PMN_GROUP_M 0
 #define PMN_GROUP_K 1
@@ -85,6 +86,22 @@ PMN_API const char *pmn_status_string(pmn_status s);
 /* Reads and clears the device error word; synchronises `stream` only.
  * *err receives the PMN_DEVERR_* bits latched since the last call. */
 PMN_API pmn_status pmn_get_device_error(void *stream, int32_t *err);
+
+/* Wall-time limit, in nanoseconds, of every bounded device wait of the
+ * library's kernels (GEMM pipeline barriers, the weight quantiser's wait for
+ * a group's amax): a wait that runs out latches PMN_DEVERR_WAIT_TIMEOUT and
+ * its kernel winds down and returns.  Default 4 s.  Process-wide, read when
+ * a kernel is enqueued; returns the previous limit.  The pages have no
+ * counterpart: it exists so that failure handling can be exercised. */
+PMN_API uint64_t pmn_set_wait_limit_ns(uint64_t ns);
+
+/* Self-test of the bounded waits: enqueues one CTA whose thread waits on an
+ * mbarrier that nothing arrives on, then on a device counter that nothing
+ * increments, each for `limit_ns` (<= 2e9, else PMN_ERR_INVALID_ARG), with
+ * the wait primitives of the GEMMs and the weight quantiser.  Both waits run
+ * out: PMN_DEVERR_WAIT_TIMEOUT is latched and the kernel returns, leaving
+ * the context usable.  The pages have no counterpart. */
+PMN_API pmn_status pmn_wait_selftest(uint64_t limit_ns, void *stream);
 
 /*
  * NVFP4 quantisation [SR] (16-value blocks, E4M3 block scale set from the
@@ -110,29 +127,46 @@ PMN_API pmn_status pmn_get_device_error(void *stream, int32_t *err);
  *  outer    out float32 (see outer_mode).
  *  h_out    optional out bf16 [rows, cols]: the SwiGLU value that was
  *           quantised (PMN_IN_BF16_SWIGLU only; NULL to skip).
+ *  workspace, workspace_bytes  PER_GROUP only (ignored for PER_ROW): caller-
+ *           owned device scratch, 16-byte aligned, at least
+ *           pmn_nvfp4_quantize_workspace_bytes(...) bytes (else
+ *           PMN_ERR_INVALID_ARG); its contents on entry do not matter (the
+ *           call clears it on `stream`).  Calls that share one workspace must
+ *           not overlap on the GPU (calls on one stream are ordered).
  * PER_GROUP runs one persistent kernel that reads each group for its amax and
- * codes it while it is still in L2.  It draws (64 + 2 * groups) * 4 bytes of
- * scratch from the stream-ordered allocator (cudaMallocAsync / cudaFreeAsync
- * on `stream`); a failed allocation returns PMN_ERR_CUDA.  A group whose amax
- * pass never completes (bounded wait, 4 s) latches PMN_DEVERR_WAIT_TIMEOUT.
+ * codes it while it is still in L2; the workspace holds its ticket counter,
+ * per-group counts and amax.  A group whose amax pass never completes
+ * (bounded wait, pmn_set_wait_limit_ns) latches PMN_DEVERR_WAIT_TIMEOUT.
  */
 PMN_API pmn_status pmn_nvfp4_quantize(const void *x, int64_t rows, int64_t cols, int64_t ldx, int in_mode,
                               int outer_mode, int64_t rows_per_group, int four_over_six,
                               uint8_t *codes, uint8_t *scales, float *outer, void *h_out,
-                              void *stream);
+                              void *workspace, int64_t workspace_bytes, void *stream);
+
+/* Workspace bytes pmn_nvfp4_quantize needs: (64 + 2 * groups) * 4 for
+ * PMN_OUTER_PER_GROUP (groups = rows / rows_per_group), 0 for
+ * PMN_OUTER_PER_ROW, -1 for invalid arguments.  Host only; no CUDA call. */
+PMN_API int64_t pmn_nvfp4_quantize_workspace_bytes(int outer_mode, int64_t rows, int64_t rows_per_group);
 
 /*
- * pmn_nvfp4_quantize with PMN_OUTER_PER_GROUP (ldx = cols, no 4/6 input
- * restriction), computing the same bytes, but with its scratch in a fixed
- * device array of the library instead of a stream-ordered allocation: the
- * call allocates nothing.  The pages have no counterpart to this entry point;
- * it exists for callers that must not allocate (graph capture without a
- * memory pool, allocation-free serving loops).
+ * pmn_nvfp4_quantize with PMN_OUTER_PER_GROUP (ldx = cols), computing the
+ * same bytes, but with its scratch in a fixed device array of the library
+ * (a file-scope __device__ array of (64 + 2 * 1024) 32-bit words, which every
+ * GPU that loads the library holds until the process exits) instead of a
+ * workspace: the caller neither allocates nor passes scratch.  The pages
+ * have no counterpart to this entry point.  It is for callers that cannot
+ * call cudaMalloc or any allocator while they run: a serving loop whose
+ * device memory is all reserved at start-up, or a host framework that owns
+ * every device allocation and hands this library only its input and output
+ * buffers.
  *  rows / rows_per_group <= 1024 groups, else PMN_ERR_INVALID_ARG.
  *  Other arguments and rules as pmn_nvfp4_quantize.
- * The fixed scratch is shared by all calls on a device: calls on different
- * streams must not overlap in time (calls on one stream are ordered).  The
- * scratch is cleared on `stream` before the kernel runs.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, once per device, with that device current).  The
+ * array is shared by every call on a device and keeps the last call's
+ * contents; each call clears it on `stream` before its kernel runs.  Calls
+ * that overlap on the GPU (on different streams) race on it; calls on one
+ * stream are ordered.
  */
 PMN_API pmn_status pmn_nvfp4_quantize_per_group_noalloc(const void *x, int64_t rows, int64_t cols,
                                                         int64_t rows_per_group, int four_over_six,
@@ -235,13 +269,49 @@ PMN_API pmn_status pmn_mxfp8_quantize_swiglu(const void *y, int64_t rows, int64_
  *           read and checked on the device: invalid offsets run nothing and
  *           latch PMN_DEVERR_BAD_OFFSETS.  num_experts <= 1024.
  *  n        multiple of 128;  k multiple of 256.
- *  out_kind PMN_OUT_BF16 (bf16 [total_rows, n]) or PMN_OUT_F32.
+ *  out_kind PMN_OUT_BF16 (bf16 [total_rows, n]) or PMN_OUT_F32, or
+ *           PMN_OUT_SWIGLU_BF16 (n % 256 == 0): bf16 h [total_rows, n/2] with
+ *           h[m, j] = silu(Z[m, j]) * Z[m, n/2 + j] formed in float32 from the
+ *           float32 Z (not rounded to bf16 first), gate = the first n/2 rows
+ *           of each B_e, up = the last n/2, then rounded to bf16 (nearest
+ *           even).  SwiGLU between w1 and w2 is not on the pages; the w1
+ *           shape [2F, d_model] makes the layer gated.
+ * Rows outside every expert segment are not written.
  */
 PMN_API pmn_status pmn_grouped_gemm_nvfp4(const uint8_t *a_codes, const uint8_t *a_scales,
                                   const float *a_outer, const uint8_t *b_codes,
                                   const uint8_t *b_scales, const float *b_outer,
                                   const int32_t *offsets, int num_experts, int64_t total_rows,
                                   int64_t n, int64_t k, int out_kind, void *out, void *stream);
+
+/*
+ * w1 GEMM with SwiGLU fused into its epilogue, then the NVFP4 quantisation
+ * of h with a per-token outer scale and the optional 4/6 choice [Cost]: the
+ * pages fuse quantisation into the GEMM epilogues [NVLink] and keep the
+ * expert forward in NVFP4 [Layers].  Two kernels on `stream`:
+ *   1. the grouped NVFP4 GEMM of pmn_grouped_gemm_nvfp4 with out_kind
+ *      PMN_OUT_SWIGLU_BF16 (n = 2 f) writes bf16 h [total_rows, f];
+ *   2. pmn_nvfp4_quantize(h, PER_ROW, four_over_six) of those rows; rows at
+ *      or past offsets[num_experts] (outside every expert segment) are
+ *      written as the quantisation of a zero row (codes 0, scales 0, outer 1).
+ * The per-token outer scale needs the amax of the whole row of h, which
+ * spans f / 128 tiles of the GEMM, so the codes are formed by the second
+ * kernel from h instead of in the GEMM's epilogue.
+ *  b_codes/b_scales/b_outer  NVFP4 W1 [num_experts, 2 f, k]: rows [0, f)
+ *           gate, [f, 2 f) up.
+ *  f        multiple of 128, <= 8192;  k multiple of 256.
+ *  h        caller-owned bf16 [total_rows, f]: receives h (the kernels'
+ *           scratch between the two steps; also a result).
+ *  codes    uint8 [total_rows, f/2]; scales uint8 [total_rows, f/16];
+ *  outer    float32 [total_rows].
+ * Other arguments as pmn_grouped_gemm_nvfp4.
+ */
+PMN_API pmn_status pmn_w1_gemm_swiglu_nvfp4(const uint8_t *a_codes, const uint8_t *a_scales,
+                                    const float *a_outer, const uint8_t *b_codes,
+                                    const uint8_t *b_scales, const float *b_outer,
+                                    const int32_t *offsets, int num_experts, int64_t total_rows,
+                                    int64_t f, int64_t k, int four_over_six, void *h,
+                                    uint8_t *codes, uint8_t *scales, float *outer, void *stream);
 
 /*
  * w2 GEMM with the combine quantisation fused into its epilogue [NVLink]:

@@ -23,6 +23,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -34,6 +35,12 @@ using namespace pmn;
 using namespace pmn::sm100;
 
 __device__ int g_pmn_device_error = 0;
+
+// Wall-time limit of the library's bounded device waits, read at each launch.
+static std::atomic<uint64_t> g_wait_limit_ns{4000000000ull};
+uint64_t pmn_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+extern "C" uint64_t pmn_set_wait_limit_ns(uint64_t ns) { return g_wait_limit_ns.exchange(ns); }
 
 // Pipeline trace points for profiling builds (-DPMN_TRACE): CTA 0 records
 // clock64() at each hand-off; compiled out otherwise.
@@ -133,6 +140,7 @@ struct GemmArgs {
     uint8_t *out_sc;
     uint64_t seed;
     float *debug_acc;        // RHT + S2F6 only, optional: the scaled fp32 accumulator [m, n]
+    uint64_t wait_ns;        // limit of every bounded wait (pmn_set_wait_limit_ns)
 };
 
 struct Tile {
@@ -171,7 +179,7 @@ __device__ __forceinline__ Tile get_tile(int t, const GemmArgs &p, const int *s_
     const int local = t - s_cum[lo];
     if (!p.group_k) {
         const int nt = (int)(p.n / TBN);
-        const int mi = local / nt, ni = local - mi * nt;  // consecutive tiles: adjacent N-tiles (cluster peers)
+        const int mi = local / nt, ni = local - mi * nt;  // consecutive tiles: adjacent N-tiles
         ti.m0 = __ldg(p.offsets + lo) + (int64_t)mi * BM;
         ti.n0 = (int64_t)ni * TBN;
         ti.row_end = __ldg(p.offsets + lo + 1);
@@ -217,13 +225,13 @@ __device__ __forceinline__ void sf_to_tmem(uint8_t *stages, uint32_t stg, uint32
 
 // Every lane of the warp waits; the outcome is made warp-uniform so that a
 // timeout can never split the warp before a .sync.aligned instruction.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
 {
-    const bool ok = mbar_wait(bar, parity);
+    const bool ok = mbar_wait(bar, parity, limit_ns);
     return __all_sync(0xFFFFFFFFu, ok) != 0;
 }
 
-template <int KIND, int OUT, int CS, int TBN>
+template <int KIND, int OUT, int TBN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
@@ -231,6 +239,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 {
     using C = Cfg<KIND, TBN>;
     constexpr int STAGES = C::STAGES;
+    constexpr bool SWI = OUT == PMN_OUT_SWIGLU_BF16;
+    static_assert(!SWI || (KIND == KIND_NVFP4 && TBN == 256), "SwiGLU tiles are 256-wide NVFP4 tiles");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
@@ -247,17 +257,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int *s_cum = reinterpret_cast<int *>(staging + 4 * C::EPI * STAGE_OUT_BYTES + 1024);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Cluster of CS CTAs along N: consecutive tiles (same expert and M-tile,
-    // adjacent N-tiles); CTA `rank` multicasts rows [rank*128/CS, +128/CS) of
-    // the shared A tile to every peer, and a stage is free only when every
-    // peer's MMAs have consumed it.
-    const uint32_t rank = CS > 1 ? cluster_ctarank() : 0u;
-    const uint16_t cl_mask = (uint16_t)((1u << CS) - 1u);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, CS);
+            mbar_init(bar_empty + 8 * s, 1);
             mbar_init(bar_sfr + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -310,7 +314,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (CS > 1) cluster_sync();  // peers' barriers are initialised before any multicast
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int total = *s_total;
@@ -323,9 +326,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int n_issued = 0, gc = 0;
             for (int t = blockIdx.x; t < total && !*(volatile int *)s_abort; t += gridDim.x) {
                 const Tile ti = get_tile<KIND, TBN>(t, p, s_cum, gc);
-                const int64_t brow = p.group_k ? ti.n0 : (int64_t)ti.g * p.n + ti.n0;
+                // SwiGLU tiles: h columns n0/2 .. n0/2 + 127 need the expert's gate
+                // rows n0/2 + (0..127) and up rows n/2 + n0/2 + (0..127) of B, loaded
+                // as two 128-row boxes into the B tile's two halves
+                const int64_t brow = p.group_k ? ti.n0 : (int64_t)ti.g * p.n + (SWI ? ti.n0 / 2 : ti.n0);
+                const int64_t brow_up = brow + p.n / 2;
                 for (int ks = 0; ks < ti.nks; ++ks) {
-                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1)) {
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.wait_ns)) {
                         *(volatile int *)s_abort = 1;
                         latch_error(PMN_DEVERR_WAIT_TIMEOUT);
                         break;
@@ -337,18 +344,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     mbar_arrive_expect_tx(fb, A_TILE_BYTES + C::B_TILE_BYTES + (C::SF_TMA ? (128u + TBN) * 16u : 0u));
                     // 128 bytes of K per stage: 256 fp4 or 128 fp8 values
                     const int32_t xk = (int32_t)(KIND == KIND_NVFP4 ? (int64_t)ks * 128 : ti.kb + (int64_t)ks * 128);
-                    if (CS > 1)
-                        tma_load_2d_mc(smem_u32(st) + rank * (BM / CS) * 128, &tmA, fb, xk,
-                                       (int32_t)(ti.m0 + rank * (BM / CS)), cl_mask);
-                    else
-                        tma_load_2d(smem_u32(st), &tmA, fb, xk, (int32_t)ti.m0);
+                    tma_load_2d(smem_u32(st), &tmA, fb, xk, (int32_t)ti.m0);
                     tma_load_2d(smem_u32(st + A_TILE_BYTES), &tmB, fb, xk, (int32_t)brow);
+                    if (SWI) tma_load_2d(smem_u32(st + A_TILE_BYTES + 128 * 128), &tmB, fb, xk, (int32_t)brow_up);
                     if (C::SF_TMA) {
                         // raw scale rows: 16-byte boxes (the MXFP8 stage's 4 bytes at (xk / 32) % 16)
                         const int32_t xs = KIND == KIND_NVFP4 ? ks * 16 : (int32_t)((xk / 32) & ~int32_t(15));
+                        const uint32_t rb = smem_u32(st + A_TILE_BYTES + C::B_TILE_BYTES + C::RAW_A);
                         tma_load_2d(smem_u32(st + A_TILE_BYTES + C::B_TILE_BYTES), &tmSA, fb, xs, (int32_t)ti.m0);
-                        tma_load_2d(smem_u32(st + A_TILE_BYTES + C::B_TILE_BYTES + C::RAW_A), &tmSB, fb, xs,
-                                    (int32_t)brow);
+                        tma_load_2d(rb, &tmSB, fb, xs, (int32_t)brow);
+                        if (SWI) tma_load_2d(rb + 128 * 16, &tmSB, fb, xs, (int32_t)brow_up);
                     }
                     issued |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -386,7 +391,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                         continue;
                     }
-                    ok = warp_wait(bar_full + 8 * stage, phase);
+                    ok = warp_wait(bar_full + 8 * stage, phase, p.wait_ns);
                     if (!ok || __any_sync(0xFFFFFFFFu, *(volatile int *)s_abort != 0)) {
                         if (!ok && lane == 0) {
                             *(volatile int *)s_abort = 1;
@@ -520,7 +525,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!vuse) return false;
                 prefetch(pre, vpre, qpre);
                 const uint32_t stage = quse % STAGES, phase = (quse / STAGES) & 1u;
-                ok = warp_wait(bar_empty + 8 * stage, phase ^ 1u);
+                ok = warp_wait(bar_empty + 8 * stage, phase ^ 1u, p.wait_ns);
                 if (!ok || __any_sync(0xFFFFFFFFu, *(volatile int *)s_abort != 0)) {
                     if (!ok && lane == 0) {
                         *(volatile int *)s_abort = 1;
@@ -596,7 +601,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             Tile ti;
             int t = next_tile(blockIdx.x, ti);
             while (ok && t < total) {
-                if (!mbar_wait(bar_acc_empty + 8 * abuf, aphase ^ 1) || *(volatile int *)s_abort) {
+                if (!mbar_wait(bar_acc_empty + 8 * abuf, aphase ^ 1, p.wait_ns) || *(volatile int *)s_abort) {
                     if (!*(volatile int *)s_abort) fail();
                     ok = false;
                     break;
@@ -609,8 +614,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // the stage's A and B tiles (implied by sf_ready where the
                     // scale-factor warps waited for the stage's TMA data) and
                     // its scale factors in TMEM
-                    if ((!C::SF_TMA && !mbar_wait(bar_full + 8 * stage, phase)) ||
-                        !mbar_wait(bar_sfr + 8 * stage, phase)) {
+                    if ((!C::SF_TMA && !mbar_wait(bar_full + 8 * stage, phase, p.wait_ns)) ||
+                        !mbar_wait(bar_sfr + 8 * stage, phase, p.wait_ns)) {
                         fail();
                         break;
                     }
@@ -635,8 +640,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         else
                             mma_mxfp8(d_tmem, ad, bd, make_idesc<KIND, TBN>((uint32_t)s), sfa, sfb, acc);
                     }
-                    if (CS > 1) tc_commit_mc(bar_empty + 8 * stage, cl_mask);
-                    else tc_commit(bar_empty + 8 * stage);
+                    tc_commit(bar_empty + 8 * stage);
                     if (ks == ti.nks - 1) tc_commit(bar_acc_full + 8 * abuf);
                     // the next tile is looked up while this stage's MMAs run
                     if (ks == 0) tn = next_tile(t + gridDim.x, tin);
@@ -674,7 +678,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // evict_first for dW1 / dW2
         uint64_t st_policy = 0;
         if (OUT == PMN_OUT_F32) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(st_policy));
-        constexpr int CH_PER_STORE = OUT == PMN_OUT_F32 ? 1 : (OUT == PMN_OUT_BF16 ? 2 : 4);
+        constexpr int CH_PER_STORE = OUT == PMN_OUT_F32 ? 1 : ((OUT == PMN_OUT_BF16 || SWI) ? 2 : 4);
         uint32_t nstore = 0;
         uint32_t abuf = 0, aphase = 0;
         int n_epi = 0, gc = 0;
@@ -690,10 +694,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 } else if (valid && OUT == PMN_OUT_BF16) {
                     uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + ((int64_t)ti.g * p.m + row) * p.n + ti.n0;
                     for (int c = 0; c < TBN; c += 8) *reinterpret_cast<uint4 *>(o + c) = make_uint4(0u, 0u, 0u, 0u);
+                } else if (valid && SWI) {  // silu(0) * 0
+                    uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + row * (p.n / 2) + ti.n0 / 2;
+                    for (int c = 0; c < TBN / 2; c += 8) *reinterpret_cast<uint4 *>(o + c) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 continue;
             }
-            if (!warp_wait(bar_acc_full + 8 * abuf, aphase)) {
+            if (!warp_wait(bar_acc_full + 8 * abuf, aphase, p.wait_ns)) {
                 if (lane == 0) {
                     *(volatile int *)s_abort = 1;
                     latch_error(PMN_DEVERR_WAIT_TIMEOUT);
@@ -718,9 +725,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // to the next tile's MMAs before any store; otherwise (and for the
             // register-hungry RHT + S2F6 conversion) chunks are read, converted
             // and stored in turn and the release follows the last read.
-            constexpr int NCH = OUT == PMN_OUT_F32 ? 8 : (OUT == PMN_OUT_BF16 ? 4 : 2);  // 16-byte pieces per chunk
+            constexpr int NCH = OUT == PMN_OUT_F32 ? 8 : ((OUT == PMN_OUT_BF16 || SWI) ? 4 : 2);  // 16-byte pieces per chunk
             constexpr int NC = TBN / 32;
-            constexpr bool TWO_PHASE = NC * NCH <= 32 && OUT != PMN_OUT_RHT_S2F6;
+            constexpr bool TWO_PHASE = NC * NCH <= 32 && OUT != PMN_OUT_RHT_S2F6 && !SWI;
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + abuf * TBN;
             auto convert = [&](uint32_t (&r)[32], int c, uint4 (&o)[NCH]) {
                 float v[32];
@@ -781,7 +788,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            const int32_t x = (int32_t)(ti.n0 + 32 * (c - part));
+                            const int32_t x = (int32_t)((SWI ? ti.n0 / 2 : ti.n0) + 32 * (c - part));
                             const int32_t y = (int32_t)(obase + ti.m0 + 32 * q);
                             if (OUT == PMN_OUT_F32) tma_store_2d_hint(&tmO, smem_u32(buf), x, y, st_policy);
                             else tma_store_2d(&tmO, smem_u32(buf), x, y);
@@ -790,16 +797,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ++nstore;
                     }
                 } else if (valid) {
-                    const int64_t col = ti.n0 + 32 * c;
+                    const int64_t col = (SWI ? ti.n0 / 2 : ti.n0) + 32 * c;
                     uint8_t *o8;
-                    if (OUT == PMN_OUT_F32) o8 = reinterpret_cast<uint8_t *>(reinterpret_cast<float *>(p.out) + orow * p.n + col);
+                    if (SWI) o8 = reinterpret_cast<uint8_t *>(reinterpret_cast<uint16_t *>(p.out) + orow * (p.n / 2) + col);
+                    else if (OUT == PMN_OUT_F32) o8 = reinterpret_cast<uint8_t *>(reinterpret_cast<float *>(p.out) + orow * p.n + col);
                     else if (OUT == PMN_OUT_BF16) o8 = reinterpret_cast<uint8_t *>(reinterpret_cast<uint16_t *>(p.out) + orow * p.n + col);
                     else o8 = reinterpret_cast<uint8_t *>(p.out) + orow * p.n + col;
 #pragma unroll
                     for (int j = 0; j < NCH; ++j) reinterpret_cast<uint4 *>(o8)[j] = o[j];
                 }
             };
-            if constexpr (TWO_PHASE) {
+            if constexpr (SWI) {
+                // accumulator columns 0..127 hold the gate values, 128..255 the up
+                // values of the same 128 h columns: chunk c of h pairs gate chunk c
+                // with up chunk c + 4.  All four are read, then the accumulator is
+                // released and h stored.
+                uint4 ch[4][NCH];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t rg[32], ru[32];
+                    tmem_ld_32x32b_x32(tbase + 32 * c, rg);
+                    tmem_ld_32x32b_x32(tbase + 128 + 32 * c, ru);
+                    tmem_ld_wait();
+                    uint32_t w[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        float hv[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            // y = acc * g_t * g_e, then h = silu(gate) * up in binary32
+                            const float a = __fmul_rn(__fmul_rn(__uint_as_float(rg[2 * j + u]), scale), gb);
+                            const float b = __fmul_rn(__fmul_rn(__uint_as_float(ru[2 * j + u]), scale), gb);
+                            hv[u] = __fmul_rn(__fdiv_rn(a, __fadd_rn(1.0f, expf(-a))), b);
+                        }
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(hv[0], hv[1]);
+                        w[j] = *reinterpret_cast<uint32_t *>(&b2);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) ch[c][j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                }
+                release();
+                if (slice_any) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) store(c, ch[c]);
+                }
+            } else if constexpr (TWO_PHASE) {
                 uint4 ch[NC][NCH];
                 if constexpr (OUT == PMN_OUT_F32) {
                     // fp32: the chunks' words are the output; one wait for all reads
@@ -854,7 +896,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (CS > 1) cluster_sync();  // no peer still multicasts into, or arrives on, this CTA
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
@@ -903,10 +944,11 @@ bool make_out_map(CUtensorMap *m, void *base, int out_kind, uint64_t n, uint64_t
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const CUtensorMapDataType dt = out_kind == PMN_OUT_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                   : out_kind == PMN_OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    const uint64_t es = out_kind == PMN_OUT_F32 ? 4 : (out_kind == PMN_OUT_BF16 ? 2 : 1);
+    const bool b16 = out_kind == PMN_OUT_BF16 || out_kind == PMN_OUT_SWIGLU_BF16;
+    const CUtensorMapDataType dt = out_kind == PMN_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : b16                   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const uint64_t es = out_kind == PMN_OUT_F32 ? 4 : (b16 ? 2 : 1);
     cuuint64_t dims[2] = {n, rows};
     cuuint64_t strides[1] = {n * es};
     cuuint32_t box[2] = {(cuuint32_t)(128 / es), 32};
@@ -937,82 +979,55 @@ struct GemmMaps {
     MapSpec a, b, sa, sb;
 };
 
-#ifndef PMN_GEMM_CLUSTER_MAX
-#define PMN_GEMM_CLUSTER_MAX 1
-#endif
 #ifndef PMN_GEMM_WIDE_M  // 256-wide tiles for M-grouped problems
 #define PMN_GEMM_WIDE_M 1
 #endif
 
-template <int KIND, int OUT, int CS, int TBN>
-pmn_status launch_gemm_cs(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
+template <int KIND, int OUT, int TBN>
+pmn_status launch_gemm_tbn(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
 {
     using C = Cfg<KIND, TBN>;
     CUtensorMap a, b, sa, sb;
     const uint32_t raw_w = 16;  // raw scale rows: one 16-byte box per row and stage
-    if (!make_map(&a, ms.a.base, ms.a.width_bytes, ms.a.rows, ms.a.pitch, 128, true, BM / CS) ||
-        !make_map(&b, ms.b.base, ms.b.width_bytes, ms.b.rows, ms.b.pitch, 128, true, TBN) ||
+    const uint32_t b_box = OUT == PMN_OUT_SWIGLU_BF16 ? 128 : TBN;  // SwiGLU: gate and up halves load separately
+    if (!make_map(&a, ms.a.base, ms.a.width_bytes, ms.a.rows, ms.a.pitch, 128, true, BM) ||
+        !make_map(&b, ms.b.base, ms.b.width_bytes, ms.b.rows, ms.b.pitch, 128, true, b_box) ||
         !make_map(&sa, ms.sa.base, ms.sa.width_bytes, ms.sa.rows, ms.sa.pitch, raw_w, false, BM) ||
-        !make_map(&sb, ms.sb.base, ms.sb.width_bytes, ms.sb.rows, ms.sb.pitch, raw_w, false, TBN))
+        !make_map(&sb, ms.sb.base, ms.sb.width_bytes, ms.sb.rows, ms.sb.pitch, raw_w, false, b_box))
         return PMN_ERR_CUDA;
     GemmArgs ka = args;  // for scale-factor warps that read global memory
+    ka.wait_ns = pmn_wait_limit_ns();
     ka.sa = static_cast<const uint8_t *>(ms.sa.base);
     ka.sb = static_cast<const uint8_t *>(ms.sb.base);
     ka.sa_pitch = (int64_t)ms.sa.pitch;
     ka.sb_pitch = (int64_t)ms.sb.pitch;
-    auto kern = block_scaled_gemm_kernel<KIND, OUT, CS, TBN>;
+    auto kern = block_scaled_gemm_kernel<KIND, OUT, TBN>;
     const int smem = C::SMEM_BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return PMN_ERR_CUDA;
     const int sms = num_sms();
     if (sms <= 0) return PMN_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cfg.gridDim = dim3(sms);
-    if constexpr (CS > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CS;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) return PMN_ERR_CUDA;
-        cfg.gridDim = dim3((unsigned)(clusters * CS));
-    }
-    if (cudaLaunchKernelEx(&cfg, kern, a, b, sa, sb, o, ka) != cudaSuccess) return PMN_ERR_CUDA;
+    kern<<<dim3((unsigned)sms), dim3(NUM_THREADS), smem, s>>>(a, b, sa, sb, o, ka);
     return cudaGetLastError() == cudaSuccess ? PMN_OK : PMN_ERR_CUDA;
-}
-
-template <int KIND, int OUT, int TBN>
-pmn_status launch_gemm_tbn(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
-{
-    const int64_t nt = args.n / TBN;
-    if constexpr (PMN_GEMM_CLUSTER_MAX >= 4)
-        if (nt % 4 == 0) return launch_gemm_cs<KIND, OUT, 4, TBN>(ms, o, args, s);
-    if constexpr (PMN_GEMM_CLUSTER_MAX >= 2)
-        if (nt % 2 == 0) return launch_gemm_cs<KIND, OUT, 2, TBN>(ms, o, args, s);
-    return launch_gemm_cs<KIND, OUT, 1, TBN>(ms, o, args, s);
 }
 
 // Tile width: 256 columns (N = 256 MMAs, half the operand traffic per
 // output) for M-grouped problems whose N is a multiple of 256 and whose
 // epilogue is a plain conversion; 128 otherwise (K-grouped gradients: short
 // per-expert K; the RHT + S2F6 epilogue), with double-buffered accumulators.
-// Cluster size: the largest of 4, 2, 1 (capped by PMN_GEMM_CLUSTER_MAX) that
-// divides the number of N-tiles.
 template <int KIND, int OUT>
 pmn_status launch_gemm(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
 {
     // 256-wide M-grouped tiles except under the RHT + S2F6 epilogue, whose
     // conversion is long enough that overlapping it with the next tile's MMAs
     // (two 128-wide accumulators) beats the halved A traffic
-    if (PMN_GEMM_WIDE_M && OUT != PMN_OUT_RHT_S2F6 && !args.group_k && args.n % 256 == 0)
+    if constexpr (OUT == PMN_OUT_SWIGLU_BF16) {
         return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);
-    return launch_gemm_tbn<KIND, OUT, 128>(ms, o, args, s);
+    } else {
+        if (PMN_GEMM_WIDE_M && OUT != PMN_OUT_RHT_S2F6 && !args.group_k && args.n % 256 == 0)
+            return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);
+        return launch_gemm_tbn<KIND, OUT, 128>(ms, o, args, s);
+    }
 }
 
 pmn_status nvfp4_common(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_outer,
@@ -1030,10 +1045,12 @@ pmn_status nvfp4_common(const uint8_t *a_codes, const uint8_t *a_scales, const f
         !aligned16(out) || ((uintptr_t)offsets & 3u) || ((uintptr_t)a_outer & 3u) || ((uintptr_t)b_outer & 3u))
         return PMN_ERR_INVALID_ARG;
     if (out_kind == PMN_OUT_RHT_S2F6 && !out_sc) return PMN_ERR_INVALID_ARG;
+    if (out_kind == PMN_OUT_SWIGLU_BF16 && n % 256 != 0) return PMN_ERR_INVALID_ARG;
     if (total_rows == 0) return PMN_OK;
     CUtensorMap mo;
     const uint64_t brows = (uint64_t)num_experts * (uint64_t)n;
-    if (!make_out_map(&mo, out, out_kind, n, total_rows)) return PMN_ERR_CUDA;
+    if (!make_out_map(&mo, out, out_kind, out_kind == PMN_OUT_SWIGLU_BF16 ? n / 2 : n, total_rows))
+        return PMN_ERR_CUDA;
     const uint64_t kb = (uint64_t)k / 2, ks = (uint64_t)k / 16;
     const GemmMaps ms{{a_codes, kb, (uint64_t)total_rows, kb}, {b_codes, kb, brows, kb},
                       {a_scales, ks, (uint64_t)total_rows, ks}, {b_scales, ks, brows, ks}};
@@ -1056,6 +1073,7 @@ pmn_status nvfp4_common(const uint8_t *a_codes, const uint8_t *a_scales, const f
         case PMN_OUT_BF16: return launch_gemm<KIND_NVFP4, PMN_OUT_BF16>(ms, mo, args, s);
         case PMN_OUT_F32: return launch_gemm<KIND_NVFP4, PMN_OUT_F32>(ms, mo, args, s);
         case PMN_OUT_RHT_S2F6: return launch_gemm<KIND_NVFP4, PMN_OUT_RHT_S2F6>(ms, mo, args, s);
+        case PMN_OUT_SWIGLU_BF16: return launch_gemm<KIND_NVFP4, PMN_OUT_SWIGLU_BF16>(ms, mo, args, s);
         default: return PMN_ERR_INVALID_ARG;
     }
 }
@@ -1078,6 +1096,8 @@ extern "C" const char *pmn_status_string(pmn_status st)
 }
 
 pmn_status pmn_take_quant_device_error(cudaStream_t s, int *bits);  // quantize.cu
+pmn_status pmn_quantize_h_rows(const uint16_t *h, int64_t rows, int cols, int fos, uint8_t *codes,
+                               uint8_t *scales, float *outer, const int32_t *row_end, cudaStream_t s);  // quantize.cu
 
 extern "C" pmn_status pmn_get_device_error(void *stream, int32_t *err)
 {
@@ -1106,9 +1126,29 @@ extern "C" pmn_status pmn_grouped_gemm_nvfp4(const uint8_t *a_codes, const uint8
                                              const int32_t *offsets, int num_experts, int64_t total_rows, int64_t n,
                                              int64_t k, int out_kind, void *out, void *stream)
 {
-    if (out_kind != PMN_OUT_BF16 && out_kind != PMN_OUT_F32) return PMN_ERR_INVALID_ARG;
+    if (out_kind != PMN_OUT_BF16 && out_kind != PMN_OUT_F32 && out_kind != PMN_OUT_SWIGLU_BF16)
+        return PMN_ERR_INVALID_ARG;
     return nvfp4_common(a_codes, a_scales, a_outer, b_codes, b_scales, b_outer, offsets, num_experts, total_rows, n,
                         k, out_kind, out, nullptr, 0, stream);
+}
+
+extern "C" pmn_status pmn_w1_gemm_swiglu_nvfp4(const uint8_t *a_codes, const uint8_t *a_scales,
+                                               const float *a_outer, const uint8_t *b_codes,
+                                               const uint8_t *b_scales, const float *b_outer,
+                                               const int32_t *offsets, int num_experts, int64_t total_rows,
+                                               int64_t f, int64_t k, int four_over_six, void *h,
+                                               uint8_t *codes, uint8_t *scales, float *outer, void *stream)
+{
+    if (four_over_six != 0 && four_over_six != 1) return PMN_ERR_INVALID_ARG;
+    if (f <= 0 || f % 128 != 0 || f > 8192) return PMN_ERR_INVALID_ARG;
+    if (!h || !codes || !scales || !outer || !aligned16(h) || !aligned16(codes) || !aligned16(scales) ||
+        !aligned16(outer))
+        return PMN_ERR_INVALID_ARG;
+    const pmn_status st = nvfp4_common(a_codes, a_scales, a_outer, b_codes, b_scales, b_outer, offsets, num_experts,
+                                       total_rows, 2 * f, k, PMN_OUT_SWIGLU_BF16, h, nullptr, 0, stream);
+    if (st != PMN_OK || total_rows == 0) return st;
+    return pmn_quantize_h_rows(static_cast<const uint16_t *>(h), total_rows, (int)f, four_over_six, codes, scales,
+                               outer, offsets + num_experts, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" pmn_status pmn_w2_gemm_rht_s2f6(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_outer,

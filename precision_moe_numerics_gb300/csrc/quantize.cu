@@ -18,8 +18,11 @@
 
 #include "../../include/pmn.h"
 #include "numerics.cuh"
+#include "sm100.cuh"
 
 using namespace pmn;
+
+uint64_t pmn_wait_limit_ns();  // gemm.cu: the limit of every bounded device wait
 
 namespace {
 
@@ -292,6 +295,22 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
+// Waits until *count >= target (acquire).  Gives up after limit_ns of wall
+// time: latches PMN_DEVERR_WAIT_TIMEOUT and returns false.  Never traps.
+__device__ __forceinline__ bool wait_count(const uint32_t *count, uint32_t target, uint64_t limit_ns)
+{
+    if (ld_acquire_u32(count) >= target) return true;
+    const uint64_t t0 = global_ns();
+    while (ld_acquire_u32(count) < target) {
+        __nanosleep(128);
+        if (global_ns() - t0 > limit_ns) {
+            atomicOr(&g_pmn_quant_error, PMN_DEVERR_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
 // L2 cache policies (createpolicy) and 16-byte loads that carry one.
 __device__ __forceinline__ uint64_t l2_policy_evict_last()
 {
@@ -320,7 +339,7 @@ __device__ __forceinline__ uint4 ld_l2_policy(const uint4 *ptr, uint64_t policy)
 __global__ void __launch_bounds__(QG_THREADS, PMN_QG_MIN_BLOCKS) nvfp4_quant_groups_kernel(
     const uint16_t *__restrict__ x, int64_t groups, int64_t blocks_per_group, int64_t nch, int64_t lead,
     int four_over_six, uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, float *__restrict__ outer,
-    uint32_t *scratch)
+    uint32_t *scratch, uint64_t wait_ns)
 {
     __shared__ uint32_t s_red[QG_THREADS / 32];
     __shared__ uint32_t s_ticket;
@@ -400,18 +419,7 @@ __global__ void __launch_bounds__(QG_THREADS, PMN_QG_MIN_BLOCKS) nvfp4_quant_gro
             };
             load2(b0 + tid);
             if (tid == 0) {
-                int st = 0;
-                if (ld_acquire_u32(done + g) < (uint32_t)nch) {
-                    const uint64_t t0 = global_ns();
-                    while (ld_acquire_u32(done + g) < (uint32_t)nch) {
-                        __nanosleep(128);
-                        if (global_ns() - t0 > 4000000000ull) {
-                            atomicOr(&g_pmn_quant_error, PMN_DEVERR_WAIT_TIMEOUT);
-                            st = 1;
-                            break;
-                        }
-                    }
-                }
+                const int st = wait_count(done + g, (uint32_t)nch, wait_ns) ? 0 : 1;
                 const float gv = outer_from_amax(__uint_as_float(ld_acquire_u32(amax + g)), fos);
                 if (c == 0 && !st) outer[g] = gv;
                 s_g = gv;
@@ -455,19 +463,48 @@ __global__ void __launch_bounds__(QG_THREADS, PMN_QG_MIN_BLOCKS) nvfp4_quant_gro
     }
 }
 
+// A counter that nothing increments (the self-test's second wait).
+static __device__ uint32_t g_never_counted = 0;
+
+// Self-test of the bounded waits: thread 0 waits on an mbarrier that nothing
+// arrives on, then on a counter that nothing increments, with the same wait
+// primitives the GEMMs and the weight quantiser use.  Each wait gives up after
+// limit_ns and latches PMN_DEVERR_WAIT_TIMEOUT; the kernel then returns.
+__global__ void wait_selftest_kernel(uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = sm100::smem_u32(&bar);
+    sm100::mbar_init(b, 1);
+    sm100::fence_barrier_init();
+    if (!sm100::mbar_wait(b, 0, limit_ns)) atomicOr(&g_pmn_quant_error, PMN_DEVERR_WAIT_TIMEOUT);
+    (void)wait_count(&g_never_counted, 1u, limit_ns);
+}
+
 // bf16 rows (no SwiGLU): the row is read twice instead of being held in
 // registers -- once for its amax, then block by block for the codes (the
 // second read hits L1/L2) -- so more warps fit per SM to hide the 4/6 scoring.
+// row_end (optional, device): rows at or past *row_end are not read and are
+// written as the quantisation of a zero row (codes 0, scales 0, outer 1).
 template <int NB>
 __global__ void __launch_bounds__(256, NB <= 8 ? PMN_QR2_MIN_BLOCKS : 1) nvfp4_quant_rows2_kernel(const uint16_t *__restrict__ x, int64_t rows,
                                                                 int cols, int64_t ldx, int four_over_six,
                                                                 uint8_t *__restrict__ codes,
-                                                                uint8_t *__restrict__ scales, float *__restrict__ outer)
+                                                                uint8_t *__restrict__ scales, float *__restrict__ outer,
+                                                                const int32_t *__restrict__ row_end)
 {
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (row >= rows) return;
     const int nblk = cols >> 4;
+    if (row_end != nullptr && row >= (int64_t)__ldg(row_end)) {
+        for (int b = lane; b < nblk; b += 32) {
+            *reinterpret_cast<uint2 *>(codes + row * (cols >> 1) + b * 8) = make_uint2(0u, 0u);
+            scales[row * nblk + b] = 0;
+        }
+        if (lane == 0) outer[row] = 1.0f;
+        return;
+    }
     const uint16_t *xr = x + row * ldx;
     uint32_t m = 0u;
 #pragma unroll
@@ -510,12 +547,28 @@ __global__ void __launch_bounds__(256, NB <= 8 ? PMN_QR2_MIN_BLOCKS : 1) nvfp4_q
 
 template <int NB>
 void launch_rows(bool swiglu, dim3 grid, dim3 block, cudaStream_t s, const uint16_t *x, int64_t rows,
-                 int cols, int64_t ldx, int fos, uint8_t *codes, uint8_t *scales, float *outer, uint16_t *h_out)
+                 int cols, int64_t ldx, int fos, uint8_t *codes, uint8_t *scales, float *outer, uint16_t *h_out,
+                 const int32_t *row_end = nullptr)
 {
     if (swiglu)
         nvfp4_quant_rows_kernel<NB, true><<<grid, block, 0, s>>>(x, rows, cols, ldx, fos, codes, scales, outer, h_out);
     else
-        nvfp4_quant_rows2_kernel<NB><<<grid, block, 0, s>>>(x, rows, cols, ldx, fos, codes, scales, outer);
+        nvfp4_quant_rows2_kernel<NB><<<grid, block, 0, s>>>(x, rows, cols, ldx, fos, codes, scales, outer, row_end);
+}
+
+// Per-row NVFP4 of bf16 rows [rows, cols] (dense), the rows at or past
+// *row_end (device) written as zero rows.
+pmn_status launch_rows_bf16(const uint16_t *x, int64_t rows, int cols, int fos, uint8_t *codes, uint8_t *scales,
+                            float *outer, const int32_t *row_end, cudaStream_t s)
+{
+    const int nb = (cols / 16 + 31) / 32;
+    dim3 block(256), grid((unsigned)((rows + 7) / 8));
+    if (nb <= 1) launch_rows<1>(false, grid, block, s, x, rows, cols, cols, fos, codes, scales, outer, nullptr, row_end);
+    else if (nb <= 2) launch_rows<2>(false, grid, block, s, x, rows, cols, cols, fos, codes, scales, outer, nullptr, row_end);
+    else if (nb <= 4) launch_rows<4>(false, grid, block, s, x, rows, cols, cols, fos, codes, scales, outer, nullptr, row_end);
+    else if (nb <= 8) launch_rows<8>(false, grid, block, s, x, rows, cols, cols, fos, codes, scales, outer, nullptr, row_end);
+    else launch_rows<16>(false, grid, block, s, x, rows, cols, cols, fos, codes, scales, outer, nullptr, row_end);
+    return launch_status();
 }
 
 // ------------------------------------------------------------------ MXFP8 RN (dY)
@@ -1321,21 +1374,36 @@ __global__ void __launch_bounds__(256, 3) combine_receive_kernel(
     }
 }
 
+constexpr int MAX_DEVICES = 64;
+
+// Resident CTAs of the per-group kernel on the current device (SMs x CTAs
+// per SM), computed once per device under a lock.
+pmn_status quant_groups_grid(int *out)
+{
+    static std::mutex mu;
+    static int grid[MAX_DEVICES] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return PMN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (grid[dev] == 0) {
+        int sms = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nvfp4_quant_groups_kernel, QG_THREADS, 0) !=
+                cudaSuccess)
+            return PMN_ERR_CUDA;
+        grid[dev] = std::max(1, sms * per_sm);
+    }
+    *out = grid[dev];
+    return PMN_OK;
+}
+
 // Clears the scratch, then runs the per-group kernel on as many CTAs as fit.
 pmn_status launch_quant_groups(const uint16_t *x, int64_t groups, int64_t blocks_per_group, int four_over_six,
                                uint8_t *codes, uint8_t *scales, float *outer, uint32_t *scratch, cudaStream_t s)
 {
+    int grid = 0;
+    if (quant_groups_grid(&grid) != PMN_OK) return PMN_ERR_CUDA;
     if (cudaMemsetAsync(scratch, 0, quant_groups_scratch_bytes(groups), s) != cudaSuccess) return PMN_ERR_CUDA;
-    static int grid = 0;
-    if (grid == 0) {
-        int dev = 0, sms = 0, per_sm = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nvfp4_quant_groups_kernel, QG_THREADS, 0) !=
-                cudaSuccess)
-            return PMN_ERR_CUDA;
-        grid = std::max(1, sms * per_sm);
-    }
     const int64_t nch = (blocks_per_group + QG_CHUNK - 1) / QG_CHUNK;
     // one group plus three quarters of an item per CTA: measured best with
     // the L2 priorities above (a longer lead pushes re-reads out of L2, a
@@ -1345,11 +1413,20 @@ pmn_status launch_quant_groups(const uint16_t *x, int64_t groups, int64_t blocks
 #endif
     const int64_t lead = std::min(groups * nch, nch + (int64_t)grid * PMN_QG_LEAD_Q / 4);
     nvfp4_quant_groups_kernel<<<(unsigned)grid, QG_THREADS, 0, s>>>(x, groups, blocks_per_group, nch, lead,
-                                                                     four_over_six, codes, scales, outer, scratch);
+                                                                     four_over_six, codes, scales, outer, scratch,
+                                                                     pmn_wait_limit_ns());
     return launch_status();
 }
 
 }  // namespace
+
+// The h coding step of pmn_w1_gemm_swiglu_nvfp4 (gemm.cu): per-row NVFP4 of
+// the GEMM's bf16 h, rows past the expert segments written as zero rows.
+pmn_status pmn_quantize_h_rows(const uint16_t *h, int64_t rows, int cols, int fos, uint8_t *codes, uint8_t *scales,
+                               float *outer, const int32_t *row_end, cudaStream_t s)
+{
+    return launch_rows_bf16(h, rows, cols, fos, codes, scales, outer, row_end, s);
+}
 
 // Reads and clears the quantisation kernels' device error bits (called by
 // pmn_get_device_error, which owns the stream synchronisation).
@@ -1373,11 +1450,10 @@ pmn_status pmn_take_quant_device_error(cudaStream_t s, int *bits)
 // Device address of the fixed scratch, looked up once per device.
 pmn_status noalloc_scratch(uint32_t **out)
 {
-    constexpr int MAX_DEV = 64;
     static std::mutex mu;
-    static void *addr[MAX_DEV] = {};
+    static void *addr[MAX_DEVICES] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return PMN_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return PMN_ERR_CUDA;
     std::lock_guard<std::mutex> lock(mu);
     if (!addr[dev]) {
         void *p = nullptr;
@@ -1389,6 +1465,13 @@ pmn_status noalloc_scratch(uint32_t **out)
 }
 
 // ====================================================================== C ABI
+extern "C" pmn_status pmn_wait_selftest(uint64_t limit_ns, void *stream)
+{
+    if (limit_ns > 2000000000ull) return PMN_ERR_INVALID_ARG;
+    wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns);
+    return launch_status();
+}
+
 extern "C" pmn_status pmn_nvfp4_quantize_per_group_noalloc(const void *x, int64_t rows, int64_t cols,
                                                             int64_t rows_per_group, int four_over_six,
                                                             uint8_t *codes, uint8_t *scales, float *outer,
@@ -1408,10 +1491,17 @@ extern "C" pmn_status pmn_nvfp4_quantize_per_group_noalloc(const void *x, int64_
                                reinterpret_cast<cudaStream_t>(stream));
 }
 
+extern "C" int64_t pmn_nvfp4_quantize_workspace_bytes(int outer_mode, int64_t rows, int64_t rows_per_group)
+{
+    if (outer_mode != PMN_OUTER_PER_GROUP) return outer_mode == PMN_OUTER_PER_ROW ? 0 : -1;
+    if (rows < 0 || rows_per_group <= 0 || rows % rows_per_group != 0) return -1;
+    return (int64_t)quant_groups_scratch_bytes(rows / rows_per_group);
+}
+
 extern "C" pmn_status pmn_nvfp4_quantize(const void *x, int64_t rows, int64_t cols, int64_t ldx, int in_mode,
                                          int outer_mode, int64_t rows_per_group, int four_over_six,
                                          uint8_t *codes, uint8_t *scales, float *outer, void *h_out,
-                                         void *stream)
+                                         void *workspace, int64_t workspace_bytes, void *stream)
 {
     if (rows < 0 || cols <= 0 || cols % 16 != 0 || cols > 8192) return PMN_ERR_INVALID_ARG;
     if (in_mode != PMN_IN_BF16 && in_mode != PMN_IN_BF16_SWIGLU) return PMN_ERR_INVALID_ARG;
@@ -1424,20 +1514,16 @@ extern "C" pmn_status pmn_nvfp4_quantize(const void *x, int64_t rows, int64_t co
     if (h_out && (!swiglu || !aligned16(h_out))) return PMN_ERR_INVALID_ARG;
     if (outer_mode == PMN_OUTER_PER_GROUP) {
         if (swiglu || rows_per_group <= 0 || rows % rows_per_group != 0 || ldx != cols) return PMN_ERR_INVALID_ARG;
+        if (!workspace || !aligned16(workspace) ||
+            workspace_bytes < (int64_t)quant_groups_scratch_bytes(rows / rows_per_group))
+            return PMN_ERR_INVALID_ARG;
     }
     if (rows == 0) return PMN_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint16_t *xb = reinterpret_cast<const uint16_t *>(x);
-    if (outer_mode == PMN_OUTER_PER_GROUP) {
-        const int64_t groups = rows / rows_per_group;
-        const size_t ws_bytes = quant_groups_scratch_bytes(groups);
-        void *ws = nullptr;
-        if (cudaMallocAsync(&ws, ws_bytes, s) != cudaSuccess) return PMN_ERR_CUDA;
-        pmn_status st = launch_quant_groups(xb, groups, rows_per_group * (cols / 16), four_over_six, codes, scales,
-                                            outer, static_cast<uint32_t *>(ws), s);
-        if (cudaFreeAsync(ws, s) != cudaSuccess) st = PMN_ERR_CUDA;
-        return st;
-    }
+    if (outer_mode == PMN_OUTER_PER_GROUP)
+        return launch_quant_groups(xb, rows / rows_per_group, rows_per_group * (cols / 16), four_over_six, codes,
+                                   scales, outer, static_cast<uint32_t *>(workspace), s);
     const int nb = (int)((cols / 16 + 31) / 32);
     dim3 block(256), grid((unsigned)((rows + 7) / 8));
     uint16_t *ho = reinterpret_cast<uint16_t *>(h_out);

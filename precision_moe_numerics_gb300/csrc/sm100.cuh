@@ -53,7 +53,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit_ns` of wall time and returns false (the caller latches an error and
 // winds down); it never traps and never spins forever.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 4000000000ull)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
@@ -82,32 +82,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
         "[%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y)
         : "memory");
-}
-
-// TMA tile load multicast to every CTA of the cluster in `mask`: the box
-// lands at the same shared-memory offset in each, and each destination's
-// mbarrier at the same offset receives the transaction bytes.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *tmap, uint32_t bar, int32_t x, int32_t y,
-                                               uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
-        "[%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// All threads of all CTAs of the cluster (release / acquire).
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // Shared -> global tile store (bulk-group completion).
@@ -172,16 +146,6 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void tc_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// As tc_commit, arriving on the barrier at the same offset in every CTA of
-// the cluster in `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                     bar),
-                 "h"(mask)
                  : "memory");
 }
 

@@ -4,8 +4,9 @@ Forward (page "Thinking Machines ... Inkling 2 Small", sections [Layers],
 [Cost], [NVLink]):
   W1, W2 (bf16 master weights)  -> NVFP4, outer scale per expert
   X (routed rows, bf16)         -> NVFP4, outer scale per token, 4/6
-  Y  = X . W1^T                 grouped NVFP4 GEMM -> bf16
-  H  = silu(Y_gate) * Y_up      -> NVFP4, per token, 4/6 (one kernel)
+  H  = silu(Y_gate) * Y_up,     grouped NVFP4 GEMM with SwiGLU in its
+       Y = X . W1^T             epilogue (bf16 h), then NVFP4 of h per token,
+                                4/6 (one call, two kernels)
   Z  = H . W2^T                 grouped NVFP4 GEMM with the RHT-32 + S2F6
                                 combine quantisation in its epilogue
 Backward (section [SR]):
@@ -61,11 +62,14 @@ class ExpertLayerStep:
         def e(*shape, dtype=u8):
             return torch.empty(shape, dtype=dtype, device=device)
 
+        # scratch of the per-expert weight quantiser (caller-owned workspace)
+        self.ws = e(max(pmn.nvfp4_quantize_workspace_bytes(pmn.OUTER_PER_GROUP, E * F2, F2),
+                        pmn.nvfp4_quantize_workspace_bytes(pmn.OUTER_PER_GROUP, E * D, D)))
         # forward operands
         self.w1q = (e(E * F2, D // 2), e(E * F2, D // 16), e(E, dtype=f32))
         self.w2q = (e(E * D, F // 2), e(E * D, F // 16), e(E, dtype=f32))
         self.xq = (e(T, D // 2), e(T, D // 16), e(T, dtype=f32))
-        self.y = e(T, F2, dtype=bf16)
+        self.h = e(T, F, dtype=bf16)
         self.hq = (e(T, F // 2), e(T, F // 16), e(T, dtype=f32))
         self.z = (e(T, D, dtype=torch.int8), e(T, D // 32))
         # backward operands
@@ -100,13 +104,12 @@ class ExpertLayerStep:
         P = pmn
         return [
             ("quant_w1", lambda: P.nvfp4_quantize(self.w1.view(E * F2, D), outer_mode=P.OUTER_PER_GROUP,
-                                                  rows_per_group=F2, out=self.w1q)),
+                                                  rows_per_group=F2, out=self.w1q, workspace=self.ws)),
             ("quant_w2", lambda: P.nvfp4_quantize(self.w2.view(E * D, F), outer_mode=P.OUTER_PER_GROUP,
-                                                  rows_per_group=D, out=self.w2q)),
+                                                  rows_per_group=D, out=self.w2q, workspace=self.ws)),
             ("quant_x", lambda: P.nvfp4_quantize(self.x, four_over_six=True, out=self.xq)),
-            ("gemm1_nvfp4", lambda: P.grouped_gemm_nvfp4(self.xq, self.w1q3(), self.offsets, out=self.y)),
-            ("swiglu_quant_h", lambda: P.nvfp4_quantize(self.y, cols=F, swiglu=True, four_over_six=True,
-                                                        out=self.hq)),
+            ("gemm1_swiglu_nvfp4", lambda: P.w1_gemm_swiglu_nvfp4(self.xq, self.w1q3(), self.offsets, True,
+                                                                  out=self.hq, h=self.h)),
             ("gemm2_nvfp4_rht_s2f6", lambda: P.w2_gemm_rht_s2f6(self.hq, self.w2q3(), self.offsets, self.seed,
                                                                 out=self.z)),
             ("requant_x", lambda: P.requant_transpose_sr_mxfp8(*self.xq, True, 1, T, D, self.seed, P.TAG_X,
@@ -153,7 +156,7 @@ class DecodeForward:
             return torch.empty(shape, dtype=dtype, device=device)
 
         self.xq = (e(T, D // 2), e(T, D // 16), e(T, dtype=f32))
-        self.y = e(T, F2, dtype=torch.bfloat16)
+        self.h = e(T, F, dtype=torch.bfloat16)
         self.hq = (e(T, F // 2), e(T, F // 16), e(T, dtype=f32))
         self.z = (e(T, D, dtype=torch.int8), e(T, D // 32))
         self.F = F
@@ -162,9 +165,8 @@ class DecodeForward:
         P = pmn
         return [
             ("quant_x", lambda: P.nvfp4_quantize(self.x, four_over_six=True, out=self.xq)),
-            ("gemm1_nvfp4", lambda: P.grouped_gemm_nvfp4(self.xq, self.w1q3, self.offsets, out=self.y)),
-            ("swiglu_quant_h", lambda: P.nvfp4_quantize(self.y, cols=self.F, swiglu=True, four_over_six=True,
-                                                        out=self.hq)),
+            ("gemm1_swiglu_nvfp4", lambda: P.w1_gemm_swiglu_nvfp4(self.xq, self.w1q3, self.offsets, True,
+                                                                  out=self.hq, h=self.h)),
             ("gemm2_nvfp4_rht_s2f6", lambda: P.w2_gemm_rht_s2f6(self.hq, self.w2q3, self.offsets, self.seed,
                                                                 out=self.z)),
         ]
@@ -242,16 +244,17 @@ def decode_algorithmic(counts, d_model, d_ff):
     hit = int((counts > 0).sum())
     F2 = 2 * d_ff
     wbytes = hit * ((F2 * d_model + d_model * d_ff) * nv + 8)
-    act = R * d_model * (2 + nv) + R * F2 * 2 * 2 + R * d_ff * nv * 2 + R * d_model * (1 + 1 / 32)
+    # X in and its NVFP4 out; h (bf16) written and read; h NVFP4 written and read; the payload written
+    act = R * d_model * (2 + nv) + R * d_ff * 2 * 2 + R * d_ff * nv * 2 + R * d_model * (1 + 1 / 32)
     flops = 2.0 * R * F2 * d_model + 2.0 * R * d_model * d_ff
     return flops, wbytes + act, wbytes
 
 
-# launches of library kernels per call name (for the launch count); every
-# call of the step launches one kernel (the scratch clear of the per-group
-# weight quantiser is a memset, not a kernel of the library)
-LAUNCHES = {}
-STEP_CALLS = ["quant_w1", "quant_w2", "quant_x", "gemm1_nvfp4", "swiglu_quant_h", "gemm2_nvfp4_rht_s2f6",
+# launches of library kernels per call name (for the launch count); a call
+# not listed launches one kernel (the scratch clear of the per-group weight
+# quantiser is a memset, not a kernel of the library)
+LAUNCHES = {"gemm1_swiglu_nvfp4": 2}  # the GEMM with the SwiGLU epilogue, then the NVFP4 coding of h
+STEP_CALLS = ["quant_w1", "quant_w2", "quant_x", "gemm1_swiglu_nvfp4", "gemm2_nvfp4_rht_s2f6",
               "requant_x", "requant_h", "requant_w1", "requant_w2", "quant_dy_rows", "quant_dy_cols",
               "quant_dy1_rows", "quant_dy1_cols", "gemm_dh_mxfp8", "gemm_dw2_mxfp8", "gemm_dx_mxfp8",
               "gemm_dw1_mxfp8"]
@@ -272,8 +275,8 @@ def algorithmic(shape: LayerShape):
         "quant_w1": (0, w1n * (2 + nv)),
         "quant_w2": (0, w2n * (2 + nv)),
         "quant_x": (0, R * D * (2 + nv)),
-        "gemm1_nvfp4": (2.0 * R * F2 * D, (R * D + w1n) * nv + R * F2 * 2),
-        "swiglu_quant_h": (0, R * F2 * 2 + R * F * nv),
+        # X and W1 (NVFP4) read; bf16 h written by the GEMM and read by the coding kernel; NVFP4 h written
+        "gemm1_swiglu_nvfp4": (2.0 * R * F2 * D, (R * D + w1n) * nv + R * F * 2 * 2 + R * F * nv),
         "gemm2_nvfp4_rht_s2f6": (2.0 * R * D * F, (R * F + w2n) * nv + R * D * mx),
         "requant_x": (0, R * D * (nv + mx)),
         "requant_h": (0, R * F * (nv + mx)),

@@ -19,7 +19,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 IN_BF16, IN_BF16_SWIGLU = 0, 1
 OUTER_PER_ROW, OUTER_PER_GROUP = 0, 1
 ROUND_SR, ROUND_RN = 0, 1
-OUT_BF16, OUT_F32, OUT_RHT_S2F6 = 0, 1, 2
+OUT_BF16, OUT_F32, OUT_RHT_S2F6, OUT_SWIGLU_BF16 = 0, 1, 2, 3
 GROUP_M, GROUP_K = 0, 1
 DEVERR_WAIT_TIMEOUT = 1
 DEVERR_BAD_OFFSETS = 2
@@ -33,13 +33,17 @@ SIGNATURES = {
     "pmn_version": ([], _I),
     "pmn_status_string": ([_I], ctypes.c_char_p),
     "pmn_get_device_error": ([_P, _P], _I),
-    "pmn_nvfp4_quantize": ([_P, _I64, _I64, _I64, _I, _I, _I64, _I, _P, _P, _P, _P, _P], _I),
+    "pmn_set_wait_limit_ns": ([_U64], _U64),
+    "pmn_wait_selftest": ([_U64, _P], _I),
+    "pmn_nvfp4_quantize": ([_P, _I64, _I64, _I64, _I, _I, _I64, _I, _P, _P, _P, _P, _P, _I64, _P], _I),
+    "pmn_nvfp4_quantize_workspace_bytes": ([_I, _I64, _I64], _I64),
     "pmn_nvfp4_quantize_per_group_noalloc": ([_P, _I64, _I64, _I64, _I, _P, _P, _P, _P], _I),
     "pmn_requant_transpose_sr_mxfp8": ([_P, _P, _P, _I, _I64, _I64, _I64, _U64, _U32, _I, _P, _P, _P], _I),
     "pmn_requant_transpose_sr_nvfp4": ([_P, _P, _P, _I, _I64, _I64, _I64, _U64, _U32, _I, _P, _P, _P, _P], _I),
     "pmn_mxfp8_quantize": ([_P, _I64, _I64, _I, _P, _P, _P], _I),
     "pmn_mxfp8_quantize_swiglu": ([_P, _I64, _I64, _P, _P, _P, _P], _I),
     "pmn_grouped_gemm_nvfp4": ([_P, _P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P], _I),
+    "pmn_w1_gemm_swiglu_nvfp4": ([_P, _P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _I, _P, _P, _P, _P, _P], _I),
     "pmn_w2_gemm_rht_s2f6": ([_P, _P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _U64, _P, _P, _P, _P], _I),
     "pmn_rht_s2f6_quantize": ([_P, _I64, _I64, _U64, _P, _P, _P], _I),
     "pmn_combine_receive_s2f6": ([_P, _P, _I64, _I64, _U64, _P, _P, _I64, _I, _I, _P, _P], _I),
@@ -103,12 +107,30 @@ def get_device_error(stream=None):
     return err.value
 
 
+def set_wait_limit_ns(ns):
+    """Sets the limit of the library's bounded device waits; returns the previous one."""
+    return lib().pmn_set_wait_limit_ns(int(ns))
+
+
+def wait_selftest(limit_ns, stream=None):
+    _check(lib().pmn_wait_selftest(int(limit_ns), _stream(stream)), "wait_selftest")
+
+
+def nvfp4_quantize_workspace_bytes(outer_mode, rows, rows_per_group=0):
+    n = lib().pmn_nvfp4_quantize_workspace_bytes(outer_mode, rows, rows_per_group)
+    if n < 0:
+        raise PmnError("nvfp4_quantize_workspace_bytes: invalid arguments")
+    return n
+
+
 # ------------------------------------------------------------------ quantisation
 def nvfp4_quantize(x, cols=None, four_over_six=False, outer_mode=OUTER_PER_ROW, rows_per_group=None,
-                   swiglu=False, want_h=False, out=None, stream=None):
+                   swiglu=False, want_h=False, out=None, workspace=None, stream=None):
     """bf16 [rows, ldx] -> (codes u8 [rows, cols/2], scales u8 [rows, cols/16], outer f32[, h bf16]).
 
-    swiglu: x holds gate | up halves of width `cols`; h = silu(gate) * up is quantised."""
+    swiglu: x holds gate | up halves of width `cols`; h = silu(gate) * up is quantised.
+    workspace: the per-group kernel's scratch (uint8 device tensor of at least
+    nvfp4_quantize_workspace_bytes(...) bytes); allocated here when None."""
     _dev(x, torch.bfloat16)
     rows, ldx = x.shape
     if cols is None:
@@ -122,9 +144,13 @@ def nvfp4_quantize(x, cols=None, four_over_six=False, outer_mode=OUTER_PER_ROW, 
     else:
         codes, scales, outer = out
     h = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev) if want_h else None
+    if workspace is None and outer_mode == OUTER_PER_GROUP:
+        workspace = torch.empty((max(1, nvfp4_quantize_workspace_bytes(outer_mode, rows, rows_per_group or 0)),),
+                                dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().pmn_nvfp4_quantize(_ptr(x), rows, cols, ldx, IN_BF16_SWIGLU if swiglu else IN_BF16, outer_mode,
                                   rows_per_group or 0, int(four_over_six), _ptr(codes), _ptr(scales), _ptr(outer),
-                                  _ptr(h), _stream(stream))
+                                  _ptr(h), _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "nvfp4_quantize")
     return (codes, scales, outer, h) if want_h else (codes, scales, outer)
 
@@ -256,21 +282,53 @@ def combine_receive_s2f6(payload, seed, row_index, gates, out_dtype=torch.bfloat
 
 
 # ------------------------------------------------------------------ GEMMs
-def grouped_gemm_nvfp4(a, b, offsets, out_dtype=torch.bfloat16, out=None, stream=None):
+def grouped_gemm_nvfp4(a, b, offsets, out_dtype=torch.bfloat16, swiglu=False, out=None, stream=None):
     """a = (codes [T, K/2], scales [T, K/16], outer [T]); b = (codes [E, N, K/2],
-    scales [E, N, K/16], outer [E]); offsets int32 [E+1] on the device."""
+    scales [E, N, K/16], outer [E]); offsets int32 [E+1] on the device.
+    swiglu: the bf16 h = silu(gate) * up [T, N/2] of the float32 product
+    (gate = the first N/2 rows of each B_e, up = the last N/2)."""
     ac, asc, ao = a
     bc, bsc, bo = b
     _dev(offsets, torch.int32)
     T = ac.shape[0]
     E, N = bc.shape[0], bc.shape[1]
     K = ac.shape[1] * 2
-    kind = OUT_BF16 if out_dtype == torch.bfloat16 else OUT_F32
+    kind = OUT_SWIGLU_BF16 if swiglu else (OUT_BF16 if out_dtype == torch.bfloat16 else OUT_F32)
     if out is None:
-        out = torch.empty((T, N), dtype=out_dtype, device=ac.device)
+        out = torch.empty((T, N // 2 if swiglu else N), dtype=torch.bfloat16 if swiglu else out_dtype,
+                          device=ac.device)
     st = lib().pmn_grouped_gemm_nvfp4(_ptr(ac), _ptr(asc), _ptr(ao), _ptr(bc), _ptr(bsc), _ptr(bo), _ptr(offsets),
                                       E, T, N, K, kind, _ptr(out), _stream(stream))
     _check(st, "grouped_gemm_nvfp4")
+    return out
+
+
+def w1_gemm_swiglu_nvfp4(a, b, offsets, four_over_six=True, out=None, h=None, stream=None):
+    """w1 GEMM with SwiGLU in its epilogue, then NVFP4 (per token, 4/6) of h.
+    a = NVFP4 rows (codes [T, K/2], scales [T, K/16], outer [T]); b = NVFP4 W1
+    (codes [E, 2F, K/2], scales [E, 2F, K/16], outer [E]) with gate rows first.
+    Returns (codes u8 [T, F/2], scales u8 [T, F/16], outer f32 [T]); `h` (bf16
+    [T, F], allocated here when None) receives h itself."""
+    ac, asc, ao = a
+    bc, bsc, bo = b
+    _dev(offsets, torch.int32)
+    T = ac.shape[0]
+    E, F2 = bc.shape[0], bc.shape[1]
+    F = F2 // 2
+    K = ac.shape[1] * 2
+    dev = ac.device
+    if out is None:
+        out = (torch.empty((T, F // 2), dtype=torch.uint8, device=dev),
+               torch.empty((T, F // 16), dtype=torch.uint8, device=dev),
+               torch.empty((T,), dtype=torch.float32, device=dev))
+    if h is None:
+        h = torch.empty((T, F), dtype=torch.bfloat16, device=dev)
+    _dev(h, torch.bfloat16)
+    c, sc, g = out
+    st = lib().pmn_w1_gemm_swiglu_nvfp4(_ptr(ac), _ptr(asc), _ptr(ao), _ptr(bc), _ptr(bsc), _ptr(bo), _ptr(offsets),
+                                        E, T, F, K, int(four_over_six), _ptr(h), _ptr(c), _ptr(sc), _ptr(g),
+                                        _stream(stream))
+    _check(st, "w1_gemm_swiglu_nvfp4")
     return out
 
 

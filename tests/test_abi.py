@@ -50,7 +50,8 @@ def test_host_argument_checks_need_no_gpu(libpath):
     from precision_moe_numerics_gb300 import pmn
     L = pmn.lib()
     null = None
-    assert L.pmn_nvfp4_quantize(null, 4, 24, 24, 0, 0, 0, 0, null, null, null, null, null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_nvfp4_quantize(null, 4, 24, 24, 0, 0, 0, 0, null, null, null, null, null, 0,
+                                null) == pmn.ERR_INVALID_ARG
     assert L.pmn_mxfp8_quantize(null, 40, 64, 1, null, null, null) == pmn.ERR_INVALID_ARG
     assert L.pmn_requant_transpose_sr_mxfp8(null, null, null, 0, 1, 32, 32, 0, 1, 0, null, null,
                                             null) == pmn.ERR_INVALID_ARG
@@ -88,6 +89,24 @@ def test_host_argument_checks_need_no_gpu(libpath):
                                             null) == pmn.ERR_INVALID_ARG
     assert L.pmn_requant_transpose_sr_nvfp4(null, null, null, 0, 0, 64, 64, 0, 1, 0, null, null, null,
                                             null) == pmn.OK          # no entry: nothing to do
+    # per-group quantisation: a missing, short or misaligned workspace is rejected on the host
+    need = L.pmn_nvfp4_quantize_workspace_bytes(pmn.OUTER_PER_GROUP, 4 * 256, 256)
+    assert need == (64 + 2 * 4) * 4
+    args = (fake, 4 * 256, 64, 64, pmn.IN_BF16, pmn.OUTER_PER_GROUP, 256, 0, fake, fake, fake, null)
+    assert L.pmn_nvfp4_quantize(*args, null, need, null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_nvfp4_quantize(*args, fake, need - 4, null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_nvfp4_quantize(*args, fake + 8, need, null) == pmn.ERR_INVALID_ARG
+    # no rows: nothing to do (the workspace is checked first, and it is valid here)
+    assert L.pmn_nvfp4_quantize(fake, 0, 64, 64, pmn.IN_BF16, pmn.OUTER_PER_GROUP, 256, 0, fake, fake, fake, null,
+                                fake, need, null) == pmn.OK
+    assert L.pmn_nvfp4_quantize_workspace_bytes(pmn.OUTER_PER_ROW, 4, 0) == 0
+    assert L.pmn_nvfp4_quantize_workspace_bytes(pmn.OUTER_PER_GROUP, 100, 16) == -1  # rows % rows_per_group
+    assert L.pmn_nvfp4_quantize_workspace_bytes(7, 4, 1) == -1
+    # bounded-wait self-test: limits above 2 s are refused before anything is enqueued
+    assert L.pmn_wait_selftest(2000000001, null) == pmn.ERR_INVALID_ARG
+    # the wait limit is process-wide and returns the previous value
+    prev = L.pmn_set_wait_limit_ns(123)
+    assert L.pmn_set_wait_limit_ns(prev) == 123
     # more groups than the fixed scratch holds: rejected before any pointer is used
     assert L.pmn_nvfp4_quantize_per_group_noalloc(fake, 1025 * 16, 64, 16, 0, fake, fake, fake,
                                                   null) == pmn.ERR_INVALID_ARG

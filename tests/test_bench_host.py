@@ -56,7 +56,7 @@ def test_traffic_table_parses_and_hashes_sources():
     assert nbytes > 1e10 and len(sha) == 12
     # the hash covers the kernel's sources: GEMM and quantiser calls hash different files
     assert b.source_sha("gemm_dw1_mxfp8") != b.source_sha("quant_w1")
-    assert b.source_sha("gemm_dw1_mxfp8") == b.source_sha("gemm1_nvfp4")
+    assert b.source_sha("gemm_dw1_mxfp8") == b.source_sha("gemm1_swiglu_nvfp4")
 
 
 def test_decode_accounting():

@@ -6,10 +6,15 @@ The oracle recomputes sampled outputs one by one from host copies of the same
 seeded inputs: sampled routed rows and sampled experts.  Bytes (codes,
 scales, outer scales, MXFP8 values) must match exactly; GEMM outputs within
 the stated tolerances (fp32: relative Frobenius 1e-5 and |err| <= 1e-3 (|A||B|);
-bf16: additionally one bf16 step).  Outputs whose inputs are themselves GEMM
-results (h, the combine payload, dW2) are checked by properties against the
-oracle's own binary64 pipeline, since the oracle never takes inputs from the
-CUDA path.
+bf16: additionally one bf16 step); h within the bound of test_gpu_swiglu_gemm.
+The oracle never takes an input from the CUDA path.  Where a step's input is
+itself a GEMM result (the w2 GEMM's h, the dW2 GEMM's H^T), the step is run a
+second time, in the same launch configuration, with the sampled expert's
+operand replaced by the oracle's own bytes, and checked element by element;
+the step's own outputs are checked against the library's pinned standalone
+kernels on every row (the combine payload against the standalone RHT + S2F6
+kernel on the fused epilogue's input, the coding of h against the plain
+row quantiser on the kernel's h).
 """
 import numpy as np
 import pytest
@@ -156,19 +161,32 @@ def test_fullsize_gradient_quantisation(run):
     same(hu(L.dy_t[1][:, lo // 32:hi // 32]), qts, "dY^T scales")
 
 
-def test_fullsize_forward_w1_gemm(run):
+def oracle_h(run, x_bits, e):
+    """the oracle's chain for rows of expert e: NVFP4 of X (4/6), the binary64 w1
+    product, |A||B|, h (bf16 from binary64) and its NVFP4 (4/6)"""
+    xc, xs, xg = oracle.nvfp4_quantize(x_bits, oracle.OUTER_PER_ROW, four_over_six=True)
+    wc, ws, wg = oracle_w(run, "w1", e)
+    y = oracle.gemm_nvfp4(xc, xs, xg, wc, ws, wg[0])
+    A = np.abs(oracle.nvfp4_dequant_f64(xc, xs)) * np.abs(xg[:, None].astype(np.float64))
+    B = np.abs(oracle.nvfp4_dequant_f64(wc, ws)) * abs(float(wg[0]))
+    F = wc.shape[0] // 2
+    h = oracle.swiglu_bf16_from_f64(y, F)
+    return y, A @ B.T, h, oracle.nvfp4_quantize(h, oracle.OUTER_PER_ROW, four_over_six=True)
+
+
+def test_fullsize_forward_w1_gemm_swiglu(run):
+    """h rows of a sampled expert against the oracle's chain; the NVFP4 of h on
+    every row against the plain per-row quantiser on the layer's own h."""
+    from swiglu_checks import check_h, check_h_coding
+    from precision_moe_numerics_gb300 import pmn
     L, r = run["L"], run["r"]
     E, F2, D = L.w1.shape
     e = run["experts"][2]
     lo, hi = seg(r, e)
-    rows = np.arange(lo, min(hi, lo + 64))
-    x = hb(L.x[lo:lo + len(rows)])
-    xc, xs, xg = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW, four_over_six=True)
-    wc, ws, wg = oracle_w(run, "w1", e)
-    ref = oracle.gemm_nvfp4(xc, xs, xg, wc, ws, wg[0])
-    A = np.abs(oracle.nvfp4_dequant_f64(xc, xs)) * np.abs(xg[:, None].astype(np.float64))
-    B = np.abs(oracle.nvfp4_dequant_f64(wc, ws)) * abs(float(wg[0]))
-    check_bf16(hb(L.y[lo:lo + len(rows)]), ref, A @ B.T, "Y rows of expert %d" % e)
+    n = min(hi - lo, 64)
+    y, absab, _, _ = oracle_h(run, hb(L.x[lo:lo + n]), e)
+    check_h(hb(L.h[lo:lo + n]), y, absab, F2 // 2, "h rows of expert %d" % e)
+    check_h_coding(pmn, L.h, *L.hq, int(r.offsets[-1]), "full-size h")
 
 
 def test_fullsize_backward_dx_gemm(run):
@@ -200,34 +218,73 @@ def test_fullsize_backward_dw1_gemm(run):
     check_f32(hu(L.dw1[e]), ref, np.abs(A) @ np.abs(B).T, "dW1 of expert %d" % e)
 
 
-def test_fullsize_combine_and_dw2_properties(run):
-    """h, the combine payload and dW2 take GPU GEMM results as inputs, so they
-    are compared with the oracle's own binary64 pipeline by loose properties:
-    decoded combine output and dW2 within 2 % relative Frobenius error."""
+def test_fullsize_combine_payload(run):
+    """The w2 GEMM + RHT + S2F6 at full size.  (a) The step's payload on every
+    row equals the standalone RHT + S2F6 kernel's bytes on the fused
+    epilogue's input (read back through debug_acc).  (b) With the sampled
+    expert's rows of h replaced by the oracle's NVFP4 of the oracle's own h,
+    the epilogue's input on those rows is within the float32 GEMM tolerance
+    of the binary64 product, and its bytes again equal the standalone
+    kernel's."""
+    from precision_moe_numerics_gb300 import pmn
+    L, r = run["L"], run["r"]
+    E, F2, D = L.w1.shape
+    e = run["experts"][2]
+    lo, hi = seg(r, e)
+    rows = L.shape.rows
+    acc = torch.empty((rows, D), dtype=torch.float32, device="cuda")
+    q, sc = pmn.w2_gemm_rht_s2f6(L.hq, L.w2q3(), L.offsets, SEED, debug_acc=acc)
+    end = int(r.offsets[-1])
+    assert torch.equal(q[:end], L.z[0][:end]) and torch.equal(sc[:end], L.z[1][:end])
+    sq, ssc = pmn.rht_s2f6_quantize(acc[:end], SEED)
+    assert torch.equal(sq, q[:end]), "payload codes differ from the standalone kernel's"
+    assert torch.equal(ssc, sc[:end]), "payload scales differ from the standalone kernel's"
+    # (b) the oracle's h for expert e
+    _, _, _, (hc, hs, hg) = oracle_h(run, hb(L.x[lo:hi]), e)
+    hq = tuple(t.clone() for t in L.hq)
+    hq[0][lo:hi] = torch.from_numpy(hc).cuda()
+    hq[1][lo:hi] = torch.from_numpy(hs).cuda()
+    hq[2][lo:hi] = torch.from_numpy(hg).cuda()
+    q, sc = pmn.w2_gemm_rht_s2f6(hq, L.w2q3(), L.offsets, SEED, debug_acc=acc)
+    w2c, w2s, w2g = oracle_w(run, "w2", e)
+    z = oracle.gemm_nvfp4(hc, hs, hg, w2c, w2s, w2g[0])
+    A = np.abs(oracle.nvfp4_dequant_f64(hc, hs)) * np.abs(hg[:, None].astype(np.float64))
+    B = np.abs(oracle.nvfp4_dequant_f64(w2c, w2s)) * abs(float(w2g[0]))
+    check_f32(hu(acc[lo:hi]), z, A @ B.T, "w2 accumulator of expert %d" % e)
+    sq, ssc = pmn.rht_s2f6_quantize(acc[lo:hi], SEED)
+    assert torch.equal(sq, q[lo:hi]) and torch.equal(ssc, sc[lo:hi])
+    del acc
+
+
+def test_fullsize_backward_dw2_gemm(run):
+    """dW2 of a sampled expert: the K-grouped GEMM over all 384 experts, run
+    with the expert's columns of H^T replaced by the oracle's SR requantisation
+    of the oracle's NVFP4 of its own h, against dY^T . H^T of the oracle's
+    operands in binary64, element by element."""
+    from precision_moe_numerics_gb300 import pmn
     L, r = run["L"], run["r"]
     E, F2, D = L.w1.shape
     F = F2 // 2
     e = run["experts"][2]
     lo, hi = seg(r, e)
-    n = hi - lo
-    xc, xs, xg = oracle.nvfp4_quantize(hb(L.x[lo:hi]), oracle.OUTER_PER_ROW, four_over_six=True)
-    w1c, w1s, w1g = oracle_w(run, "w1", e)
-    y = oracle.bf16_rne_array(oracle.gemm_nvfp4(xc, xs, xg, w1c, w1s, w1g[0]))
-    h = oracle.swiglu_bf16(y, F)
-    hc, hs, hg = oracle.nvfp4_quantize(h, oracle.OUTER_PER_ROW, four_over_six=True)
-    w2c, w2s, w2g = oracle_w(run, "w2", e)
-    z = oracle.gemm_nvfp4(hc, hs, hg, w2c, w2s, w2g[0])
-    zq = oracle.s2f6_dequant_inverse_rht(hu(L.z[0][lo:hi]), hu(L.z[1][lo:hi]), SEED)
-    real = int(r.counts[e])
-    rel = np.linalg.norm(zq[:real] - z[:real]) / np.linalg.norm(z[:real])
-    assert rel < 0.02, rel
-    ht, hts = oracle.requant_transpose_mxfp8(hc, hs, hg, True, 1, n, F, SEED, oracle.TAG_H,
+    _, _, _, (hc, hs, hg) = oracle_h(run, hb(L.x[lo:hi]), e)
+    ht, hts = oracle.requant_transpose_mxfp8(hc, hs, hg, True, 1, hi - lo, F, SEED, oracle.TAG_H,
                                             rows_total=L.shape.rows, r_begin=lo)
+    hq = L.ht[0][0].clone()
+    hqs = L.ht[1][0].clone()
+    hq[:, lo:hi] = torch.from_numpy(ht[0]).cuda()
+    hqs[:, lo // 32:hi // 32] = torch.from_numpy(hts[0]).cuda()
+    dw2 = pmn.gemm_mxfp8(L.dy_t[0], L.dy_t[1], hq, hqs, L.offsets, pmn.GROUP_K, torch.float32)
+    torch.cuda.synchronize()
+    assert pmn.get_device_error() == 0
     dq, dqs = oracle.mxfp8_quantize(hb(L.dy[lo:hi]), transpose=True)
-    ref = oracle.mxfp8_dequant_f64(dq, dqs) @ oracle.mxfp8_dequant_f64(ht[0], hts[0]).T
-    got = hu(L.dw2[e]).astype(np.float64)
-    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
-    assert rel < 0.02, rel
+    A = oracle.mxfp8_dequant_f64(dq, dqs)
+    B = oracle.mxfp8_dequant_f64(ht[0], hts[0])
+    check_f32(hu(dw2[e]), A @ B.T, np.abs(A) @ np.abs(B).T, "dW2 of expert %d" % e)
+    # the step's own dW2 of that expert is the same GEMM on the step's H^T
+    assert torch.equal(pmn.gemm_mxfp8(L.dy_t[0], L.dy_t[1], L.ht[0][0], L.ht[1][0], L.offsets, pmn.GROUP_K,
+                                      torch.float32)[e], L.dw2[e])
+    del dw2
 
 
 def test_fullsize_step_is_deterministic(run):
@@ -243,10 +300,15 @@ def test_fullsize_step_is_deterministic(run):
 def test_decode_forward_against_oracle(run):
     """Decode batch: 64 tokens, top-8 of the 384 experts, segments of 1-5 rows
     (not padded), against the step's NVFP4 weights of every expert.  The
-    activation codes and scales are bytes; Y rows of the first, the last and
-    the most-used hit expert within the GEMM tolerance; the combine payload of
-    the most-used one by the step's property."""
-    from precision_moe_numerics_gb300 import layer
+    activation codes and scales are bytes; h rows of the first, the last and
+    the most-used hit expert within the SwiGLU bound, and the NVFP4 of h on
+    every row equal to the plain quantiser's on the kernel's h; the combine
+    payload on every row equal to the standalone RHT + S2F6 kernel's bytes on
+    the fused epilogue's input, and that input, on the most-used expert's rows
+    with h replaced by the oracle's own NVFP4 of its h, within the float32
+    GEMM tolerance of the binary64 product."""
+    from swiglu_checks import check_h, check_h_coding
+    from precision_moe_numerics_gb300 import layer, pmn
     L = run["L"]
     E, F2, D = L.w1.shape
     F = F2 // 2
@@ -265,18 +327,26 @@ def test_decode_forward_against_oracle(run):
     top = int(np.argmax(r.counts))
     for e in sorted({hit[0], hit[-1], top}):
         lo, hi = seg(r, e)
-        wc, ws, wg = oracle_w(run, "w1", e)
-        ref = oracle.gemm_nvfp4(xc[lo:hi], xs[lo:hi], xg[lo:hi], wc, ws, wg[0])
-        A = np.abs(oracle.nvfp4_dequant_f64(xc[lo:hi], xs[lo:hi])) * np.abs(xg[lo:hi, None].astype(np.float64))
-        B = np.abs(oracle.nvfp4_dequant_f64(wc, ws)) * abs(float(wg[0]))
-        check_bf16(hb(dec.y[lo:hi]), ref, A @ B.T, "decode Y rows of expert %d" % e)
+        y, absab, _, _ = oracle_h(run, xb[lo:hi], e)
+        check_h(hb(dec.h[lo:hi]), y, absab, F, "decode h rows of expert %d" % e)
+    check_h_coding(pmn, dec.h, *dec.hq, int(r.offsets[-1]), "decode h")
+    T = xb.shape[0]
+    acc = torch.empty((T, D), dtype=torch.float32, device="cuda")
+    q, sc = pmn.w2_gemm_rht_s2f6(dec.hq, L.w2q3(), offs, SEED, debug_acc=acc)
+    assert torch.equal(q, dec.z[0]) and torch.equal(sc, dec.z[1])
+    sq, ssc = pmn.rht_s2f6_quantize(acc, SEED)
+    assert torch.equal(sq, q) and torch.equal(ssc, sc)
     lo, hi = seg(r, top)
-    w1c, w1s, w1g = oracle_w(run, "w1", top)
-    y = oracle.bf16_rne_array(oracle.gemm_nvfp4(xc[lo:hi], xs[lo:hi], xg[lo:hi], w1c, w1s, w1g[0]))
-    h = oracle.swiglu_bf16(y, F)
-    hc, hs, hg = oracle.nvfp4_quantize(h, oracle.OUTER_PER_ROW, four_over_six=True)
+    _, _, _, (hc, hs, hg) = oracle_h(run, xb[lo:hi], top)
+    hq = tuple(t.clone() for t in dec.hq)
+    for t, v in zip(hq, (hc, hs, hg)):
+        t[lo:hi] = torch.from_numpy(v).cuda()
+    q, sc = pmn.w2_gemm_rht_s2f6(hq, L.w2q3(), offs, SEED, debug_acc=acc)
     w2c, w2s, w2g = oracle_w(run, "w2", top)
     z = oracle.gemm_nvfp4(hc, hs, hg, w2c, w2s, w2g[0])
-    zq = oracle.s2f6_dequant_inverse_rht(hu(dec.z[0][lo:hi]), hu(dec.z[1][lo:hi]), SEED)
-    rel = np.linalg.norm(zq - z) / np.linalg.norm(z)
-    assert rel < 0.02, rel
+    A = np.abs(oracle.nvfp4_dequant_f64(hc, hs)) * np.abs(hg[:, None].astype(np.float64))
+    B = np.abs(oracle.nvfp4_dequant_f64(w2c, w2s)) * abs(float(w2g[0]))
+    check_f32(hu(acc[lo:hi]), z, A @ B.T, "decode w2 accumulator of expert %d" % top)
+    sq, ssc = pmn.rht_s2f6_quantize(acc[lo:hi], SEED)
+    assert torch.equal(sq, q[lo:hi]) and torch.equal(ssc, sc[lo:hi])
+    assert pmn.get_device_error() == 0

@@ -144,10 +144,24 @@ def test_bf16_rne_vs_torch():
 
 
 def test_storage_bits_per_value(golden):
+    """The pages' bits per value (NVFP4 4.5, MXFP8 and the S2F6 combine 8.25)
+    measured on the buffers the oracle returns: the bytes of every code and
+    scale tensor (outer scales are per row or per tensor, not per value)."""
+    import precision_moe_numerics_gb300.workloads as W
     bpv = golden["bits_per_value"]
+    rng = np.random.default_rng(4)
     rows, cols = 64, 4096
-    codes_bytes = rows * cols // 2
-    scale_bytes = rows * cols // 16
-    assert (codes_bytes + scale_bytes) * 8 / (rows * cols) == bpv["nvfp4"]
-    assert (rows * cols + rows * cols // 32) * 8 / (rows * cols) == bpv["mxfp8"]
-    assert (rows * cols + rows * cols // 32) * 8 / (rows * cols) == bpv["combine_s2f6"]
+    x = W.normal_bf16_host(rng, (rows, cols))
+    c, s, g = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW, four_over_six=True)
+    assert (c.nbytes + s.nbytes) * 8 / x.size == bpv["nvfp4"]
+    assert g.shape == (rows,)
+    q, qs = oracle.mxfp8_quantize(x)
+    assert (q.nbytes + qs.nbytes) * 8 / x.size == bpv["mxfp8"]
+    qt, qts = oracle.mxfp8_quantize(x, transpose=True)
+    assert (qt.nbytes + qts.nbytes) * 8 / x.size == bpv["mxfp8"]
+    rq, rqs = oracle.requant_transpose_mxfp8(c, s, g, True, 1, rows, cols, 0, oracle.TAG_X)
+    assert (rq.nbytes + rqs.nbytes) * 8 / x.size == bpv["mxfp8"]
+    z, zs = oracle.rht_s2f6(W.bf16_bits_to_f32(x), 0)
+    assert (z.nbytes + zs.nbytes) * 8 / x.size == bpv["combine_s2f6"]
+    fc, fs, fg = oracle.requant_transpose_nvfp4(c, s, g, True, 1, rows, cols, 0, oracle.TAG_X)
+    assert (fc.nbytes + fs.nbytes) * 8 / x.size == bpv["nvfp4"]

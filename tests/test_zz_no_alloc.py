@@ -1,7 +1,9 @@
 """The per-group NVFP4 quantisation entry point whose scratch is a fixed device
 array (pmn_nvfp4_quantize_per_group_noalloc) produces the same bytes as the
-allocating entry point, call after call.  Collected last, so it also runs
-after every other GPU test has used the library."""
+workspace entry point, call after call.  It serves callers that cannot
+allocate device memory while they run (all memory reserved at start-up, or a
+host framework that owns every allocation).  Collected last, so it also runs
+after every other GPU test has used the library; it passes alone as well."""
 import numpy as np
 import pytest
 import torch
@@ -50,3 +52,26 @@ def test_noalloc_group_limit(pmn):
     with pytest.raises(pmn.PmnError):
         pmn.nvfp4_quantize_per_group_noalloc(y, 16)  # 1025 groups: rejected on the host
     assert pmn.get_device_error() == 0
+
+
+def test_noalloc_on_a_side_stream_with_four_over_six(pmn):
+    """The stream argument and the 4/6 flag are forwarded: two calls in a row on
+    a non-default stream, byte for byte against the workspace entry point
+    (four_over_six=1) on the same stream."""
+    rng = np.random.default_rng(7)
+    E, N, K = 3, 600, 2048
+    x = dev_bf16(W.normal_bf16_host(rng, (E * N, K), 0.02, 0.001, 30.0))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        ref = pmn.nvfp4_quantize(x, outer_mode=pmn.OUTER_PER_GROUP, rows_per_group=N, four_over_six=True,
+                                 stream=side)
+        for call in range(2):
+            got = pmn.nvfp4_quantize_per_group_noalloc(x, N, four_over_six=True, stream=side)
+            side.synchronize()
+            for a, b, what in zip(got, ref, ("codes", "scales", "outer")):
+                assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), "call %d: %s differ" % (call, what)
+    # the 4/6 flag reached the kernel: its outer scale is amax / (4 * 448), not amax / (6 * 448)
+    amax = x.float().abs().view(E, -1).amax(dim=1)
+    assert torch.allclose(got[2], amax / 1792.0, rtol=1e-6, atol=0.0)
+    assert pmn.get_device_error(side) == 0
