@@ -167,7 +167,7 @@ def oracle_sample(inputs, experts, seed=0):
         w2q = oracle.nvfp4_quantize(w2, oracle.OUTER_PER_GROUP, group_offsets=[0, D])
         xq = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW, four_over_six=True)
         y = oracle.grouped_gemm_nvfp4(xq[0], xq[1], xq[2], w1q[0][None], w1q[1][None], w1q[2], [0, n])
-        h = oracle.swiglu_bf16_from_f64(y, F)
+        h = oracle.swiglu_bf16(oracle.bf16_rne_array(y), F)
         hq = oracle.nvfp4_quantize(h, oracle.OUTER_PER_ROW, four_over_six=True)
         z = oracle.grouped_gemm_nvfp4(hq[0], hq[1], hq[2], w2q[0][None], w2q[1][None], w2q[2], [0, n])
         oracle.rht_s2f6(z.astype(np.float32), seed)

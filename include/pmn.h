@@ -112,7 +112,9 @@ PMN_API pmn_status pmn_wait_selftest(uint64_t limit_ns, void *stream);
  *  x        bf16 [rows, ldx] (PMN_IN_BF16: the row's first `cols` values are
  *           quantised) or bf16 [rows, ldx] holding gate | up halves of width
  *           `cols` each (PMN_IN_BF16_SWIGLU: h = silu(gate) * up is formed in
- *           float32, rounded to bf16, then quantised).
+ *           float32 -- gate * up / (1 + e^-gate) with the hardware's
+ *           approximate exponential and division, within a few dozen float32
+ *           ulps -- rounded to bf16, then quantised).
  *  rows, cols  cols % 16 == 0, cols <= 8192 (one row lives in one CTA).
  *  ldx      leading dimension of x in elements (>= cols, or >= 2*cols).
  *  outer_mode  PMN_OUTER_PER_ROW: outer[rows], g = amax(row) / M.
@@ -271,11 +273,13 @@ PMN_API pmn_status pmn_mxfp8_quantize_swiglu(const void *y, int64_t rows, int64_
  *  n        multiple of 128;  k multiple of 256.
  *  out_kind PMN_OUT_BF16 (bf16 [total_rows, n]) or PMN_OUT_F32, or
  *           PMN_OUT_SWIGLU_BF16 (n % 256 == 0): bf16 h [total_rows, n/2] with
- *           h[m, j] = silu(Z[m, j]) * Z[m, n/2 + j] formed in float32 from the
- *           float32 Z (not rounded to bf16 first), gate = the first n/2 rows
- *           of each B_e, up = the last n/2, then rounded to bf16 (nearest
- *           even).  SwiGLU between w1 and w2 is not on the pages; the w1
- *           shape [2F, d_model] makes the layer gated.
+ *           h[m, j] = silu(y[m, j]) * y[m, n/2 + j], y = Z rounded to bf16 as
+ *           PMN_OUT_BF16 writes it (gate = the first n/2 rows of each B_e, up =
+ *           the last n/2), formed in float32 and rounded to bf16 (nearest
+ *           even): the arithmetic of pmn_nvfp4_quantize's PMN_IN_BF16_SWIGLU
+ *           on the bf16 output, so h equals that unfused path's bit for bit.
+ *           SwiGLU between w1 and w2 is not on the pages; the w1 shape
+ *           [2F, d_model] makes the layer gated.
  * Rows outside every expert segment are not written.
  */
 PMN_API pmn_status pmn_grouped_gemm_nvfp4(const uint8_t *a_codes, const uint8_t *a_scales,

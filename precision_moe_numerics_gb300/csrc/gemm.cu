@@ -809,37 +809,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             };
             if constexpr (SWI) {
                 // accumulator columns 0..127 hold the gate values, 128..255 the up
-                // values of the same 128 h columns: chunk c of h pairs gate chunk c
-                // with up chunk c + 4.  All four are read, then the accumulator is
-                // released and h stored.
-                uint4 ch[4][NCH];
+                // values of the same 128 h columns.  y = acc * g_t * g_e is rounded
+                // to bf16 as the bf16 output does (every chunk is read, then the
+                // accumulator is released to the next tile's MMAs); h = silu(gate)
+                // * up is then formed in binary32 from those bf16 values while the
+                // MMAs run -- the same arithmetic as the SwiGLU input mode of the
+                // row quantiser, so h equals the unfused path's bit for bit.
+                uint32_t yb[NC][16];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t rg[32], ru[32];
-                    tmem_ld_32x32b_x32(tbase + 32 * c, rg);
-                    tmem_ld_32x32b_x32(tbase + 128 + 32 * c, ru);
+                for (int c = 0; c < NC; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + 32 * c, r);
                     tmem_ld_wait();
-                    uint32_t w[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        float hv[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            // y = acc * g_t * g_e, then h = silu(gate) * up in binary32
-                            const float a = __fmul_rn(__fmul_rn(__uint_as_float(rg[2 * j + u]), scale), gb);
-                            const float b = __fmul_rn(__fmul_rn(__uint_as_float(ru[2 * j + u]), scale), gb);
-                            hv[u] = __fmul_rn(__fdiv_rn(a, __fadd_rn(1.0f, expf(-a))), b);
-                        }
-                        __nv_bfloat162 b2 = __floats2bfloat162_rn(hv[0], hv[1]);
-                        w[j] = *reinterpret_cast<uint32_t *>(&b2);
+                        const float v0 = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * j]), scale), gb);
+                        const float v1 = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * j + 1]), scale), gb);
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
+                        yb[c][j] = *reinterpret_cast<uint32_t *>(&b2);
                     }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) ch[c][j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                 }
                 release();
                 if (slice_any) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) store(c, ch[c]);
+                    for (int c = 0; c < NC / 2; ++c) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const uint32_t gw = yb[c][j], uw = yb[c + NC / 2][j];
+                            float hv[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const float a = __uint_as_float(u ? (gw & 0xFFFF0000u) : (gw << 16));
+                                const float b = __uint_as_float(u ? (uw & 0xFFFF0000u) : (uw << 16));
+                                hv[u] = silu_mul(a, b);
+                            }
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(hv[0], hv[1]);
+                            w[j] = *reinterpret_cast<uint32_t *>(&b2);
+                        }
+                        uint4 o[NCH];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) o[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                        store(c, o);
+                    }
                 }
             } else if constexpr (TWO_PHASE) {
                 uint4 ch[NC][NCH];

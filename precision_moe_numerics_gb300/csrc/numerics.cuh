@@ -12,6 +12,19 @@
 
 namespace pmn {
 
+// ---------------------------------------------------------------- SwiGLU
+// h = silu(a) * b = a * b / (1 + e^-a) in binary32, with the hardware's
+// approximate exponential and division (the __expf / __fdividef intrinsics:
+// a few dozen binary32 ulps at most for |a| <= 40; for a < -87 the quotient
+// is 0, against a true |silu(a)| < 2^-120 |a|).  Every SwiGLU of the library
+// (the w1 GEMM epilogue, the row quantisers' SwiGLU input modes) uses this
+// one function, so they give the same h bit for bit; h is rounded to bf16
+// afterwards, a step of 2^-8 relative.
+__device__ __forceinline__ float silu_mul(float a, float b)
+{
+    return __fmul_rn(__fdividef(a, __fadd_rn(1.0f, __expf(-a))), b);
+}
+
 // ---------------------------------------------------------------- decoders
 // E2M1 magnitude code m (0..7): e = m >> 1, mantissa bit m & 1; e == 0 is the
 // subnormal 0 / 0.5, otherwise (1 + mant/2) * 2^(e-1).  Built as float bits.

@@ -211,8 +211,8 @@ __global__ void __launch_bounds__(256, NB <= 4 ? PMN_QR_MIN_BLOCKS : 1) nvfp4_qu
                     for (int t = 0; t < 4; ++t) {
                         float a0 = bf16_lo(gw[t]), a1 = bf16_hi(gw[t]);
                         float u0 = bf16_lo(uw[t]), u1 = bf16_hi(uw[t]);
-                        float h0 = __fmul_rn(__fdiv_rn(a0, __fadd_rn(1.0f, expf(-a0))), u0);
-                        float h1 = __fmul_rn(__fdiv_rn(a1, __fadd_rn(1.0f, expf(-a1))), u1);
+                        float h0 = silu_mul(a0, u0);
+                        float h1 = silu_mul(a1, u1);
                         __nv_bfloat16 b0 = __float2bfloat16_rn(h0), b1 = __float2bfloat16_rn(h1);
                         hw[t] = (uint32_t)__bfloat16_as_ushort(b0) | ((uint32_t)__bfloat16_as_ushort(b1) << 16);
                     }
@@ -631,8 +631,8 @@ __global__ void __launch_bounds__(256) mxfp8_swiglu_rowwise_kernel(const uint16_
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const float a0 = bf16_lo(gw[i]), a1 = bf16_hi(gw[i]);
-        const float h0 = __fmul_rn(__fdiv_rn(a0, __fadd_rn(1.0f, expf(-a0))), bf16_lo(uw[i]));
-        const float h1 = __fmul_rn(__fdiv_rn(a1, __fadd_rn(1.0f, expf(-a1))), bf16_hi(uw[i]));
+        const float h0 = silu_mul(a0, bf16_lo(uw[i]));
+        const float h1 = silu_mul(a1, bf16_hi(uw[i]));
         hw[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(h0)) |
                 ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(h1)) << 16);
         m = __vmaxu2(m, hw[i] & 0x7FFF7FFFu);  // |bf16| orders as integers

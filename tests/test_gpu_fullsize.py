@@ -163,14 +163,15 @@ def test_fullsize_gradient_quantisation(run):
 
 def oracle_h(run, x_bits, e):
     """the oracle's chain for rows of expert e: NVFP4 of X (4/6), the binary64 w1
-    product, |A||B|, h (bf16 from binary64) and its NVFP4 (4/6)"""
+    product, |A||B|, h (SwiGLU of the product rounded to bf16, as the layer
+    computes it) and its NVFP4 (4/6)"""
     xc, xs, xg = oracle.nvfp4_quantize(x_bits, oracle.OUTER_PER_ROW, four_over_six=True)
     wc, ws, wg = oracle_w(run, "w1", e)
     y = oracle.gemm_nvfp4(xc, xs, xg, wc, ws, wg[0])
     A = np.abs(oracle.nvfp4_dequant_f64(xc, xs)) * np.abs(xg[:, None].astype(np.float64))
     B = np.abs(oracle.nvfp4_dequant_f64(wc, ws)) * abs(float(wg[0]))
     F = wc.shape[0] // 2
-    h = oracle.swiglu_bf16_from_f64(y, F)
+    h = oracle.swiglu_bf16(oracle.bf16_rne_array(y), F)
     return y, A @ B.T, h, oracle.nvfp4_quantize(h, oracle.OUTER_PER_ROW, four_over_six=True)
 
 

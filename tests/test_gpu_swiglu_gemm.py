@@ -3,14 +3,16 @@ coding of h (pmn_w1_gemm_swiglu_nvfp4), and of the single-expert forward at
 T = 4096 tokens (X -> NVFP4 with 4/6 -> w1 GEMM + SwiGLU -> NVFP4 of h -> w2
 GEMM -> bf16).
 
-h.  The epilogue forms y = acc * g_t * g_e in float32, h = silu(gate) * up in
-float32 and rounds h to bf16.  The oracle's reading (swiglu_bf16_from_f64)
-forms h from the binary64 product, Y not rounded to bf16 first, and rounds it
-once to bf16.  Per element: |h - h_ref| <= 2^-7 |h_ref| (the two roundings to
-bf16, half a step each) + 2^-20 |h_ref| (the float32 arithmetic of the
-SwiGLU) + 2 (|dh/da| tau_a + |dh/db| tau_b), the GEMM's tolerance tau =
-1e-3 (|A||B|) (outer scales included) carried through the SwiGLU to first
-order with a factor of two.
+h.  The epilogue rounds y = acc * g_t * g_e to bf16 (as the bf16 GEMM output
+does), then forms h = silu(gate) * up in binary32 and rounds h to bf16: the
+arithmetic of the unfused path (bf16 GEMM output, then the row quantiser's
+SwiGLU input mode), so h must equal that path's h bit for bit.  Against the
+oracle (swiglu_bf16_from_f64 of the binary64 product): per element
+|h - h_ref| <= 2^-7 |h_ref| (two roundings to bf16, half a step each)
++ 2^-16 |h_ref| (the float32 SwiGLU with the approximate exponential and
+division, a few dozen float32 ulps) + 2 (|dh/da| tau_a + |dh/db| tau_b), the
+bf16 GEMM tolerance of y, tau = 2^-8 |y| + 1e-3 (|A||B|) (outer scales
+included), carried through the SwiGLU to first order with a factor of two.
 
 NVFP4 of h.  Codes, scales and outer scales equal, byte for byte on every row,
 those of the plain per-row quantiser (pmn_nvfp4_quantize, PER_ROW, 4/6) run on
@@ -88,6 +90,13 @@ def test_swiglu_gemm_small_moe(pmn):
     h2 = torch.full_like(h, 7.0)
     P.grouped_gemm_nvfp4(A, B, offs, swiglu=True, out=h2)
     assert torch.equal(h.view(torch.int16), h2.view(torch.int16))
+    # the unfused path (bf16 Y, then the row quantiser's SwiGLU input mode) gives the same h and bytes
+    rows = int(r.offsets[-1])
+    y = P.grouped_gemm_nvfp4(A, B, offs, out_dtype=torch.bfloat16)
+    uc, us, ug, uh = P.nvfp4_quantize(y[:rows], cols=f, swiglu=True, four_over_six=True, want_h=True)
+    assert torch.equal(uh.view(torch.int16), h[:rows].view(torch.int16))
+    for a, b in zip((uc, us, ug), hq):
+        assert torch.equal(a.view(torch.uint8), b[:rows].view(torch.uint8))
     # run to run: same bytes
     again = P.w1_gemm_swiglu_nvfp4(A, B, offs, True)
     for a, b in zip(hq, again):
@@ -159,8 +168,8 @@ def test_single_expert_forward(pmn):
     check_h(host_bits(h), y_ref, absab, F, "single expert")
     check_h_coding(P, h, *hq, T, "single expert")
 
-    # w2 GEMM on the oracle's own NVFP4 of its own h
-    h_ref = oracle.swiglu_bf16_from_f64(y_ref, F)
+    # w2 GEMM on the oracle's own NVFP4 of its own h (the SwiGLU of the product rounded to bf16)
+    h_ref = oracle.swiglu_bf16(oracle.bf16_rne_array(y_ref), F)
     rh = oracle.nvfp4_quantize(h_ref, oracle.OUTER_PER_ROW, four_over_six=True)
     b2 = (rw2[0].reshape(1, D, F // 2), rw2[1].reshape(1, D, F // 16), rw2[2])
     z = P.grouped_gemm_nvfp4((dev(rh[0]), dev(rh[1]), dev(rh[2])), tuple(dev(a) for a in b2), offs,
