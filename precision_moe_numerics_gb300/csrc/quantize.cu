@@ -1067,18 +1067,36 @@ __device__ __forceinline__ uint32_t sr_bits_of(const uint4 &wd, int e)
 
 // Thread = 16 input rows x 8 input columns, as requant_transpose_kernel: the
 // 16 rows of one column are exactly one output 16-block and one Philox
-// counter.  CTA = 4 warps = 128 rows x 128 columns.
+// counter.  CTA = 4 warps = 128 rows x 128 columns.  Per block the scale's
+// reciprocal RN(1 / RN(dec(S') g')) comes from a per-CTA table of the 127
+// finite E4M3 values (g' is the entry's); the products are packed binary32
+// multiplies; per-expert inputs take the block's amax from the exact f16
+// products code * S (amax_i RN(cs_i g) = RN(amax_i cs_i * g), g > 0).  Codes
+// and scales are staged in shared memory ([output row][16-row chunk], chunk
+// XOR bits 3..5 of the row) and written as 16-byte pieces, four lanes per
+// output row.
 template <bool PER_ROW>
 __global__ void __launch_bounds__(128, 4) requant_transpose_nvfp4_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, const float *__restrict__ outer,
     int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, int stochastic, const uint32_t *__restrict__ gmax,
     uint8_t *__restrict__ out, uint8_t *__restrict__ out_sc)
 {
+    __shared__ __align__(16) uint2 oS[128 * 8];     // [output row][chunk ^ swizzle]: 16 codes = 8 bytes
+    __shared__ __align__(8) uint8_t scS[128 * 8];   // [output row][chunk]: E4M3 block scale
+    __shared__ float rtab[128];                     // RN(1 / RN(dec(S) g')), 0 where that product is 0
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, q = lane & 15, hf = lane >> 4;
     const int64_t b = blockIdx.z;
-    const int64_t row0 = (int64_t)blockIdx.y * 128 + 32 * w + 16 * hf;
-    const int64_t col0 = (int64_t)blockIdx.x * 128 + 8 * q;
-    if (row0 >= rows || col0 >= cols) return;
+    const int64_t r0 = (int64_t)blockIdx.y * 128, c0 = (int64_t)blockIdx.x * 128;
+    const int64_t row0 = r0 + 32 * w + 16 * hf;
+    const int64_t col0 = c0 + 8 * q;
+    const float gp = nvfp4_outer_from_max(__ldg(gmax + b));
+    if (threadIdx.x < 127) {
+        const float sd = __fmul_rn(e4m3_to_f32(threadIdx.x), gp);
+        rtab[threadIdx.x] = sd == 0.0f ? 0.0f : __frcp_rn(sd);
+    }
+    __syncthreads();
+    if (row0 < rows && col0 < cols) {
+    const int chunk = 2 * w + hf;  // the thread's 16-row chunk of the tile
     const int64_t cols2 = cols / 2, cols16 = cols / 16;
     const uint8_t *cp = codes + (b * rows + row0) * cols2 + col0 / 2;
     const uint8_t *sp = scales + (b * rows + row0) * cols16 + col0 / 16;
@@ -1094,7 +1112,6 @@ __global__ void __launch_bounds__(128, 4) requant_transpose_nvfp4_kernel(
     } else {
         g[0] = __ldg(outer + b);
     }
-    const float gp = nvfp4_outer_from_max(__ldg(gmax + b));
     const float six_g = __fmul_rn(6.0f, gp);
     const uint64_t j0 = (uint64_t)((b * cols + col0) * rows + row0) >> 4;
     const uint64_t jstep = (uint64_t)rows >> 4;
@@ -1106,20 +1123,36 @@ __global__ void __launch_bounds__(128, 4) requant_transpose_nvfp4_kernel(
         uint32_t cs[16];  // exact code * S of columns 2K (low halves) and 2K + 1 (high halves)
 #pragma unroll
         for (int i = 0; i < 16; ++i) cs[i] = e2m1x2_byte_mul_h2<K>(word[i], s2[i]);
+        uint32_t mm = 0u;
+        if (!PER_ROW) {
+            uint32_t m[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m[i] = h2_absmax_xs(cs[2 * i], cs[2 * i + 1]);
+#pragma unroll
+            for (int hh = 4; hh >= 1; hh >>= 1)
+#pragma unroll
+                for (int i = 0; i < hh; ++i) m[i] = h2_absmax_xs(m[i], m[i + hh]);
+            mm = m[0] & 0x7FFF7FFFu;
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int c = 2 * K + h;
             float d[16], amax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                d[i] = __fmul_rn(h ? h2_hi_to_f32(cs[i]) : h2_lo_to_f32(cs[i]), g[PER_ROW ? i : 0]);
-                amax = fmaxf(amax, fabsf(d[i]));
+            for (int i = 0; i < 16; i += 2) {
+                const float a0 = h ? h2_hi_to_f32(cs[i]) : h2_lo_to_f32(cs[i]);
+                const float a1 = h ? h2_hi_to_f32(cs[i + 1]) : h2_lo_to_f32(cs[i + 1]);
+                mul2(a0, a1, g[PER_ROW ? i : 0], g[PER_ROW ? i + 1 : 0], d[i], d[i + 1]);
+                if (PER_ROW) amax = fmaxf(amax, fmaxf(fabsf(d[i]), fabsf(d[i + 1])));
             }
-            const float s = __fdiv_rn(amax, six_g);
-            uint32_t S = cvt_e4m3(s);
-            if (e4m3_to_f32(S) < s && S < 0x7Eu) ++S;  // round the scale up: no value clips
-            const float sd = __fmul_rn(e4m3_to_f32(S), gp);
-            const float r = sd == 0.0f ? 0.0f : __frcp_rn(sd);
+            if (!PER_ROW) amax = __fmul_rn(h ? h2_hi_to_f32(mm) : h2_lo_to_f32(mm), g[0]);
+            const float sq = __fdiv_rn(amax, six_g);
+            uint32_t S = cvt_e4m3(sq);
+            if (e4m3_to_f32(S) < sq && S < 0x7Eu) ++S;  // round the scale up: no value clips
+            const float r = rtab[S];
+            float y[16];
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) mul2(d[i], d[i + 1], r, r, y[i], y[i + 1]);
             uint32_t packed[2] = {0u, 0u};
             if (stochastic) {
                 const uint64_t j = j0 + (uint64_t)c * jstep;
@@ -1128,28 +1161,40 @@ __global__ void __launch_bounds__(128, 4) requant_transpose_nvfp4_kernel(
                 const uint32_t wv[4] = {wd.x, wd.y, wd.z, wd.w};
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
-                    packed[q4 >> 1] |= cvt_e2m1x4_rs(__fmul_rn(d[4 * q4], r), __fmul_rn(d[4 * q4 + 1], r),
-                                                     __fmul_rn(d[4 * q4 + 2], r), __fmul_rn(d[4 * q4 + 3], r),
-                                                     wv[q4]) << (16 * (q4 & 1));
+                    packed[q4 >> 1] |= cvt_e2m1x4_rs(y[4 * q4], y[4 * q4 + 1], y[4 * q4 + 2], y[4 * q4 + 3], wv[q4])
+                                       << (16 * (q4 & 1));
 #else
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    packed[i >> 3] |= e2m1_sr(__fmul_rn(d[i], r), sr_bits_of(wd, i)) << (4 * (i & 7));
+                for (int i = 0; i < 16; ++i) packed[i >> 3] |= e2m1_sr(y[i], sr_bits_of(wd, i)) << (4 * (i & 7));
 #endif
             } else {
 #pragma unroll
-                for (int i = 0; i < 16; i += 2)
-                    packed[i >> 3] |= cvt_e2m1x2(__fmul_rn(d[i], r), __fmul_rn(d[i + 1], r)) << (4 * (i & 7));
+                for (int i = 0; i < 16; i += 2) packed[i >> 3] |= cvt_e2m1x2(y[i], y[i + 1]) << (4 * (i & 7));
             }
-            const int64_t oc = b * cols + col0 + c;
-            *reinterpret_cast<uint2 *>(out + oc * (rows / 2) + row0 / 2) = make_uint2(packed[0], packed[1]);
-            out_sc[oc * (rows / 16) + row0 / 16] = (uint8_t)S;
+            const int orow = 8 * q + c;  // output row within the tile; bits 3..5 = q & 7
+            oS[orow * 8 + (chunk ^ (q & 7))] = make_uint2(packed[0], packed[1]);
+            scS[orow * 8 + chunk] = (uint8_t)S;
         }
     };
     column_pair(std::integral_constant<int, 0>());
     column_pair(std::integral_constant<int, 1>());
     column_pair(std::integral_constant<int, 2>());
     column_pair(std::integral_constant<int, 3>());
+    }
+    __syncthreads();
+    // write-out: four lanes per output row, 16 bytes (two chunks) each
+    const int64_t vrows = min((int64_t)128, rows - r0), vcols = min((int64_t)128, cols - c0);
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int orow = it * 32 + (threadIdx.x >> 2), seg = threadIdx.x & 3;
+        if (orow >= vcols || 32 * seg >= vrows) continue;
+        const int sw = (orow >> 3) & 7;
+        const uint2 lo = oS[orow * 8 + ((2 * seg) ^ sw)], hi = oS[orow * 8 + ((2 * seg + 1) ^ sw)];
+        const int64_t oc = b * cols + c0 + orow;
+        *reinterpret_cast<uint4 *>(out + oc * (rows / 2) + r0 / 2 + 16 * seg) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        *reinterpret_cast<uint16_t *>(out_sc + oc * (rows / 16) + r0 / 16 + 2 * seg) =
+            (uint16_t)(scS[orow * 8 + 2 * seg] | (scS[orow * 8 + 2 * seg + 1] << 8));
+    }
 }
 
 // ------------------------------------------------------------------ RHT + S2F6
