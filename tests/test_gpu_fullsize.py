@@ -290,10 +290,10 @@ def test_fullsize_backward_dw2_gemm(run):
 
 def test_fullsize_step_is_deterministic(run):
     L = run["L"]
-    before = [t.clone() for t in (L.z[0], L.dw1[:2], L.dx[:512], L.w1t[0][:2])]
+    before = [t.clone() for t in (L.z[0], L.dw1[:2], L.dx[:512], L.w1t[0][:2], L.h, L.hq[0], L.hq[2])]
     L.step()
     torch.cuda.synchronize()
-    after = (L.z[0], L.dw1[:2], L.dx[:512], L.w1t[0][:2])
+    after = (L.z[0], L.dw1[:2], L.dx[:512], L.w1t[0][:2], L.h, L.hq[0], L.hq[2])
     for a, b in zip(before, after):
         assert torch.equal(a, b)
 
