@@ -1,24 +1,30 @@
 // gemm.cu -- block-scaled grouped GEMMs on the 5th-generation tensor cores
 // (tcgen05, sm_103a) for the MoE expert layer:
 //   pmn_grouped_gemm_nvfp4   forward expert GEMM, NVFP4 x NVFP4      [Layers]
+//                            (bf16, fp32 or SwiGLU epilogue)
+//   pmn_w1_gemm_swiglu_nvfp4 the w1 GEMM with SwiGLU in its epilogue,
+//                            then NVFP4 (4/6) of h            [NVLink], [Cost]
 //   pmn_w2_gemm_rht_s2f6     the same with RHT-32 + S2F6 epilogue    [NVLink]
 //   pmn_gemm_mxfp8           backward MXFP8 GEMMs, M- or K-grouped   [SR]
 // (sections of the page "Thinking Machines ... Inkling 2 Small ... native
-// 4-bit forward", arex-research.com).
+// 4-bit forward", arex-research.com), plus the library's status strings,
+// device error word and bounded-wait limit.
 //
 // One persistent kernel per call, one CTA per SM, 8 warps:
 //   warp 0      TMA producer: code tiles (128 rows x 128 bytes, 128-byte
-//               swizzle) and raw scale tiles into a 4-stage ring
+//               swizzle) and raw scale tiles into a 3- to 5-stage ring
 //   warps 2, 3  re-lay each stage's scale factors into the 32x128-bit form
-//               tcgen05.cp expects (even / odd stage slots, ahead of the MMAs)
-//   warp 1      one lane copies the scale factors to TMEM (one stage ahead)
-//               and issues the MMAs, committing to the stage's empty barrier
+//               tcgen05.cp expects (even / odd stage slots), copy them into
+//               the stage's TMEM slot and commit to its sf_ready barrier
+//   warp 1      one lane issues the MMAs of a stage once its scale factors
+//               are in TMEM, committing to the stage's empty barrier
 //   warps 4..7  epilogue: TMEM -> registers (one row per thread), outer
-//               scales, bf16/fp32 or RHT + S2F6, staged in shared memory and
-//               written by TMA tensor stores in full 128-byte lines
-// Tiles are 128 x 128 with two TMEM accumulators, so the epilogue of one
-// tile overlaps the main loop of the next.  Every wait is bounded: on timeout
-// a device error bit is latched and the CTA winds down (no trap).
+//               scales, bf16/fp32, SwiGLU or RHT + S2F6, staged in shared
+//               memory and written by TMA tensor stores in full 128-byte lines
+// 128-wide tiles hold two TMEM accumulators, so the epilogue of one tile
+// overlaps the main loop of the next; 256-wide tiles hold one and release it
+// as soon as it has been read.  Every wait is bounded: on timeout a device
+// error bit is latched and the CTA winds down (no trap).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

@@ -6,6 +6,9 @@
 //   pmn_requant_transpose_sr_nvfp4  dequant -> transpose -> SR NVFP4 (FP4 backward) [SR]
 //   pmn_rht_s2f6_quantize           RHT-32 + S2F6 combine quantisation [NVLink]
 //   pmn_combine_receive_s2f6        S2F6 decode + inverse RHT-32 + top-k sum [NVLink]
+//   pmn_nvfp4_quantize_per_group_noalloc, pmn_nvfp4_quantize_workspace_bytes,
+//   pmn_wait_selftest               (the boundary's scratch and failure handling)
+// and the h coding step of pmn_w1_gemm_swiglu_nvfp4 (gemm.cu).
 // Sections cited are those of the page "Thinking Machines ... Inkling 2
 // Small ... native 4-bit forward" (arex-research.com).
 #include <cuda_bf16.h>
