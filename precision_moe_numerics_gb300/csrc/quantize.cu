@@ -791,32 +791,26 @@ __device__ __forceinline__ PhiloxPrefix philox_prefix(uint64_t seed, uint32_t ta
     PhiloxPrefix p;
     p.k0 = (uint32_t)seed;
     p.k1 = (uint32_t)(seed >> 32);
-    const uint64_t t1 = (uint64_t)0xCD9E8D57u * tag;  // round 1, second product
-    const uint32_t x1 = (uint32_t)(t1 >> 32) ^ jhi ^ p.k0;  // round 1 output word 0
-    p.y1 = (uint32_t)t1;                                  // round 1 output word 1
-    const uint64_t t2 = (uint64_t)0xD2511F53u * x1;       // round 2, first product
-    p.x2hi = (uint32_t)(t2 >> 32);
-    p.x2lo = (uint32_t)t2;
+    const uint32_t x1 = __umulhi(0xCD9E8D57u, tag) ^ jhi ^ p.k0;  // round 1 output word 0
+    p.y1 = 0xCD9E8D57u * tag;                                   // round 1 output word 1
+    p.x2hi = __umulhi(0xD2511F53u, x1);                         // round 2, first product
+    p.x2lo = 0xD2511F53u * x1;
     return p;
 }
 
 __device__ __forceinline__ uint4 philox_from_prefix(const PhiloxPrefix &p, uint32_t jlo)
 {
     // round 1: c = (jlo, jhi, tag, 0)
-    const uint64_t a1 = (uint64_t)0xD2511F53u * jlo;
-    const uint32_t z1 = (uint32_t)(a1 >> 32) ^ p.k1, w1 = (uint32_t)a1;
+    const uint32_t z1 = __umulhi(0xD2511F53u, jlo) ^ p.k1, w1 = 0xD2511F53u * jlo;
     // round 2: c = (x1, y1, z1, w1) with keys bumped once
     const uint32_t k0 = p.k0 + 0x9E3779B9u, k1 = p.k1 + 0xBB67AE85u;
-    const uint64_t b2 = (uint64_t)0xCD9E8D57u * z1;
-    uint4 c = make_uint4((uint32_t)(b2 >> 32) ^ p.y1 ^ k0, (uint32_t)b2, p.x2hi ^ w1 ^ k1, p.x2lo);
+    uint4 c = make_uint4(__umulhi(0xCD9E8D57u, z1) ^ p.y1 ^ k0, 0xCD9E8D57u * z1, p.x2hi ^ w1 ^ k1, p.x2lo);
     uint32_t q0 = k0, q1 = k1;
 #pragma unroll
     for (int r = 2; r < 10; ++r) {
         q0 += 0x9E3779B9u;
         q1 += 0xBB67AE85u;
-        const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
-        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
-        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ q0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ q1, (uint32_t)p0);
+        c = philox_round(c, q0, q1);
     }
     return c;
 }
