@@ -87,7 +87,6 @@ constexpr int EPI_BUFS = PMN_EPI_BUFS;      // epilogue staging buffers per warp
 constexpr int STAGE_OUT_BYTES = 32 * 128;  // one epilogue staging buffer: 32 rows x 128 bytes
 constexpr int A_TILE_BYTES = BM * 128;     // A stage tile: 128 rows x 128 bytes of K
 constexpr int MAX_GROUPS = PMN_MAX_GROUPS;
-constexpr int NUM_THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;
 
 // Per (format, N-tile width) layout.  TBN = 256 tiles hold a single TMEM
@@ -99,10 +98,16 @@ constexpr uint32_t TMEM_COLS = 512;
 // loads win only where a warp-wide load covers few cache lines: MXFP8 scale
 // rows of the M-grouped 256-wide problems are 48..128 bytes long; K-grouped
 // rows are whole token ranges apart, NVFP4 rows are 16 bytes per stage.
-template <int KIND, int TBN>
+//
+// EW = 8 (the K-grouped fp32 weight gradients on 256-wide tiles): eight
+// epilogue warps, two per TMEM lane quadrant, each owning 128 of the tile's
+// 256 columns, so a thread holds its whole half-row of fp32 accumulators in
+// registers and the single accumulator is released after four chunk reads.
+// Their scale rows come by TMA (K-grouped rows are token ranges apart).
+template <int KIND, int TBN, int EW = 4>
 struct Cfg {
     static constexpr int RB = TBN / 128;  // 128-row blocks of B
-    static constexpr bool SF_TMA = !(KIND == KIND_MXFP8 && TBN == 256);
+    static constexpr bool SF_TMA = !(KIND == KIND_MXFP8 && TBN == 256 && EW == 4);
     // raw scale bytes per row and stage: NVFP4 needs 16; MXFP8 needs 4, which
     // never straddle a 16-byte box because every K start (M-grouped: 0,
     // K-grouped: expert segments aligned to 128) is a multiple of 128
@@ -117,15 +122,20 @@ struct Cfg {
 #ifndef PMN_W256_MX_STAGES  // 256-wide MXFP8 tiles: 4 stages with one epilogue staging buffer per warp
 #define PMN_W256_MX_STAGES 4
 #endif
-    static constexpr int STAGES = TBN == 256 ? (KIND == KIND_MXFP8 ? PMN_W256_MX_STAGES : 3)
-                                             : (KIND == KIND_MXFP8 ? PMN_GEMM_STAGES_MXFP8 : PMN_GEMM_STAGES);
-    static constexpr int EPI = TBN == 256 ? (STAGES == 4 ? 1 : 2) : EPI_BUFS;  // epilogue staging buffers per warp
+#ifndef PMN_KG256_STAGES  // 256-wide K-grouped tiles (EW = 8)
+#define PMN_KG256_STAGES 3
+#endif
+    static constexpr int STAGES = EW == 8 ? PMN_KG256_STAGES
+                                  : TBN == 256 ? (KIND == KIND_MXFP8 ? PMN_W256_MX_STAGES : 3)
+                                               : (KIND == KIND_MXFP8 ? PMN_GEMM_STAGES_MXFP8 : PMN_GEMM_STAGES);
+    static constexpr int EPI = EW == 8 ? 1 : TBN == 256 ? (STAGES == 4 ? 1 : 2) : EPI_BUFS;  // staging buffers per warp
+    static constexpr int THREADS = 128 + 32 * EW;  // warps 0..3: producer, MMA, scale factors; then EW epilogue warps
     static constexpr int ACC = TBN == 256 ? 1 : 2;
     static constexpr uint32_t SF_COL0 = ACC * TBN;  // scale factors live after the accumulators
     static constexpr uint32_t SFA_COLS = 4 * SFT_CHUNKS, SFB_COLS = 4 * SFT_CHUNKS * RB;
     static constexpr uint32_t SF_COLS_STAGE = SFA_COLS + SFB_COLS;
     static constexpr int SMEM_BYTES =
-        1024 + STAGES * STAGE_BYTES + 4 * EPI * STAGE_OUT_BYTES + 1024 + (MAX_GROUPS + 1) * 4;
+        1024 + STAGES * STAGE_BYTES + EW * EPI * STAGE_OUT_BYTES + 1024 + (MAX_GROUPS + 1) * 4;
     static_assert(SF_COL0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -211,10 +221,10 @@ __device__ __forceinline__ void latch_error(int bit) { atomicOr(&g_pmn_device_er
 // Copies a stage's re-laid scale-factor chunks from shared memory into the
 // stage's TMEM columns (A: one 32x128b.warpx4 copy per K-step; B: one per
 // K-step and 128-row block).  Issued by one thread, which then commits.
-template <int KIND, int TBN>
+template <int KIND, int TBN, int EW>
 __device__ __forceinline__ void sf_to_tmem(uint8_t *stages, uint32_t stg, uint32_t tmem)
 {
-    using C = Cfg<KIND, TBN>;
+    using C = Cfg<KIND, TBN, EW>;
     const uint8_t *sftA = stages + stg * C::STAGE_BYTES + C::SFT_OFF;
     const uint8_t *sftB = sftA + C::SFT_A;
     const uint32_t sfa = tmem + C::SF_COL0 + stg * C::SF_COLS_STAGE;
@@ -237,21 +247,22 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
     return __all_sync(0xFFFFFFFFu, ok) != 0;
 }
 
-template <int KIND, int OUT, int TBN>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int KIND, int OUT, int TBN, int EW>
+__global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                              const __grid_constant__ CUtensorMap tmO, const GemmArgs p)
 {
-    using C = Cfg<KIND, TBN>;
+    using C = Cfg<KIND, TBN, EW>;
     constexpr int STAGES = C::STAGES;
     constexpr bool SWI = OUT == PMN_OUT_SWIGLU_BF16;
+    static_assert(EW == 4 || (EW == 8 && OUT == PMN_OUT_F32 && TBN == 256), "eight epilogue warps: fp32, 256-wide");
     static_assert(!SWI || (KIND == KIND_NVFP4 && TBN == 256), "SwiGLU tiles are 256-wide NVFP4 tiles");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
     uint8_t *staging = smem + STAGES * C::STAGE_BYTES;  // epilogue: 4 warps x EPI x 4 KB
-    uint64_t *bars = reinterpret_cast<uint64_t *>(staging + 4 * C::EPI * STAGE_OUT_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(staging + EW * C::EPI * STAGE_OUT_BYTES);
     // barrier slots: full[S], empty[S], sf_ready[S], acc_full[2], acc_empty[2], drain
     const uint32_t bar_full = smem_u32(bars), bar_empty = bar_full + 8 * STAGES;
     const uint32_t bar_sfr = bar_empty + 8 * STAGES;  // scale factors re-laid for the stage
@@ -260,7 +271,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 5);
     int *s_abort = reinterpret_cast<int *>(tmem_slot + 1);
     int *s_total = s_abort + 1;
-    int *s_cum = reinterpret_cast<int *>(staging + 4 * C::EPI * STAGE_OUT_BYTES + 1024);
+    int *s_cum = reinterpret_cast<int *>(staging + EW * C::EPI * STAGE_OUT_BYTES + 1024);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -272,7 +283,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_acc_full + 8 * b, 1);
-            mbar_init(bar_acc_empty + 8 * b, 4);
+            mbar_init(bar_acc_empty + 8 * b, EW);
         }
         mbar_init(bar_drain, 1);
         *s_abort = 0;
@@ -442,7 +453,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (lane == 0) {
                         PMN_TRACE_POINT(2, seq);
                         tc_fence_after();
-                        sf_to_tmem<KIND, TBN>(stages, stage, tmem);
+                        sf_to_tmem<KIND, TBN, EW>(stages, stage, tmem);
                         tc_commit(bar_sfr + 8 * stage);  // sf_ready once the copies land
                     }
                     if (++stage == STAGES) {
@@ -560,7 +571,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) {
                     PMN_TRACE_POINT(2, quse);
                     tc_fence_after();
-                    sf_to_tmem<KIND, TBN>(stages, stage, tmem);
+                    sf_to_tmem<KIND, TBN, EW>(stages, stage, tmem);
                     tc_commit(bar_sfr + 8 * stage);  // sf_ready once the copies land
                 }
                 return true;
@@ -678,7 +689,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // full 128-byte lines; a slice cut by an expert boundary is written
         // row by row with predicated stores.
         const int q = warp & 3;
-        uint8_t *stg = staging + q * C::EPI * STAGE_OUT_BYTES;
+        constexpr int CW = TBN / (EW / 4);  // columns per epilogue warp
+        const int cb = ((warp - 4) >> 2) * CW;  // the warp's first column in the tile
+        uint8_t *stg = staging + (warp - 4) * C::EPI * STAGE_OUT_BYTES;
         // fp32 outputs (the weight gradients, written once) are stored with an
         // L2 evict_last policy: measured 1-2 % faster than the default or
         // evict_first for dW1 / dW2
@@ -695,8 +708,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (ti.nks == 0) {
                 // empty contraction: the product is zero
                 if (valid && OUT == PMN_OUT_F32) {
-                    float *o = reinterpret_cast<float *>(p.out) + ((int64_t)ti.g * p.m + row) * p.n + ti.n0;
-                    for (int c = 0; c < TBN; c += 4) *reinterpret_cast<float4 *>(o + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float *o = reinterpret_cast<float *>(p.out) + ((int64_t)ti.g * p.m + row) * p.n + ti.n0 + cb;
+                    for (int c = 0; c < CW; c += 4) *reinterpret_cast<float4 *>(o + c) = make_float4(0.f, 0.f, 0.f, 0.f);
                 } else if (valid && OUT == PMN_OUT_BF16) {
                     uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + ((int64_t)ti.g * p.m + row) * p.n + ti.n0;
                     for (int c = 0; c < TBN; c += 8) *reinterpret_cast<uint4 *>(o + c) = make_uint4(0u, 0u, 0u, 0u);
@@ -732,9 +745,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // register-hungry RHT + S2F6 conversion) chunks are read, converted
             // and stored in turn and the release follows the last read.
             constexpr int NCH = OUT == PMN_OUT_F32 ? 8 : ((OUT == PMN_OUT_BF16 || SWI) ? 4 : 2);  // 16-byte pieces per chunk
-            constexpr int NC = TBN / 32;
+            constexpr int NC = CW / 32;  // 32-column chunks of the warp
             constexpr bool TWO_PHASE = NC * NCH <= 32 && OUT != PMN_OUT_RHT_S2F6 && !SWI;
-            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + abuf * TBN;
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + abuf * TBN + cb;
             auto convert = [&](uint32_t (&r)[32], int c, uint4 (&o)[NCH]) {
                 float v[32];
 #pragma unroll
@@ -794,7 +807,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            const int32_t x = (int32_t)((SWI ? ti.n0 / 2 : ti.n0) + 32 * (c - part));
+                            const int32_t x = (int32_t)((SWI ? ti.n0 / 2 : ti.n0) + cb + 32 * (c - part));
                             const int32_t y = (int32_t)(obase + ti.m0 + 32 * q);
                             if (OUT == PMN_OUT_F32) tma_store_2d_hint(&tmO, smem_u32(buf), x, y, st_policy);
                             else tma_store_2d(&tmO, smem_u32(buf), x, y);
@@ -803,7 +816,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ++nstore;
                     }
                 } else if (valid) {
-                    const int64_t col = (SWI ? ti.n0 / 2 : ti.n0) + 32 * c;
+                    const int64_t col = (SWI ? ti.n0 / 2 : ti.n0) + cb + 32 * c;
                     uint8_t *o8;
                     if (SWI) o8 = reinterpret_cast<uint8_t *>(reinterpret_cast<uint16_t *>(p.out) + orow * (p.n / 2) + col);
                     else if (OUT == PMN_OUT_F32) o8 = reinterpret_cast<uint8_t *>(reinterpret_cast<float *>(p.out) + orow * p.n + col);
@@ -997,14 +1010,17 @@ struct GemmMaps {
     MapSpec a, b, sa, sb;
 };
 
+#ifndef PMN_GEMM_WIDE_KG  // 256-wide tiles with eight epilogue warps for the K-grouped fp32 gradients
+#define PMN_GEMM_WIDE_KG 1
+#endif
 #ifndef PMN_GEMM_WIDE_M  // 256-wide tiles for M-grouped problems
 #define PMN_GEMM_WIDE_M 1
 #endif
 
-template <int KIND, int OUT, int TBN>
+template <int KIND, int OUT, int TBN, int EW = 4>
 pmn_status launch_gemm_tbn(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
 {
-    using C = Cfg<KIND, TBN>;
+    using C = Cfg<KIND, TBN, EW>;
     CUtensorMap a, b, sa, sb;
     const uint32_t raw_w = 16;  // raw scale rows: one 16-byte box per row and stage
     const uint32_t b_box = OUT == PMN_OUT_SWIGLU_BF16 ? 128 : TBN;  // SwiGLU: gate and up halves load separately
@@ -1019,13 +1035,13 @@ pmn_status launch_gemm_tbn(const GemmMaps &ms, const CUtensorMap &o, const GemmA
     ka.sb = static_cast<const uint8_t *>(ms.sb.base);
     ka.sa_pitch = (int64_t)ms.sa.pitch;
     ka.sb_pitch = (int64_t)ms.sb.pitch;
-    auto kern = block_scaled_gemm_kernel<KIND, OUT, TBN>;
+    auto kern = block_scaled_gemm_kernel<KIND, OUT, TBN, EW>;
     const int smem = C::SMEM_BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return PMN_ERR_CUDA;
     const int sms = num_sms();
     if (sms <= 0) return PMN_ERR_CUDA;
-    kern<<<dim3((unsigned)sms), dim3(NUM_THREADS), smem, s>>>(a, b, sa, sb, o, ka);
+    kern<<<dim3((unsigned)sms), dim3(C::THREADS), smem, s>>>(a, b, sa, sb, o, ka);
     return cudaGetLastError() == cudaSuccess ? PMN_OK : PMN_ERR_CUDA;
 }
 
@@ -1041,6 +1057,13 @@ pmn_status launch_gemm(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs 
     // (two 128-wide accumulators) beats the halved A traffic
     if constexpr (OUT == PMN_OUT_SWIGLU_BF16) {
         return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);
+    } else if constexpr (KIND == KIND_MXFP8 && OUT == PMN_OUT_F32) {
+        // K-grouped weight gradients: 256-wide tiles with eight epilogue warps
+        if (PMN_GEMM_WIDE_KG && args.group_k && args.n % 256 == 0)
+            return launch_gemm_tbn<KIND, OUT, 256, 8>(ms, o, args, s);
+        if (PMN_GEMM_WIDE_M && !args.group_k && args.n % 256 == 0)
+            return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);
+        return launch_gemm_tbn<KIND, OUT, 128>(ms, o, args, s);
     } else {
         if (PMN_GEMM_WIDE_M && OUT != PMN_OUT_RHT_S2F6 && !args.group_k && args.n % 256 == 0)
             return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);

@@ -205,6 +205,29 @@ def test_gemm_mxfp8_kgrouped(pmn):
         check_mx(out[g], ref[g], absab, "mxfp8 K-grouped g=%d" % g)
 
 
+@pytest.mark.parametrize("M,N", [(256, 512), (128, 1536)])
+def test_gemm_mxfp8_kgrouped_wide_tiles(pmn, M, N):
+    """K-grouped with N a multiple of 256: the 256-wide tiles with eight
+    epilogue warps (each holding half a row of the accumulator); an empty
+    group, segments of one, four and six 128-row stages."""
+    rng = np.random.default_rng(24 + N)
+    offs = np.array([0, 128, 128, 640, 768, 1536], np.int32)
+    G, Kt = len(offs) - 1, int(offs[-1])
+    a, asc = oracle.mxfp8_quantize(W.normal_bf16_host(rng, (Kt, M), 1e-3, 0.01, 20.0), transpose=True)
+    b, bsc = oracle.mxfp8_quantize(W.normal_bf16_host(rng, (Kt, N), 1.0), transpose=True)
+    out = pmn.gemm_mxfp8(dev(a), dev(asc), dev(b), dev(bsc), dev(offs), pmn.GROUP_K, torch.float32).cpu().numpy()
+    assert pmn.get_device_error() == 0
+    ref = oracle.gemm_mxfp8_kgrouped(a, asc, b, bsc, offs)
+    for g in range(G):
+        lo, hi = offs[g], offs[g + 1]
+        if hi == lo:
+            assert np.all(out[g] == 0)
+            continue
+        absab = np.abs(oracle.mxfp8_dequant_f64(a[:, lo:hi], asc[:, lo // 32:hi // 32])) @ np.abs(
+            oracle.mxfp8_dequant_f64(b[:, lo:hi], bsc[:, lo // 32:hi // 32])).T
+        check_mx(out[g], ref[g], absab, "mxfp8 K-grouped wide g=%d" % g)
+
+
 def test_gemm_mxfp8_kgrouped_rejects_unaligned_segments(pmn):
     """K segments must start on 128-row boundaries; a 32-aligned one runs no
     tile and latches the bad-offsets bit (checked on the device)."""
