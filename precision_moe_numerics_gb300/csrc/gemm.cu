@@ -92,12 +92,26 @@ constexpr uint32_t TMEM_COLS = 512;
 // Per (format, N-tile width) layout.  TBN = 256 tiles hold a single TMEM
 // accumulator (two of 256 columns would leave no room for scale factors) and
 // three stages; TBN = 128 tiles double-buffer the accumulator.  A stage holds
-// the A and B tiles (TMA) and the stage's scale factors in the tcgen05.cp
-// chunk layout, re-laid by the scale-factor warps from either raw scale rows
-// that TMA brought into the stage (SF_TMA) or plain global loads.  Global
-// loads win only where a warp-wide load covers few cache lines: MXFP8 scale
-// rows of the M-grouped 256-wide problems are 48..128 bytes long; K-grouped
-// rows are whole token ranges apart, NVFP4 rows are 16 bytes per stage.
+// the A and B tiles (TMA) and, where TMA brings them (SF_TMA), the raw scale
+// rows; otherwise the scale-factor warps read the rows from global memory.
+// Global loads win only where a warp-wide load covers few cache lines: MXFP8
+// scale rows of the M-grouped 256-wide problems are 48..128 bytes long;
+// K-grouped rows are whole token ranges apart, NVFP4 rows are 16 bytes per
+// stage.
+//
+// The MMA reads a stage's scale factors from TMEM in a layout replicated
+// into the four 32-lane sub-partitions (column j of a 128-row block holds
+// rows 32j .. 32j+31).  Two ways to put them there:
+//  - two warps re-lay the rows into 32 x 128-bit chunks in shared memory and
+//    tcgen05.cp copies each chunk into all four sub-partitions.  The copies
+//    queue in order with the MMAs on the tensor pipe;
+//  - SF_ST (256-wide NVFP4 tiles): four warps, one per sub-partition, write
+//    the words with tcgen05.st from registers, so the tensor pipe carries
+//    only MMAs.  There a stage needs 12 copies against 4 MMAs (measured: w1
+//    GEMM 1.29 -> 1.15 ms).  Elsewhere the copies are fewer or the issue
+//    slots of two more warps cost more than they save (measured: the
+//    128-wide w2 + RHT GEMM 0.89 -> 0.92 ms, MXFP8 dX 1.61 -> 2.18 ms with
+//    global scale rows).
 //
 // EW = 8 (the K-grouped fp32 weight gradients on 256-wide tiles): eight
 // epilogue warps, two per TMEM lane quadrant, each owning 128 of the tile's
@@ -108,6 +122,10 @@ template <int KIND, int TBN, int EW = 4>
 struct Cfg {
     static constexpr int RB = TBN / 128;  // 128-row blocks of B
     static constexpr bool SF_TMA = !(KIND == KIND_MXFP8 && TBN == 256 && EW == 4);
+#ifndef PMN_SF_ST  // scale factors into TMEM by tcgen05.st (four warps) instead of tcgen05.cp
+#define PMN_SF_ST 1
+#endif
+    static constexpr bool SF_ST = PMN_SF_ST && EW == 4 && KIND == KIND_NVFP4 && TBN == 256;
     // raw scale bytes per row and stage: NVFP4 needs 16; MXFP8 needs 4, which
     // never straddle a 16-byte box because every K start (M-grouped: 0,
     // K-grouped: expert segments aligned to 128) is a multiple of 128
@@ -115,7 +133,7 @@ struct Cfg {
     static constexpr int B_TILE_BYTES = TBN * 128;
     static constexpr int RAW_A = 128 * RAW_W, RAW_B = TBN * RAW_W;
     static constexpr int SFT_CHUNKS = KIND == KIND_NVFP4 ? 4 : 1;  // K-step chunks per stage
-    static constexpr int SFT_A = 512 * SFT_CHUNKS, SFT_B = 512 * SFT_CHUNKS * RB;
+    static constexpr int SFT_A = SF_ST ? 0 : 512 * SFT_CHUNKS, SFT_B = SF_ST ? 0 : 512 * SFT_CHUNKS * RB;
     static constexpr int SFT_OFF = A_TILE_BYTES + B_TILE_BYTES + RAW_A + RAW_B;  // re-laid chunks in a stage
     static constexpr int STAGE_RAW = SFT_OFF + SFT_A + SFT_B;
     static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
@@ -129,7 +147,9 @@ struct Cfg {
                                   : TBN == 256 ? (KIND == KIND_MXFP8 ? PMN_W256_MX_STAGES : 3)
                                                : (KIND == KIND_MXFP8 ? PMN_GEMM_STAGES_MXFP8 : PMN_GEMM_STAGES);
     static constexpr int EPI = EW == 8 ? 1 : TBN == 256 ? (STAGES == 4 ? 1 : 2) : EPI_BUFS;  // staging buffers per warp
-    static constexpr int THREADS = 128 + 32 * EW;  // warps 0..3: producer, MMA, scale factors; then EW epilogue warps
+    // warps 0..3: producer, MMA, scale factors; then EW epilogue warps; then
+    // (SF_ST) the scale-factor warps of sub-partitions 0 and 1
+    static constexpr int THREADS = 128 + 32 * EW + (SF_ST ? 64 : 0);
     static constexpr int ACC = TBN == 256 ? 1 : 2;
     static constexpr uint32_t SF_COL0 = ACC * TBN;  // scale factors live after the accumulators
     static constexpr uint32_t SFA_COLS = 4 * SFT_CHUNKS, SFB_COLS = 4 * SFT_CHUNKS * RB;
@@ -279,7 +299,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
-            mbar_init(bar_sfr + 8 * s, 1);
+            mbar_init(bar_sfr + 8 * s, C::SF_ST ? 4 : 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_acc_full + 8 * b, 1);
@@ -384,15 +404,52 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
             for (int s = 0; s < STAGES; ++s)
                 if (issued & (1u << s)) (void)mbar_wait(bar_full + 8 * s, (last_parity >> s) & 1u, 1000000000ull);
         }
-    } else if (warp == 2 || warp == 3) {
+    } else if (warp == 2 || warp == 3 || (C::SF_ST && warp >= 4 + EW)) {
         // ---------------------------------------------------- scale factors
-        // A stage's scale factors are written into the 32 x 128-bit chunks
-        // tcgen05.cp expects (chunk c, 16-byte line r0 = the scale words of
-        // rows r0, r0+32, r0+64, r0+96); then sf_ready.
+        // A stage's scale words, 4-column block by block: block (operand
+        // block blk = A or 128-row block h of B, K-step chunk c), lane r0,
+        // column r1 = the scale word of row r0 + 32 r1.  SF_ST: each of the
+        // four warps writes them into its own TMEM sub-partition and arrives
+        // on sf_ready after its stores complete.  Otherwise they are written
+        // as 32 x 128-bit chunks to shared memory, copied by tcgen05.cp, and
+        // the copies' commit is sf_ready.
+        const uint32_t tq = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        auto sf_put = [&](uint32_t stage, int blk, int c, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+            const int chunk = blk == 0 ? c : c * C::RB + (blk - 1);  // block index within its operand
+            if constexpr (C::SF_ST) {
+                const uint32_t col = C::SF_COL0 + stage * C::SF_COLS_STAGE + (blk == 0 ? 0u : C::SFA_COLS) + 4 * chunk;
+                tmem_st_32x32b_x4(tq + col, w0, w1, w2, w3);
+            } else {
+                uint8_t *sft = stages + stage * C::STAGE_BYTES + C::SFT_OFF + (blk == 0 ? 0 : C::SFT_A);
+                *reinterpret_cast<uint4 *>(sft + chunk * 512 + lane * 16) = make_uint4(w0, w1, w2, w3);
+            }
+        };
+        auto sf_done = [&](uint32_t stage, int seq) {
+            if constexpr (C::SF_ST) {
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (warp == 2) PMN_TRACE_POINT(2, seq);  // one sub-partition's arrival
+                    mbar_arrive(bar_sfr + 8 * stage);
+                }
+            } else {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    PMN_TRACE_POINT(2, seq);
+                    tc_fence_after();
+                    sf_to_tmem<KIND, TBN, EW>(stages, stage, tmem);
+                    tc_commit(bar_sfr + 8 * stage);  // sf_ready once the copies land
+                }
+            }
+        };
+        // without SF_ST, warp 2 takes the even stages of the sequence, warp 3
+        // the odd ones; with it, every warp takes every stage
+        constexpr uint32_t NSPLIT = C::SF_ST ? 1u : 2u;
+        const uint32_t mine = C::SF_ST ? 0u : (uint32_t)(warp - 2);
         if constexpr (C::SF_TMA) {
             // Raw rows arrive with the stage's TMA data: wait for it, re-lay.
-            // Warp 2 owns the even stage slots, warp 3 the odd ones.
-            const uint32_t mine = (uint32_t)(warp - 2);
             constexpr int raw_w = 16;
             uint32_t stage = 0, phase = 0;
             bool ok = true;
@@ -401,7 +458,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
                 const Tile ti = get_tile<KIND, TBN>(t, p, s_cum, gc);
                 for (int ks = 0; ks < ti.nks; ++ks) {
                     const int seq = n_seq++;
-                    if ((stage & 1u) != mine) {
+                    if (NSPLIT == 2u && (stage & 1u) != mine) {
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1;
@@ -417,17 +474,13 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
                         ok = false;
                         break;
                     }
-                    if (lane == 0) PMN_TRACE_POINT(1, seq);
+                    if (lane == 0 && (!C::SF_ST || warp == 2)) PMN_TRACE_POINT(1, seq);
                     uint8_t *st = stages + stage * C::STAGE_BYTES;
                     const uint8_t *rawA = st + A_TILE_BYTES + C::B_TILE_BYTES, *rawB = rawA + C::RAW_A;
-                    uint8_t *sftA = st + C::SFT_OFF, *sftB = sftA + C::SFT_A;
-                    // operand op, 128-row block h: chunks at sft + (c * blocks + h) * 512
 #pragma unroll
                     for (int blk = 0; blk < 1 + C::RB; ++blk) {
                         const int op = blk == 0 ? 0 : 1, h = blk == 0 ? 0 : blk - 1;
                         const uint8_t *raw = (op ? rawB : rawA) + h * 128 * raw_w;
-                        uint8_t *sft = (op ? sftB : sftA) + h * 512;
-                        const int cstride = (op ? C::RB : 1) * 512;
                         if (KIND == KIND_NVFP4) {
                             uint4 w[4];
 #pragma unroll
@@ -435,8 +488,8 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
                                 w[j] = *reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * 16);
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
-                                *reinterpret_cast<uint4 *>(sft + c * cstride + lane * 16) =
-                                    make_uint4(u4_word(w[0], c), u4_word(w[1], c), u4_word(w[2], c), u4_word(w[3], c));
+                                sf_put(stage, blk, c, u4_word(w[0], c), u4_word(w[1], c), u4_word(w[2], c),
+                                       u4_word(w[3], c));
                         } else {
                             // the stage's 4 scale bytes: word ((k0 / 32) % 16) / 4 of the raw row
                             const int64_t k0 = ti.kb + (int64_t)ks * 128;
@@ -445,17 +498,10 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
                                 v[j] = u4_word(*reinterpret_cast<const uint4 *>(raw + (lane + 32 * j) * raw_w), wsel);
-                            *reinterpret_cast<uint4 *>(sft + lane * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+                            sf_put(stage, blk, 0, v[0], v[1], v[2], v[3]);
                         }
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        PMN_TRACE_POINT(2, seq);
-                        tc_fence_after();
-                        sf_to_tmem<KIND, TBN, EW>(stages, stage, tmem);
-                        tc_commit(bar_sfr + 8 * stage);  // sf_ready once the copies land
-                    }
+                    sf_done(stage, seq);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -464,10 +510,8 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
             }
         } else {
             // Rows are read straight from global memory (four per lane and
-            // operand block).  Warp 2 takes the even stages of the sequence,
-            // warp 3 the odd ones; a warp's loads run two of its stages ahead
-            // of the stage it writes, so their latency overlaps the waits.
-            const uint32_t mine = (uint32_t)(warp - 2);
+            // operand block); a warp's loads run two of its stages ahead of
+            // the stage it writes, so their latency overlaps the waits.
             constexpr int W = KIND == KIND_NVFP4 ? 4 : 1;  // scale words per row and stage
             constexpr int NR = 4 * (1 + C::RB);  // scale rows one lane fetches
             struct It {
@@ -527,11 +571,12 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
                 valid = f.t < total;
                 seq = fseq;
                 if (valid) fetch(f, v);
-                ++f.ks;
-                settle(f);
-                ++f.ks;
-                settle(f);
-                fseq += 2;
+#pragma unroll
+                for (uint32_t u = 0; u < NSPLIT; ++u) {
+                    ++f.ks;
+                    settle(f);
+                }
+                fseq += NSPLIT;
             };
             bool ok = true;
             // write the stage held in `use` (fetched DEPTH - 1 turns earlier),
@@ -551,29 +596,16 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
                     ok = false;
                     return false;
                 }
-                if (lane == 0) PMN_TRACE_POINT(1, quse);
-                uint8_t *sftA = stages + stage * C::STAGE_BYTES + C::SFT_OFF;
-                uint8_t *sftB = sftA + C::SFT_A;
+                if (lane == 0 && (!C::SF_ST || warp == 2)) PMN_TRACE_POINT(1, quse);
 #pragma unroll
                 for (int blk = 0; blk < 1 + C::RB; ++blk) {
-                    // operand block: A, or 128-row block h of B; chunk c at
-                    // sft + (c * blocks + h) * 512
-                    uint8_t *sft = blk == 0 ? sftA : sftB + (blk - 1) * 512;
-                    const int cstride = (blk == 0 ? 1 : C::RB) * 512;
+                    // operand block: A, or 128-row block h of B
                     const int j0 = 4 * blk;
 #pragma unroll
                     for (int c = 0; c < C::SFT_CHUNKS; ++c)
-                        *reinterpret_cast<uint4 *>(sft + c * cstride + lane * 16) =
-                            make_uint4(use[j0][c], use[j0 + 1][c], use[j0 + 2][c], use[j0 + 3][c]);
+                        sf_put(stage, blk, c, use[j0][c], use[j0 + 1][c], use[j0 + 2][c], use[j0 + 3][c]);
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    PMN_TRACE_POINT(2, quse);
-                    tc_fence_after();
-                    sf_to_tmem<KIND, TBN, EW>(stages, stage, tmem);
-                    tc_commit(bar_sfr + 8 * stage);  // sf_ready once the copies land
-                }
+                sf_done(stage, (int)quse);
                 return true;
             };
             uint32_t s0[NR][W], s1[NR][W];
@@ -681,7 +713,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
             (void)mbar_wait(bar_drain, 0, 1000000000ull);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 4 + EW) {
         // ---------------------------------------------------- epilogue
         // Warp q owns accumulator lanes (rows) 32q .. 32q+31.  A slice whose
         // 32 rows are all valid is staged in shared memory (32 rows x 128 B,
