@@ -733,6 +733,11 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
         uint32_t nstore = 0;
         uint32_t abuf = 0, aphase = 0;
         int n_epi = 0, gc = 0;
+        // RHT: the block signs sigma (the same for every block) are folded into
+        // the expert scale, gbs[j] = (-1)^sigma_j * g_e: (acc * g_t) * gbs[j] is
+        // exactly the sign-flipped (acc * g_t) * g_e
+        const uint32_t sigma = OUT == PMN_OUT_RHT_S2F6 ? rht_sigma(p.seed) : 0u;
+        float gbs[OUT == PMN_OUT_RHT_S2F6 ? 32 : 1];
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const Tile ti = get_tile<KIND, TBN>(t, p, s_cum, gc);
             const int64_t row = ti.m0 + 32 * q + lane;
@@ -765,7 +770,10 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
             float scale = 1.0f;
             if (KIND == KIND_NVFP4 && valid) scale = p.a_outer[row];
             const float gb = KIND == KIND_NVFP4 ? p.b_outer[ti.g] : 1.0f;
-            const uint32_t sigma = OUT == PMN_OUT_RHT_S2F6 ? rht_sigma(p.seed) : 0u;
+            if constexpr (OUT == PMN_OUT_RHT_S2F6) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) gbs[j] = __uint_as_float(__float_as_uint(gb) ^ (((sigma >> j) & 1u) << 31));
+            }
             const int64_t obase = p.group_k ? (int64_t)ti.g * p.m : 0;
             const int64_t orow = obase + row;
             uint64_t sc_word = 0u;
@@ -785,7 +793,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     v[j] = __uint_as_float(r[j]);
-                    if (KIND == KIND_NVFP4) v[j] = __fmul_rn(__fmul_rn(v[j], scale), gb);
+                    if (KIND == KIND_NVFP4) v[j] = __fmul_rn(__fmul_rn(v[j], scale), OUT == PMN_OUT_RHT_S2F6 ? gbs[j] : gb);
                 }
                 if constexpr (OUT == PMN_OUT_F32) {
 #pragma unroll
@@ -802,13 +810,19 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) o[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                 } else {
-                    if (p.debug_acc != nullptr && valid) {  // the epilogue's input, before the transform
+                    if (p.debug_acc != nullptr && valid) {  // the epilogue's input (signs undone), before the transform
                         float4 *d4 = reinterpret_cast<float4 *>(p.debug_acc + orow * p.n + ti.n0 + 32 * c);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        for (int j = 0; j < 8; ++j) {
+                            float u[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                u[k] = __uint_as_float(__float_as_uint(v[4 * j + k]) ^ (((sigma >> (4 * j + k)) & 1u) << 31));
+                            d4[j] = make_float4(u[0], u[1], u[2], u[3]);
+                        }
                     }
                     uint32_t qv[8];
-                    const uint32_t sb = rht32_s2f6(v, sigma, qv);
+                    const uint32_t sb = rht32_s2f6_signed(v, qv);
                     o[0] = make_uint4(qv[0], qv[1], qv[2], qv[3]);
                     o[1] = make_uint4(qv[4], qv[5], qv[6], qv[7]);
                     sc_word |= (uint64_t)sb << (8 * c);

@@ -222,23 +222,49 @@ __device__ __forceinline__ uint4 sr_words16(uint64_t seed, uint32_t tag, uint64_
 // In-register 32-point randomised Hadamard transform and S2F6 block
 // quantisation [NVLink]: v = sigma . x; butterflies (a, b) -> (a + b, a - b)
 // for strides 1, 2, 4, 8, 16; z = v * RN(1/sqrt(32)); e = smallest exponent
-// with amax <= (127/64) 2^e; k = rint(z * 2^(6 - e)).  Returns the E8M0 byte
-// and writes 32 int8 codes packed little-endian into q[8].
-__device__ __forceinline__ uint32_t rht32_s2f6(float (&v)[32], uint32_t sigma, uint32_t (&q)[8])
+// with amax <= (127/64) 2^e; k = rint(z * 2^(6 - e)).  The block functions
+// return the E8M0 byte and write 32 int8 codes packed little-endian into q[8].
+
+// (a, b) -> (a + b, a - b) on two lanes at once (each lane rounded to nearest
+// even, exactly the scalar __fadd_rn / __fsub_rn).  Only for sums whose inputs
+// are themselves sums, so no product can be contracted into them.
+__device__ __forceinline__ void add_sub2(float &a0, float &a1, float &b0, float &b1)
+{
+    asm("{\n\t.reg .b64 a, b, s, d;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 b, {%2, %3};\n\t"
+        "add.rn.f32x2 s, a, b;\n\tsub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, s;\n\tmov.b64 {%2, %3}, d;\n\t}"
+        : "+f"(a0), "+f"(a1), "+f"(b0), "+f"(b1));
+}
+
+// RN(a * s + c) on two lanes.
+__device__ __forceinline__ void fma2(float a0, float a1, float s, float c, float &r0, float &r1)
+{
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %4};\n\tmov.b64 c, {%5, %5};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(s), "f"(c));
+}
+
+// The RHT-32 + S2F6 of a block whose signs sigma have already been applied:
+// butterflies, z = v * RN(1/sqrt(32)), e from max |z|, k = RNE(z * 2^(6-e)).
+// The exponent is chosen so that |z| * 2^(6-e) <= 127; the product by the
+// power of two is exact (or far below 1/2, where it is rounded once), so
+// RN(z * 2^(6-e) + 1.5 * 2^23) holds rint(z * 2^(6-e)) in its low mantissa
+// bits: its low byte is k's two's-complement byte.  A block at the clamped
+// exponent 127 (an amax of 2^127 or more, or not finite) takes the general
+// ldexp / convert / clamp path instead.
+__device__ __forceinline__ uint32_t rht32_s2f6_signed(float (&v)[32], uint32_t (&q)[8])
 {
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-        if ((sigma >> j) & 1u) v[j] = -v[j];
+    for (int i = 0; i < 32; i += 2) {  // stride 1: inputs may be products, scalar sums
+        const float a = v[i], b = v[i + 1];
+        v[i] = __fadd_rn(a, b);
+        v[i + 1] = __fsub_rn(a, b);
+    }
 #pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
+    for (int h = 2; h < 32; h <<= 1) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            if ((i & h) == 0) {
-                float a = v[i], b = v[i + h];
-                v[i] = __fadd_rn(a, b);
-                v[i + h] = __fsub_rn(a, b);
-            }
-        }
+        for (int i = 0; i < 32; i += 2)
+            if ((i & h) == 0) add_sub2(v[i], v[i + 1], v[i + h], v[i + h + 1]);
     }
     const float rs = __uint_as_float(0x3E3504F3u);  // RN(1/sqrt(32))
     float amax = 0.0f;
@@ -247,19 +273,46 @@ __device__ __forceinline__ uint32_t rht32_s2f6(float (&v)[32], uint32_t sigma, u
         v[j] = __fmul_rn(v[j], rs);
         amax = fmaxf(amax, fabsf(v[j]));
     }
-    int e = mx_exponent_s2f6(amax);
+    const int e = mx_exponent_s2f6(amax);
+    if (e < 127) {
+        int n = 6 - e;  // -120 .. 133
+        if (n > 127) {  // 2^n is not a binary32 value: scale by 2^64 first (exact: |v| < 2^-120)
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-        uint32_t packed = 0u;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            int k = __float2int_rn(ldexpf(v[4 * w + t], 6 - e));
-            k = k > 127 ? 127 : (k < -128 ? -128 : k);
-            packed |= ((uint32_t)k & 0xFFu) << (8 * t);
+            for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(v[j], 18446744073709551616.0f);
+            n -= 64;
         }
-        q[w] = packed;
+        const float sc = __uint_as_float((uint32_t)(n + 127) << 23), magic = 12582912.0f;  // 2^n, 1.5 * 2^23
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            float t[4];
+            fma2(v[4 * w], v[4 * w + 1], sc, magic, t[0], t[1]);
+            fma2(v[4 * w + 2], v[4 * w + 3], sc, magic, t[2], t[3]);
+            q[w] = __byte_perm(__byte_perm(__float_as_uint(t[0]), __float_as_uint(t[1]), 0x0040u),
+                               __byte_perm(__float_as_uint(t[2]), __float_as_uint(t[3]), 0x0040u), 0x5410u);
+        }
+    } else {
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            uint32_t packed = 0u;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                int k = __float2int_rn(ldexpf(v[4 * w + t], 6 - e));
+                k = k > 127 ? 127 : (k < -128 ? -128 : k);
+                packed |= ((uint32_t)k & 0xFFu) << (8 * t);
+            }
+            q[w] = packed;
+        }
     }
     return (uint32_t)(e + 127);
+}
+
+// In-register 32-point randomised Hadamard transform and S2F6 block
+// quantisation [NVLink] of x: v = sigma . x, then rht32_s2f6_signed.
+__device__ __forceinline__ uint32_t rht32_s2f6(float (&v)[32], uint32_t sigma, uint32_t (&q)[8])
+{
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(__float_as_uint(v[j]) ^ (((sigma >> j) & 1u) << 31));
+    return rht32_s2f6_signed(v, q);
 }
 
 __device__ __forceinline__ uint32_t rht_sigma(uint64_t seed)
