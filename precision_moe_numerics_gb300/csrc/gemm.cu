@@ -791,9 +791,18 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
             auto convert = [&](uint32_t (&r)[32], int c, uint4 (&o)[NCH]) {
                 float v[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    v[j] = __uint_as_float(r[j]);
-                    if (KIND == KIND_NVFP4) v[j] = __fmul_rn(__fmul_rn(v[j], scale), OUT == PMN_OUT_RHT_S2F6 ? gbs[j] : gb);
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                if constexpr (KIND == KIND_NVFP4 && OUT == PMN_OUT_RHT_S2F6) {
+                    // scalar: these products feed the butterfly sums
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__fmul_rn(v[j], scale), gbs[j]);
+                } else if constexpr (KIND == KIND_NVFP4) {
+                    // packed: these products are stored or converted, never summed
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        mul2(v[j], v[j + 1], scale, scale, v[j], v[j + 1]);
+                        mul2(v[j], v[j + 1], gb, gb, v[j], v[j + 1]);
+                    }
                 }
                 if constexpr (OUT == PMN_OUT_F32) {
 #pragma unroll
@@ -887,9 +896,10 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
                     tmem_ld_32x32b_x32(tbase + 32 * c, r);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float v0 = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * j]), scale), gb);
-                        const float v1 = __fmul_rn(__fmul_rn(__uint_as_float(r[2 * j + 1]), scale), gb);
+                    for (int j = 0; j < 16; ++j) {  // packed products feed only the bf16 conversion
+                        float v0, v1;
+                        mul2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]), scale, scale, v0, v1);
+                        mul2(v0, v1, gb, gb, v0, v1);
                         __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
                         yb[c][j] = *reinterpret_cast<uint32_t *>(&b2);
                     }

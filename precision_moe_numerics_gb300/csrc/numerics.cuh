@@ -225,6 +225,18 @@ __device__ __forceinline__ uint4 sr_words16(uint64_t seed, uint32_t tag, uint64_
 // with amax <= (127/64) 2^e; k = rint(z * 2^(6 - e)).  The block functions
 // return the E8M0 byte and write 32 int8 codes packed little-endian into q[8].
 
+// Packed binary32 product (each lane rounded to nearest even).  Used only
+// where the product feeds a conversion: measured on sm_103a, a packed multiply
+// whose result feeds a packed add is contracted into a fused multiply-add
+// despite the .rn modifiers, so sums of products stay on the scalar
+// intrinsics, which are never contracted.
+__device__ __forceinline__ void mul2(float a0, float a1, float b0, float b1, float &c0, float &c1)
+{
+    asm("{\n\t.reg .b64 a, b, c;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 c, a, b;\n\tmov.b64 {%0, %1}, c;\n\t}"
+        : "=f"(c0), "=f"(c1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // (a, b) -> (a + b, a - b) on two lanes at once (each lane rounded to nearest
 // even, exactly the scalar __fadd_rn / __fsub_rn).  Only for sums whose inputs
 // are themselves sums, so no product can be contracted into them.

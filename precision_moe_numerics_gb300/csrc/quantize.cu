@@ -100,18 +100,6 @@ __device__ __forceinline__ uint32_t block_scale_byte(float amax, float d, float 
     return cvt_e4m3(__fdiv_rn(amax, d));
 }
 
-// Packed binary32 product (each lane rounded to nearest even).  Used only
-// where the product feeds a conversion: measured on sm_103a, a packed multiply
-// whose result feeds a packed add is contracted into a fused multiply-add
-// despite the .rn modifiers, so sums of products stay on the scalar
-// intrinsics, which are never contracted.
-__device__ __forceinline__ void mul2(float a0, float a1, float b0, float b1, float &c0, float &c1)
-{
-    asm("{\n\t.reg .b64 a, b, c;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-        "mul.rn.f32x2 c, a, b;\n\tmov.b64 {%0, %1}, c;\n\t}"
-        : "=f"(c0), "=f"(c1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-
 __device__ __forceinline__ float quant_block_candidate(const float (&x)[16], float amax, float g, float d, float rd,
                                                        bool fast, bool want_err, BlockQ &out)
 {
