@@ -370,9 +370,10 @@ __global__ void __launch_bounds__(QG_THREADS, PMN_QG_MIN_BLOCKS) nvfp4_quant_gro
         bool stop = false;
         if (is_a) {
             {
-                // ---- A(g, c): max |x| over the chunk on bf16 bit patterns
+                // ---- A(g, c): max |x| over the chunk on bf16 bit patterns (the
+                // 8 blocks of a thread fully unrolled: measured 1 % faster than 4)
                 uint32_t m = 0u;
-#pragma unroll 4
+#pragma unroll 8
                 for (int64_t b = b0 + tid; b < b1; b += QG_THREADS) {
                     const uint4 *q = reinterpret_cast<const uint4 *>(xg + b * 16);
                     const uint4 v0 = ld_l2_policy(q, keep), v1 = ld_l2_policy(q + 1, keep);
