@@ -10,17 +10,20 @@
 // 4-bit forward", arex-research.com), plus the library's status strings,
 // device error word and bounded-wait limit.
 //
-// One persistent kernel per call, one CTA per SM, 8 warps:
+// One persistent kernel per call, one CTA per SM:
 //   warp 0      TMA producer: code tiles (128 rows x 128 bytes, 128-byte
 //               swizzle) and raw scale tiles into a 3- to 5-stage ring
-//   warps 2, 3  re-lay each stage's scale factors into the 32x128-bit form
-//               tcgen05.cp expects (even / odd stage slots), copy them into
-//               the stage's TMEM slot and commit to its sf_ready barrier
+//   scale-factor warps: put each stage's scale factors into its TMEM slot,
+//               then sf_ready.  256-wide NVFP4 tiles: warps 2, 3, 8, 9, one
+//               per TMEM sub-partition, tcgen05.st from the raw rows.
+//               Otherwise warps 2, 3 (even / odd stage slots) re-lay them
+//               into the 32x128-bit form tcgen05.cp expects and copy them.
 //   warp 1      one lane issues the MMAs of a stage once its scale factors
 //               are in TMEM, committing to the stage's empty barrier
-//   warps 4..7  epilogue: TMEM -> registers (one row per thread), outer
-//               scales, bf16/fp32, SwiGLU or RHT + S2F6, staged in shared
-//               memory and written by TMA tensor stores in full 128-byte lines
+//   warps 4..   epilogue (4, or 8 on the K-grouped fp32 tiles): TMEM ->
+//               registers (one row per thread), outer scales, bf16/fp32,
+//               SwiGLU or RHT + S2F6, staged in shared memory and written by
+//               TMA tensor stores in full 128-byte lines
 // 128-wide tiles hold two TMEM accumulators, so the epilogue of one tile
 // overlaps the main loop of the next; 256-wide tiles hold one and release it
 // as soon as it has been read.  Every wait is bounded: on timeout a device
