@@ -215,6 +215,25 @@ def test_rht_s2f6_quantize(pmn, shape):
         assert_same(q, rq, "codes")
 
 
+def test_rht_s2f6_extreme_blocks(pmn):
+    """Blocks whose exponent needs the 2^64 pre-scale (amax below 2^-121, down
+    into float32 subnormals) and blocks with an infinite value (the clamped
+    exponent 127 and its general path; one infinity per block spreads through
+    the butterflies without meeting another, so no NaN arises)."""
+    rng = np.random.default_rng(13)
+    rows = [rng.standard_normal(64) * 2.0 ** (-100 - r) for r in range(48)]
+    inf_row = rng.standard_normal(64)
+    inf_row[5], inf_row[40] = np.inf, -np.inf
+    rows += [inf_row, rng.standard_normal(64)]
+    x = np.stack(rows).astype(np.float32)
+    for seed in (0, 7):
+        q, sc = pmn.rht_s2f6_quantize(torch.from_numpy(x).cuda(), seed)
+        rq, rsc = oracle.rht_s2f6(x, seed)
+        assert_same(sc, rsc, "scales")
+        assert_same(q, rq, "codes")
+    assert (rsc[:48] < 127 - 121).any() and (rsc[48] == 254).all()  # both branches taken
+
+
 def test_quantize_deterministic(pmn):
     rng = np.random.default_rng(12)
     x = to_dev_bf16(W.normal_bf16_host(rng, (512, 4096)))
