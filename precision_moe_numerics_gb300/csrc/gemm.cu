@@ -1111,9 +1111,9 @@ pmn_status launch_gemm_tbn(const GemmMaps &ms, const CUtensorMap &o, const GemmA
 template <int KIND, int OUT>
 pmn_status launch_gemm(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
 {
-    // 256-wide M-grouped tiles except under the RHT + S2F6 epilogue, whose
-    // conversion is long enough that overlapping it with the next tile's MMAs
-    // (two 128-wide accumulators) beats the halved A traffic
+    // 256-wide M-grouped tiles except under the RHT + S2F6 epilogue on long
+    // segments, whose conversion is long enough that overlapping it with the
+    // next tile's MMAs (two 128-wide accumulators) beats the halved A traffic
     if constexpr (OUT == PMN_OUT_SWIGLU_BF16) {
         return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);
     } else if constexpr (KIND == KIND_MXFP8 && OUT == PMN_OUT_F32) {
@@ -1124,7 +1124,12 @@ pmn_status launch_gemm(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs 
             return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);
         return launch_gemm_tbn<KIND, OUT, 128>(ms, o, args, s);
     } else {
-        if (PMN_GEMM_WIDE_M && OUT != PMN_OUT_RHT_S2F6 && !args.group_k && args.n % 256 == 0)
+        // RHT + S2F6 on short segments (fewer than 64 rows per group on
+        // average, e.g. a decode batch): the epilogue has few rows to transform
+        // and the wide tile streams twice the weight bytes per stage (decode
+        // w2 GEMM 0.298 -> 0.265 ms); the bytes are the same at either width
+        const bool short_segments = args.m < 64 * (int64_t)args.groups;
+        if (PMN_GEMM_WIDE_M && (OUT != PMN_OUT_RHT_S2F6 || short_segments) && !args.group_k && args.n % 256 == 0)
             return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);
         return launch_gemm_tbn<KIND, OUT, 128>(ms, o, args, s);
     }

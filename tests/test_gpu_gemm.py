@@ -51,8 +51,8 @@ def check_bf16(got_bf16, ref, absab, what):
     assert not bad.any(), "%s: %d elements beyond one bf16 step" % (what, bad.sum())
 
 
-def moe_case(seed=0, tokens=256, experts=8, k=2, d=512, f=256):
-    m = W.small_moe(seed, tokens=tokens, experts=experts, k=k, d=d, f=f)
+def moe_case(seed=0, tokens=256, experts=8, k=2, d=512, f=256, pad=W.PAD):
+    m = W.small_moe(seed, tokens=tokens, experts=experts, k=k, d=d, f=f, pad=pad)
     r = m["routing"]
     xa = oracle.nvfp4_quantize(m["x"], oracle.OUTER_PER_ROW, four_over_six=True)
     E = experts
@@ -123,8 +123,11 @@ def test_grouped_gemm_nvfp4_edge_offsets(pmn):
     check_f32(out.cpu().numpy(), ref, absab, "edge offsets")
 
 
-def test_w2_gemm_rht_s2f6(pmn):
-    m, r, (ac, asc, ag), _ = moe_case()
+@pytest.mark.parametrize("tokens,pad", [(256, W.PAD), (16, 1)])
+def test_w2_gemm_rht_s2f6(pmn, tokens, pad):
+    """128-row expert segments (128-wide tiles), and a decode-like batch of
+    unpadded segments of a few rows (the library then takes 256-wide tiles)."""
+    m, r, (ac, asc, ag), _ = moe_case(tokens=tokens, pad=pad)
     E, d, f = 8, 512, 256
     w2 = m["w2"].reshape(E * d, f)
     hq = oracle.nvfp4_quantize(W.normal_bf16_host(np.random.default_rng(9), (r.rows, f)), oracle.OUTER_PER_ROW,
