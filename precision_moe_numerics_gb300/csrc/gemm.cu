@@ -88,7 +88,6 @@ constexpr int BN_MIN = 128;  // N-tiles are 128 or 256 columns
 #endif
 constexpr int EPI_BUFS = PMN_EPI_BUFS;      // epilogue staging buffers per warp
 constexpr int STAGE_OUT_BYTES = 32 * 128;  // one epilogue staging buffer: 32 rows x 128 bytes
-constexpr int A_TILE_BYTES = BM * 128;     // A stage tile: 128 rows x 128 bytes of K
 constexpr int MAX_GROUPS = PMN_MAX_GROUPS;
 constexpr uint32_t TMEM_COLS = 512;
 
@@ -121,7 +120,7 @@ constexpr uint32_t TMEM_COLS = 512;
 // 256 columns, so a thread holds its whole half-row of fp32 accumulators in
 // registers and the single accumulator is released after four chunk reads.
 // Their scale rows come by TMA (K-grouped rows are token ranges apart).
-template <int KIND, int TBN, int EW = 4>
+template <int KIND, int TBN, int EW = 4, bool SHORT = false>
 struct Cfg {
     static constexpr int RB = TBN / 128;  // 128-row blocks of B
     static constexpr bool SF_TMA = !(KIND == KIND_MXFP8 && TBN == 256 && EW == 4);
@@ -129,15 +128,24 @@ struct Cfg {
 #define PMN_SF_ST 1
 #endif
     static constexpr bool SF_ST = PMN_SF_ST && EW == 4 && KIND == KIND_NVFP4 && TBN == 256;
+    // SHORT (M-grouped problems whose segments are a few rows, e.g. a decode
+    // batch): a tile covers 32 rows of one segment and only those 32 rows of A
+    // (and their scales) are loaded.  The MMA still reads 128 rows of A from
+    // the stage; rows 32..127 come from whatever follows in the stage and give
+    // accumulator rows that are never stored.  The epilogue stores its rows
+    // directly (no staging buffers), so a stage of mostly weight bytes fits
+    // five times (256-wide) or eight times (128-wide).
+    static constexpr int AM = SHORT ? 32 : BM;  // rows of A per tile (and per stage load)
+    static constexpr int A_BYTES = AM * 128;
     // raw scale bytes per row and stage: NVFP4 needs 16; MXFP8 needs 4, which
     // never straddle a 16-byte box because every K start (M-grouped: 0,
     // K-grouped: expert segments aligned to 128) is a multiple of 128
     static constexpr int RAW_W = !SF_TMA ? 0 : 16;
     static constexpr int B_TILE_BYTES = TBN * 128;
-    static constexpr int RAW_A = 128 * RAW_W, RAW_B = TBN * RAW_W;
+    static constexpr int RAW_A = AM * RAW_W, RAW_B = TBN * RAW_W;
     static constexpr int SFT_CHUNKS = KIND == KIND_NVFP4 ? 4 : 1;  // K-step chunks per stage
     static constexpr int SFT_A = SF_ST ? 0 : 512 * SFT_CHUNKS, SFT_B = SF_ST ? 0 : 512 * SFT_CHUNKS * RB;
-    static constexpr int SFT_OFF = A_TILE_BYTES + B_TILE_BYTES + RAW_A + RAW_B;  // re-laid chunks in a stage
+    static constexpr int SFT_OFF = A_BYTES + B_TILE_BYTES + RAW_A + RAW_B;  // re-laid chunks in a stage
     static constexpr int STAGE_RAW = SFT_OFF + SFT_A + SFT_B;
     static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
 #ifndef PMN_W256_MX_STAGES  // 256-wide MXFP8 tiles: 4 stages with one epilogue staging buffer per warp
@@ -146,10 +154,13 @@ struct Cfg {
 #ifndef PMN_KG256_STAGES  // 256-wide K-grouped tiles (EW = 8)
 #define PMN_KG256_STAGES 3
 #endif
-    static constexpr int STAGES = EW == 8 ? PMN_KG256_STAGES
+    static constexpr bool DIRECT = SHORT;  // epilogue rows stored straight to global memory
+    static constexpr int STAGES = SHORT ? (TBN == 256 ? 5 : 8)
+                                  : EW == 8 ? PMN_KG256_STAGES
                                   : TBN == 256 ? (KIND == KIND_MXFP8 ? PMN_W256_MX_STAGES : 3)
                                                : (KIND == KIND_MXFP8 ? PMN_GEMM_STAGES_MXFP8 : PMN_GEMM_STAGES);
-    static constexpr int EPI = EW == 8 ? 1 : TBN == 256 ? (STAGES == 4 ? 1 : 2) : EPI_BUFS;  // staging buffers per warp
+    static constexpr int EPI = DIRECT ? 0 : EW == 8 ? 1 : TBN == 256 ? (STAGES == 4 ? 1 : 2) : EPI_BUFS;  // staging buffers per warp
+    static_assert(!SHORT || (KIND == KIND_NVFP4 && EW == 4 && SF_TMA && B_TILE_BYTES >= 96 * 128), "short tiles: NVFP4");
     // warps 0..3: producer, MMA, scale factors; then EW epilogue warps; then
     // (SF_ST) the scale-factor warps of sub-partitions 0 and 1
     static constexpr int THREADS = 128 + 32 * EW + (SF_ST ? 64 : 0);
@@ -206,7 +217,7 @@ __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id)
 // role walks its tiles in increasing order, so the group of t is found by
 // stepping forward from the group of the previous lookup (a few shared-memory
 // reads, against a binary search on the critical path between tiles).
-template <int KIND, int TBN>
+template <int KIND, int TBN, int AM = BM>
 __device__ __forceinline__ Tile get_tile(int t, const GemmArgs &p, const int *s_cum, int &gc)
 {
     int lo = gc;
@@ -219,9 +230,10 @@ __device__ __forceinline__ Tile get_tile(int t, const GemmArgs &p, const int *s_
     if (!p.group_k) {
         const int nt = (int)(p.n / TBN);
         const int mi = local / nt, ni = local - mi * nt;  // consecutive tiles: adjacent N-tiles
-        ti.m0 = __ldg(p.offsets + lo) + (int64_t)mi * BM;
+        ti.m0 = __ldg(p.offsets + lo) + (int64_t)mi * AM;
         ti.n0 = (int64_t)ni * TBN;
         ti.row_end = __ldg(p.offsets + lo + 1);
+        if (AM < BM) ti.row_end = min(ti.row_end, ti.m0 + AM);  // rows past the loaded ones are not stored
         ti.kb = 0;
         ti.ke = p.k;
     } else {
@@ -244,10 +256,9 @@ __device__ __forceinline__ void latch_error(int bit) { atomicOr(&g_pmn_device_er
 // Copies a stage's re-laid scale-factor chunks from shared memory into the
 // stage's TMEM columns (A: one 32x128b.warpx4 copy per K-step; B: one per
 // K-step and 128-row block).  Issued by one thread, which then commits.
-template <int KIND, int TBN, int EW>
+template <class C>
 __device__ __forceinline__ void sf_to_tmem(uint8_t *stages, uint32_t stg, uint32_t tmem)
 {
-    using C = Cfg<KIND, TBN, EW>;
     const uint8_t *sftA = stages + stg * C::STAGE_BYTES + C::SFT_OFF;
     const uint8_t *sftB = sftA + C::SFT_A;
     const uint32_t sfa = tmem + C::SF_COL0 + stg * C::SF_COLS_STAGE;
@@ -270,13 +281,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
     return __all_sync(0xFFFFFFFFu, ok) != 0;
 }
 
-template <int KIND, int OUT, int TBN, int EW>
-__global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
+template <int KIND, int OUT, int TBN, int EW, bool SHORT>
+__global__ void __launch_bounds__(Cfg<KIND, TBN, EW, SHORT>::THREADS, 1)
     block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                              const __grid_constant__ CUtensorMap tmO, const GemmArgs p)
 {
-    using C = Cfg<KIND, TBN, EW>;
+    using C = Cfg<KIND, TBN, EW, SHORT>;
     constexpr int STAGES = C::STAGES;
     constexpr bool SWI = OUT == PMN_OUT_SWIGLU_BF16;
     static_assert(EW == 4 || (EW == 8 && OUT == PMN_OUT_F32 && TBN == 256), "eight epilogue warps: fp32, 256-wide");
@@ -343,7 +354,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
             s_cum[gi] = cum;
             if (!p.group_k) {
                 int rows = p.offsets[gi + 1] - p.offsets[gi];
-                cum += ((rows + BM - 1) / BM) * (int)(p.n / TBN);
+                cum += ((rows + C::AM - 1) / C::AM) * (int)(p.n / TBN);
             } else {
                 cum += (int)(p.m / BM) * (int)(p.n / TBN);
             }
@@ -365,7 +376,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
             uint32_t issued = 0, last_parity = 0;
             int n_issued = 0, gc = 0;
             for (int t = blockIdx.x; t < total && !*(volatile int *)s_abort; t += gridDim.x) {
-                const Tile ti = get_tile<KIND, TBN>(t, p, s_cum, gc);
+                const Tile ti = get_tile<KIND, TBN, C::AM>(t, p, s_cum, gc);
                 // SwiGLU tiles: h columns n0/2 .. n0/2 + 127 need the expert's gate
                 // rows n0/2 + (0..127) and up rows n/2 + n0/2 + (0..127) of B, loaded
                 // as two 128-row boxes into the B tile's two halves
@@ -381,17 +392,17 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
                     ++n_issued;
                     uint8_t *st = stages + stage * C::STAGE_BYTES;
                     const uint32_t fb = bar_full + 8 * stage;
-                    mbar_arrive_expect_tx(fb, A_TILE_BYTES + C::B_TILE_BYTES + (C::SF_TMA ? (128u + TBN) * 16u : 0u));
+                    mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_TILE_BYTES + (C::SF_TMA ? (uint32_t)(C::AM + TBN) * 16u : 0u));
                     // 128 bytes of K per stage: 256 fp4 or 128 fp8 values
                     const int32_t xk = (int32_t)(KIND == KIND_NVFP4 ? (int64_t)ks * 128 : ti.kb + (int64_t)ks * 128);
                     tma_load_2d(smem_u32(st), &tmA, fb, xk, (int32_t)ti.m0);
-                    tma_load_2d(smem_u32(st + A_TILE_BYTES), &tmB, fb, xk, (int32_t)brow);
-                    if (SWI) tma_load_2d(smem_u32(st + A_TILE_BYTES + 128 * 128), &tmB, fb, xk, (int32_t)brow_up);
+                    tma_load_2d(smem_u32(st + C::A_BYTES), &tmB, fb, xk, (int32_t)brow);
+                    if (SWI) tma_load_2d(smem_u32(st + C::A_BYTES + 128 * 128), &tmB, fb, xk, (int32_t)brow_up);
                     if (C::SF_TMA) {
                         // raw scale rows: 16-byte boxes (the MXFP8 stage's 4 bytes at (xk / 32) % 16)
                         const int32_t xs = KIND == KIND_NVFP4 ? ks * 16 : (int32_t)((xk / 32) & ~int32_t(15));
-                        const uint32_t rb = smem_u32(st + A_TILE_BYTES + C::B_TILE_BYTES + C::RAW_A);
-                        tma_load_2d(smem_u32(st + A_TILE_BYTES + C::B_TILE_BYTES), &tmSA, fb, xs, (int32_t)ti.m0);
+                        const uint32_t rb = smem_u32(st + C::A_BYTES + C::B_TILE_BYTES + C::RAW_A);
+                        tma_load_2d(smem_u32(st + C::A_BYTES + C::B_TILE_BYTES), &tmSA, fb, xs, (int32_t)ti.m0);
                         tma_load_2d(rb, &tmSB, fb, xs, (int32_t)brow);
                         if (SWI) tma_load_2d(rb + 128 * 16, &tmSB, fb, xs, (int32_t)brow_up);
                     }
@@ -442,7 +453,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
                 if (lane == 0) {
                     PMN_TRACE_POINT(2, seq);
                     tc_fence_after();
-                    sf_to_tmem<KIND, TBN, EW>(stages, stage, tmem);
+                    sf_to_tmem<C>(stages, stage, tmem);  // the kernel's own layout
                     tc_commit(bar_sfr + 8 * stage);  // sf_ready once the copies land
                 }
             }
@@ -458,7 +469,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
             bool ok = true;
             int n_seq = 0, gc = 0;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile ti = get_tile<KIND, TBN>(t, p, s_cum, gc);
+                const Tile ti = get_tile<KIND, TBN, C::AM>(t, p, s_cum, gc);
                 for (int ks = 0; ks < ti.nks; ++ks) {
                     const int seq = n_seq++;
                     if (NSPLIT == 2u && (stage & 1u) != mine) {
@@ -479,7 +490,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
                     }
                     if (lane == 0 && (!C::SF_ST || warp == 2)) PMN_TRACE_POINT(1, seq);
                     uint8_t *st = stages + stage * C::STAGE_BYTES;
-                    const uint8_t *rawA = st + A_TILE_BYTES + C::B_TILE_BYTES, *rawB = rawA + C::RAW_A;
+                    const uint8_t *rawA = st + C::A_BYTES + C::B_TILE_BYTES, *rawB = rawA + C::RAW_A;
 #pragma unroll
                     for (int blk = 0; blk < 1 + C::RB; ++blk) {
                         const int op = blk == 0 ? 0 : 1, h = blk == 0 ? 0 : blk - 1;
@@ -525,7 +536,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
                 while (it.t < total && it.ks >= it.ti.nks) {
                     it.t += gridDim.x;
                     it.ks = 0;
-                    if (it.t < total) it.ti = get_tile<KIND, TBN>(it.t, p, s_cum, it.gc);
+                    if (it.t < total) it.ti = get_tile<KIND, TBN, C::AM>(it.t, p, s_cum, it.gc);
                 }
             };
             auto fetch = [&](const It &it, uint32_t (&v)[NR][W]) {
@@ -562,7 +573,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
             };
             // stages of this warp, in order: f is the next one to fetch
             It f{(int)blockIdx.x, 0, 0, Tile{}};
-            if (f.t < total) f.ti = get_tile<KIND, TBN>(f.t, p, s_cum, f.gc);
+            if (f.t < total) f.ti = get_tile<KIND, TBN, C::AM>(f.t, p, s_cum, f.gc);
             settle(f);
             uint32_t fseq = 0;
             if (mine) {
@@ -640,7 +651,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
             int gc = 0;
             auto next_tile = [&](int t0, Tile &out) {
                 for (int tt = t0; tt < total; tt += gridDim.x) {
-                    out = get_tile<KIND, TBN>(tt, p, s_cum, gc);
+                    out = get_tile<KIND, TBN, C::AM>(tt, p, s_cum, gc);
                     if (out.nks > 0) return tt;
                 }
                 return total;
@@ -676,7 +687,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
                     uint8_t *st = stages + stage * C::STAGE_BYTES;
                     const uint32_t sfa = tmem + C::SF_COL0 + stage * C::SF_COLS_STAGE;
                     const uint32_t sfb = sfa + C::SFA_COLS;
-                    const uint32_t a_addr = smem_u32(st), b_addr = smem_u32(st + A_TILE_BYTES);
+                    const uint32_t a_addr = smem_u32(st), b_addr = smem_u32(st + C::A_BYTES);
                     int nk = 4;
                     if (KIND == KIND_MXFP8) {
                         const int64_t left = ti.ke - (ti.kb + (int64_t)ks * 128);
@@ -742,7 +753,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
         const uint32_t sigma = OUT == PMN_OUT_RHT_S2F6 ? rht_sigma(p.seed) : 0u;
         float gbs[OUT == PMN_OUT_RHT_S2F6 ? 32 : 1];
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const Tile ti = get_tile<KIND, TBN>(t, p, s_cum, gc);
+            const Tile ti = get_tile<KIND, TBN, C::AM>(t, p, s_cum, gc);
             const int64_t row = ti.m0 + 32 * q + lane;
             const bool valid = row < ti.row_end;
             if (ti.nks == 0) {
@@ -850,10 +861,10 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW>::THREADS, 1)
             };
             auto store = [&](int c, const uint4 (&o)[NCH]) {
                 const int part = c % CH_PER_STORE;
-                if (slice_full) {
+                if (!C::DIRECT && slice_full) {
                     uint8_t *buf = stg + (nstore % C::EPI) * STAGE_OUT_BYTES;
                     if (part == 0) {
-                        if (lane == 0) bulk_wait_group_read<C::EPI - 1>();  // this buffer's last store has read it
+                        if (lane == 0) bulk_wait_group_read<(C::EPI > 0 ? C::EPI - 1 : 0)>();  // this buffer's last store has read it
                         __syncwarp();
                     }
 #pragma unroll
@@ -1075,17 +1086,20 @@ struct GemmMaps {
 #ifndef PMN_GEMM_WIDE_M  // 256-wide tiles for M-grouped problems
 #define PMN_GEMM_WIDE_M 1
 #endif
+#ifndef PMN_GEMM_SHORT  // 32-row tiles for NVFP4 problems of a few rows per group
+#define PMN_GEMM_SHORT 1
+#endif
 
-template <int KIND, int OUT, int TBN, int EW = 4>
+template <int KIND, int OUT, int TBN, int EW = 4, bool SHORT = false>
 pmn_status launch_gemm_tbn(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs &args, cudaStream_t s)
 {
-    using C = Cfg<KIND, TBN, EW>;
+    using C = Cfg<KIND, TBN, EW, SHORT>;
     CUtensorMap a, b, sa, sb;
     const uint32_t raw_w = 16;  // raw scale rows: one 16-byte box per row and stage
     const uint32_t b_box = OUT == PMN_OUT_SWIGLU_BF16 ? 128 : TBN;  // SwiGLU: gate and up halves load separately
-    if (!make_map(&a, ms.a.base, ms.a.width_bytes, ms.a.rows, ms.a.pitch, 128, true, BM) ||
+    if (!make_map(&a, ms.a.base, ms.a.width_bytes, ms.a.rows, ms.a.pitch, 128, true, C::AM) ||
         !make_map(&b, ms.b.base, ms.b.width_bytes, ms.b.rows, ms.b.pitch, 128, true, b_box) ||
-        !make_map(&sa, ms.sa.base, ms.sa.width_bytes, ms.sa.rows, ms.sa.pitch, raw_w, false, BM) ||
+        !make_map(&sa, ms.sa.base, ms.sa.width_bytes, ms.sa.rows, ms.sa.pitch, raw_w, false, C::AM) ||
         !make_map(&sb, ms.sb.base, ms.sb.width_bytes, ms.sb.rows, ms.sb.pitch, raw_w, false, b_box))
         return PMN_ERR_CUDA;
     GemmArgs ka = args;  // for scale-factor warps that read global memory
@@ -1094,7 +1108,7 @@ pmn_status launch_gemm_tbn(const GemmMaps &ms, const CUtensorMap &o, const GemmA
     ka.sb = static_cast<const uint8_t *>(ms.sb.base);
     ka.sa_pitch = (int64_t)ms.sa.pitch;
     ka.sb_pitch = (int64_t)ms.sb.pitch;
-    auto kern = block_scaled_gemm_kernel<KIND, OUT, TBN, EW>;
+    auto kern = block_scaled_gemm_kernel<KIND, OUT, TBN, EW, SHORT>;
     const int smem = C::SMEM_BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return PMN_ERR_CUDA;
@@ -1114,7 +1128,11 @@ pmn_status launch_gemm(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs 
     // 256-wide M-grouped tiles except under the RHT + S2F6 epilogue on long
     // segments, whose conversion is long enough that overlapping it with the
     // next tile's MMAs (two 128-wide accumulators) beats the halved A traffic
+    // NVFP4 M-grouped problems of a few rows per group (16 or fewer on
+    // average, e.g. a decode batch): 32-row tiles (Cfg SHORT)
+    const bool tiny_segments = KIND == KIND_NVFP4 && !args.group_k && args.m <= 16 * (int64_t)args.groups;
     if constexpr (OUT == PMN_OUT_SWIGLU_BF16) {
+        if (PMN_GEMM_SHORT && tiny_segments) return launch_gemm_tbn<KIND, OUT, 256, 4, true>(ms, o, args, s);
         return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);
     } else if constexpr (KIND == KIND_MXFP8 && OUT == PMN_OUT_F32) {
         // K-grouped weight gradients: 256-wide tiles with eight epilogue warps
@@ -1129,8 +1147,16 @@ pmn_status launch_gemm(const GemmMaps &ms, const CUtensorMap &o, const GemmArgs 
         // and the wide tile streams twice the weight bytes per stage (decode
         // w2 GEMM 0.298 -> 0.265 ms); the bytes are the same at either width
         const bool short_segments = args.m < 64 * (int64_t)args.groups;
-        if (PMN_GEMM_WIDE_M && (OUT != PMN_OUT_RHT_S2F6 || short_segments) && !args.group_k && args.n % 256 == 0)
+        if constexpr (KIND == KIND_NVFP4 && OUT == PMN_OUT_RHT_S2F6) {
+            // 32-row tiles keep two 128-wide accumulators here: only one warp
+            // holds the tile's rows, and its RHT overlaps the next tile's MMAs
+            if (PMN_GEMM_SHORT && tiny_segments) return launch_gemm_tbn<KIND, OUT, 128, 4, true>(ms, o, args, s);
+        }
+        if (PMN_GEMM_WIDE_M && (OUT != PMN_OUT_RHT_S2F6 || short_segments) && !args.group_k && args.n % 256 == 0) {
+            if constexpr (KIND == KIND_NVFP4 && OUT != PMN_OUT_RHT_S2F6)
+                if (PMN_GEMM_SHORT && tiny_segments) return launch_gemm_tbn<KIND, OUT, 256, 4, true>(ms, o, args, s);
             return launch_gemm_tbn<KIND, OUT, 256>(ms, o, args, s);
+        }
         return launch_gemm_tbn<KIND, OUT, 128>(ms, o, args, s);
     }
 }

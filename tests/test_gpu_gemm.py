@@ -123,6 +123,31 @@ def test_grouped_gemm_nvfp4_edge_offsets(pmn):
     check_f32(out.cpu().numpy(), ref, absab, "edge offsets")
 
 
+def test_grouped_nvfp4_gemm_short_segments(pmn):
+    """16 or fewer rows per expert on average (the library's 32-row tiles):
+    empty experts, segments of 1..5 rows, and 33- and 70-row segments that
+    span several 32-row tiles; fp32 and bf16 outputs"""
+    rng = np.random.default_rng(44)
+    n, k = 512, 256
+    counts = np.array([1, 2, 0, 70, 3, 0, 5, 1, 0, 2, 33, 4])
+    E = len(counts)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    T = int(offs[-1])
+    assert T <= 16 * E
+    a = oracle.nvfp4_quantize(W.normal_bf16_host(rng, (T, k), 1.0, 0.01, 30.0), oracle.OUTER_PER_ROW,
+                              four_over_six=True)
+    bq = oracle.nvfp4_quantize(W.normal_bf16_host(rng, (E * n, k), 0.02), oracle.OUTER_PER_GROUP,
+                               group_offsets=np.arange(E + 1) * n)
+    bc, bsc, bg = bq[0].reshape(E, n, k // 2), bq[1].reshape(E, n, k // 16), bq[2]
+    ref = oracle.grouped_gemm_nvfp4(*a, bc, bsc, bg, offs)
+    absab = abs_product(*a, bc, bsc, bg, offs)
+    A, B = tuple(dev(t) for t in a), (dev(bc), dev(bsc), dev(bg))
+    out = pmn.grouped_gemm_nvfp4(A, B, dev(offs), out_dtype=torch.float32)
+    check_f32(out.cpu().numpy(), ref, absab, "short segments, fp32")
+    outb = pmn.grouped_gemm_nvfp4(A, B, dev(offs), out_dtype=torch.bfloat16)
+    check_bf16(outb.view(torch.int16).cpu().numpy(), ref, absab, "short segments, bf16")
+
+
 @pytest.mark.parametrize("tokens,pad", [(256, W.PAD), (16, 1)])
 def test_w2_gemm_rht_s2f6(pmn, tokens, pad):
     """128-row expert segments (128-wide tiles), and a decode-like batch of

@@ -117,6 +117,21 @@ def test_swiglu_gemm_edge_offsets(pmn):
     run_case(pmn, x, w1, offs, f, extra_rows=3, what="edge offsets")
 
 
+def test_swiglu_gemm_short_segments(pmn):
+    """a decode-like batch (16 or fewer rows per expert on average, where the
+    library takes 32-row tiles): empty experts, 1..5-row segments, and 33- and
+    70-row segments that need several 32-row tiles"""
+    rng = np.random.default_rng(42)
+    d, f = 512, 256
+    counts = [1, 2, 0, 70, 3, 0, 5, 1, 0, 2, 33, 4]
+    E = len(counts)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    assert offs[-1] <= 16 * E
+    x = W.normal_bf16_host(rng, (int(offs[-1]), d), 1.0, 0.01, 30.0)
+    w1 = W.normal_bf16_host(rng, (E, 2 * f, d), 0.02)
+    run_case(pmn, x, w1, offs, f, extra_rows=5, what="short segments")
+
+
 def test_swiglu_gemm_rejects_bad_arguments(pmn):
     z8 = torch.zeros((128, 128), dtype=torch.uint8, device="cuda")
     A = (z8, torch.zeros((128, 16), dtype=torch.uint8, device="cuda"), torch.ones(128, device="cuda"))
