@@ -23,7 +23,8 @@
 //   warps 4..   epilogue (4, or 8 on the K-grouped fp32 tiles): TMEM ->
 //               registers (one row per thread), outer scales, bf16/fp32,
 //               SwiGLU or RHT + S2F6, staged in shared memory and written by
-//               TMA tensor stores in full 128-byte lines
+//               TMA tensor stores in full 128-byte lines (the 32-row tiles of
+//               short segments store their rows directly)
 // 128-wide tiles hold two TMEM accumulators, so the epilogue of one tile
 // overlaps the main loop of the next; 256-wide tiles hold one and release it
 // as soon as it has been read.  Every wait is bounded: on timeout a device
@@ -77,7 +78,7 @@ constexpr int BN_MIN = 128;  // N-tiles are 128 or 256 columns
 #ifndef PMN_GEMM_STAGES  // 128-wide NVFP4 tiles (the w2 GEMM with the RHT + S2F6 epilogue)
 #define PMN_GEMM_STAGES 5
 #endif
-#ifndef PMN_GEMM_STAGES_MXFP8  // 128-wide MXFP8 tiles (the K-grouped weight gradients)
+#ifndef PMN_GEMM_STAGES_MXFP8  // 128-wide MXFP8 tiles (problems whose N is not a multiple of 256)
 #define PMN_GEMM_STAGES_MXFP8 5
 #endif
 #ifndef PMN_EPI_BUFS  // 128-wide tiles; one buffer leaves room for a fifth NVFP4 stage (measured: w2 GEMM
