@@ -862,30 +862,36 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW, SHORT>::THREADS, 1)
             };
             auto store = [&](int c, const uint4 (&o)[NCH]) {
                 const int part = c % CH_PER_STORE;
-                if (!C::DIRECT && slice_full) {
-                    uint8_t *buf = stg + (nstore % C::EPI) * STAGE_OUT_BYTES;
-                    if (part == 0) {
-                        if (lane == 0) bulk_wait_group_read<(C::EPI > 0 ? C::EPI - 1 : 0)>();  // this buffer's last store has read it
-                        __syncwarp();
-                    }
-#pragma unroll
-                    for (int j = 0; j < NCH; ++j) {
-                        const int ci = part * NCH + j;
-                        *reinterpret_cast<uint4 *>(buf + lane * 128 + ((ci ^ (lane & 7)) << 4)) = o[j];
-                    }
-                    if (part == CH_PER_STORE - 1) {
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            const int32_t x = (int32_t)((SWI ? ti.n0 / 2 : ti.n0) + cb + 32 * (c - part));
-                            const int32_t y = (int32_t)(obase + ti.m0 + 32 * q);
-                            if (OUT == PMN_OUT_F32) tma_store_2d_hint(&tmO, smem_u32(buf), x, y, st_policy);
-                            else tma_store_2d(&tmO, smem_u32(buf), x, y);
-                            bulk_commit_group();
+                if constexpr (!C::DIRECT) {
+                    if (slice_full) {
+                        uint8_t *buf = stg + (nstore % C::EPI) * STAGE_OUT_BYTES;
+                        if (part == 0) {
+                            if (lane == 0) bulk_wait_group_read<C::EPI - 1>();  // this buffer's last store has read it
+                            __syncwarp();
                         }
-                        ++nstore;
+#pragma unroll
+                        for (int j = 0; j < NCH; ++j) {
+                            const int ci = part * NCH + j;
+                            *reinterpret_cast<uint4 *>(buf + lane * 128 + ((ci ^ (lane & 7)) << 4)) = o[j];
+                        }
+                        if (part == CH_PER_STORE - 1) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                const int32_t x = (int32_t)((SWI ? ti.n0 / 2 : ti.n0) + cb + 32 * (c - part));
+                                const int32_t y = (int32_t)(obase + ti.m0 + 32 * q);
+                                if (OUT == PMN_OUT_F32) tma_store_2d_hint(&tmO, smem_u32(buf), x, y, st_policy);
+                                else tma_store_2d(&tmO, smem_u32(buf), x, y);
+                                bulk_commit_group();
+                            }
+                            ++nstore;
+                        }
+                        return;
                     }
-                } else if (valid) {
+                }
+                // a slice cut by an expert boundary (and every slice of a
+                // 32-row tile) is written row by row
+                if (valid) {
                     const int64_t col = (SWI ? ti.n0 / 2 : ti.n0) + cb + 32 * c;
                     uint8_t *o8;
                     if (SWI) o8 = reinterpret_cast<uint8_t *>(reinterpret_cast<uint16_t *>(p.out) + orow * (p.n / 2) + col);
