@@ -185,3 +185,36 @@ def test_guard_bytes_gemms(P):
     bt, bts = (dev(v) for v in oracle.mxfp8_quantize(W.normal_bf16_host(rng, (Kt, 128)), transpose=True))
     check_guarded(P, lambda o: P.gemm_mxfp8(at, ats, bt, bts, koffs, P.GROUP_K, f32, out=o), [((3, 256, 128), f32)],
                   "MXFP8 K-grouped")
+
+
+def test_guard_bytes_short_segment_gemms(P):
+    """The 32-row tiles that the NVFP4 GEMMs take for short segments (a
+    decode-like batch, 16 rows per expert or fewer on average) store their
+    rows directly: every output row written once, nothing past the last row."""
+    rng = np.random.default_rng(6)
+    u8, f32, bf16 = torch.uint8, torch.float32, torch.bfloat16
+    E, d, f = 8, 512, 256
+    counts = [1, 0, 40, 3, 2, 0, 5, 1]
+    offs_h = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    T = int(offs_h[-1])
+    assert T <= 16 * E
+    offs = dev(offs_h)
+    A = tuple(dev(a) for a in oracle.nvfp4_quantize(W.normal_bf16_host(rng, (T, d)), oracle.OUTER_PER_ROW,
+                                                    four_over_six=True))
+    wq = oracle.nvfp4_quantize(W.normal_bf16_host(rng, (E * 2 * f, d), 0.02), oracle.OUTER_PER_GROUP,
+                               group_offsets=np.arange(E + 1) * 2 * f)
+    B = (dev(wq[0].reshape(E, 2 * f, d // 2)), dev(wq[1].reshape(E, 2 * f, d // 16)), dev(wq[2]))
+    check_guarded(P, lambda o: P.grouped_gemm_nvfp4(A, B, offs, out_dtype=bf16, out=o), [((T, 2 * f), bf16)],
+                  "short NVFP4 GEMM bf16")
+    check_guarded(P, lambda o: P.grouped_gemm_nvfp4(A, B, offs, out_dtype=f32, out=o), [((T, 2 * f), f32)],
+                  "short NVFP4 GEMM f32")
+    check_guarded(P, lambda h, c, s, g: P.w1_gemm_swiglu_nvfp4(A, B, offs, True, out=(c, s, g), h=h),
+                  [((T, f), bf16), ((T, f // 2), u8), ((T, f // 16), u8), ((T,), f32)],
+                  "short w1 GEMM + SwiGLU + NVFP4")
+    H = tuple(dev(a) for a in oracle.nvfp4_quantize(W.normal_bf16_host(rng, (T, f)), oracle.OUTER_PER_ROW,
+                                                    four_over_six=True))
+    w2 = oracle.nvfp4_quantize(W.normal_bf16_host(rng, (E * d, f), 0.02), oracle.OUTER_PER_GROUP,
+                               group_offsets=np.arange(E + 1) * d)
+    B2 = (dev(w2[0].reshape(E, d, f // 2)), dev(w2[1].reshape(E, d, f // 16)), dev(w2[2]))
+    check_guarded(P, lambda q, s: P.w2_gemm_rht_s2f6(H, B2, offs, 11, out=(q, s)),
+                  [((T, d), torch.int8), ((T, d // 32), u8)], "short w2 GEMM + RHT + S2F6")
