@@ -238,10 +238,28 @@ PMN_API pmn_status pmn_requant_transpose_sr_nvfp4(const uint8_t *codes, const ui
  * bf16 -> MXFP8 with round-to-nearest-even (the gradient dY; the pages ask
  * for SR on the saved forward tensors only).  Same scale rule as above.
  *  transpose 0: out [rows, cols], out_scales [rows, cols/32] (cols % 32 == 0)
- *  transpose 1: out [cols, rows], out_scales [cols, rows/32] (rows % 32 == 0)
+ *  transpose 1: out [cols, rows], out_scales [cols, rows/32] (rows % 32 == 0,
+ *               rows <= 65535 * 128, else PMN_ERR_UNSUPPORTED)
+ * x and out 16-byte aligned.  One kernel on `stream`.
  */
 PMN_API pmn_status pmn_mxfp8_quantize(const void *x, int64_t rows, int64_t cols, int transpose,
                               uint8_t *out, uint8_t *out_scales, void *stream);
+
+/*
+ * Both orientations of pmn_mxfp8_quantize in one pass over x [SR]: the
+ * gradient's rowwise copy feeds dX / dH, its transposed copy the weight
+ * gradients of the MXFP8 backward.  x is read once; the bytes equal those of
+ * the two separate calls.
+ *  x      bf16 [rows, cols], row-major, 16-byte aligned.
+ *  rows % 32 == 0 and cols % 32 == 0 (else PMN_ERR_INVALID_ARG);
+ *  rows <= 65535 * 128 (else PMN_ERR_UNSUPPORTED).
+ *  out_rows [rows, cols] (16-byte aligned), out_rows_scales [rows, cols/32];
+ *  out_cols [cols, rows] (16-byte aligned), out_cols_scales [cols, rows/32].
+ * All buffers are the caller's device memory.  One kernel on `stream`.
+ */
+PMN_API pmn_status pmn_mxfp8_quantize_both(const void *x, int64_t rows, int64_t cols, uint8_t *out_rows,
+                                          uint8_t *out_rows_scales, uint8_t *out_cols, uint8_t *out_cols_scales,
+                                          void *stream);
 
 /*
  * SwiGLU followed by MXFP8 quantisation (round to nearest even, E8M0 per 32

@@ -684,13 +684,27 @@ __device__ __forceinline__ int rq_chunk(int c, int logical)
 // it in registers and stores 16-byte chunks (8 rows of one column) into the
 // swizzled tile.  Phase 2: task (c, rb) forms the 32-block of output row c;
 // four consecutive lanes write one 128-byte line of the output row.
-#ifndef PMN_MXT_MIN_BLOCKS  // resident CTAs per SM the register allocation aims for (measured: 5
-#define PMN_MXT_MIN_BLOCKS 5  // is 6 % faster than the uncapped 4; 6 spills)
+// ROWS: the same pass also writes the rowwise MXFP8 of the tile (the input is
+// read once for both orientations): in phase 1 the four lanes that hold one
+// row's 32-column block (column groups 4b .. 4b+3, adjacent lanes) take the
+// block's amax with two shuffles and each converts its 8 values, with the
+// arithmetic of mxfp8_quant_rowwise_kernel.
+// Resident CTAs per SM the register allocation aims for.  Column blocks only:
+// 5 (6 % faster than the uncapped 4; 6 spills).  Both orientations: 4 (at 5
+// the added row pass spills, 21 % slower; 3 is 10 % slower).
+#ifndef PMN_MXT_MIN_BLOCKS
+#define PMN_MXT_MIN_BLOCKS 5
 #endif
-__global__ void __launch_bounds__(256, PMN_MXT_MIN_BLOCKS) mxfp8_quant_transposed_kernel(const uint16_t *__restrict__ x,
+#ifndef PMN_MXB_MIN_BLOCKS
+#define PMN_MXB_MIN_BLOCKS 4
+#endif
+template <bool ROWS>
+__global__ void __launch_bounds__(256, ROWS ? PMN_MXB_MIN_BLOCKS : PMN_MXT_MIN_BLOCKS) mxfp8_quant_transposed_kernel(const uint16_t *__restrict__ x,
                                                                      int64_t rows, int64_t cols,
                                                                      uint8_t *__restrict__ out,
-                                                                     uint8_t *__restrict__ out_sc)
+                                                                     uint8_t *__restrict__ out_sc,
+                                                                     uint8_t *__restrict__ out_r,
+                                                                     uint8_t *__restrict__ out_r_sc)
 {
     __shared__ __align__(16) uint4 cS[RQ_T * 16];  // [c][16 chunks of 8 rows] bf16
     const int64_t r0 = (int64_t)blockIdx.y * RQ_T, c0 = (int64_t)blockIdx.x * RQ_T;
@@ -704,6 +718,34 @@ __global__ void __launch_bounds__(256, PMN_MXT_MIN_BLOCKS) mxfp8_quant_transpose
         for (int i = 0; i < 8; ++i) {
             v[i] = make_uint4(0u, 0u, 0u, 0u);
             if (col_ok && i < rows_left) v[i] = __ldg(reinterpret_cast<const uint4 *>(xp + i * cols));
+        }
+        if constexpr (ROWS) {
+            // rowwise blocks: lanes 4b .. 4b+3 of a 16-lane row group hold one
+            // row's 32 columns (out-of-range lanes hold zeros and store nothing)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                float amax = 0.0f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+                const int e = mx_exponent_448(amax);
+                const float sc = exp2_neg(e);  // y = x * 2^-e is exact
+                uint32_t o[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    float p0, p1, p2, p3;
+                    mul2(bf16_lo(w[2 * k]), bf16_hi(w[2 * k]), sc, sc, p0, p1);
+                    mul2(bf16_lo(w[2 * k + 1]), bf16_hi(w[2 * k + 1]), sc, sc, p2, p3);
+                    o[k] = cvt_e4m3x2_rn(p0, p1) | (cvt_e4m3x2_rn(p2, p3) << 16);
+                }
+                if (col_ok && i < rows_left) {
+                    const int64_t row = r0 + 8 * rg + i, col = c0 + 8 * cg;
+                    *reinterpret_cast<uint2 *>(out_r + row * cols + col) = make_uint2(o[0], o[1]);
+                    if ((cg & 3) == 0) out_r_sc[row * (cols / 32) + col / 32] = (uint8_t)(e + 127);
+                }
+            }
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // columns 2k, 2k+1
@@ -1584,9 +1626,26 @@ extern "C" pmn_status pmn_mxfp8_quantize(const void *x, int64_t rows, int64_t co
         mxfp8_quant_rowwise_kernel<<<(unsigned)((nblocks + 255) / 256), 256, 0, s>>>(xb, nblocks, cols / 32, out,
                                                                                      out_scales);
     } else {
+        if ((rows + RQ_T - 1) / RQ_T > 65535) return PMN_ERR_UNSUPPORTED;  // grid.y: one row of CTAs per 128 rows
         dim3 grid((unsigned)((cols + RQ_T - 1) / RQ_T), (unsigned)((rows + RQ_T - 1) / RQ_T));
-        mxfp8_quant_transposed_kernel<<<grid, 256, 0, s>>>(xb, rows, cols, out, out_scales);
+        mxfp8_quant_transposed_kernel<false><<<grid, 256, 0, s>>>(xb, rows, cols, out, out_scales, nullptr, nullptr);
     }
+    return launch_status();
+}
+
+extern "C" pmn_status pmn_mxfp8_quantize_both(const void *x, int64_t rows, int64_t cols, uint8_t *out_rows,
+                                              uint8_t *out_rows_scales, uint8_t *out_cols, uint8_t *out_cols_scales,
+                                              void *stream)
+{
+    if (rows < 0 || cols < 0 || rows % 32 != 0 || cols % 32 != 0) return PMN_ERR_INVALID_ARG;
+    if (!x || !out_rows || !out_rows_scales || !out_cols || !out_cols_scales) return PMN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out_rows) || !aligned16(out_cols)) return PMN_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return PMN_OK;
+    if ((rows + RQ_T - 1) / RQ_T > 65535) return PMN_ERR_UNSUPPORTED;  // grid.y: one row of CTAs per 128 rows
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    dim3 grid((unsigned)((cols + RQ_T - 1) / RQ_T), (unsigned)((rows + RQ_T - 1) / RQ_T));
+    mxfp8_quant_transposed_kernel<true><<<grid, 256, 0, s>>>(reinterpret_cast<const uint16_t *>(x), rows, cols,
+                                                             out_cols, out_cols_scales, out_rows, out_rows_scales);
     return launch_status();
 }
 

@@ -120,10 +120,10 @@ class ExpertLayerStep:
                                                                 out=self.w1t)),
             ("requant_w2", lambda: P.requant_transpose_sr_mxfp8(*self.w2q, False, E, D, F, self.seed, P.TAG_W2,
                                                                 out=self.w2t)),
-            ("quant_dy_rows", lambda: P.mxfp8_quantize(self.dy, False, out=self.dy_r)),
-            ("quant_dy_cols", lambda: P.mxfp8_quantize(self.dy, True, out=self.dy_t)),
-            ("quant_dy1_rows", lambda: P.mxfp8_quantize(self.dy1, False, out=self.dy1_r)),
-            ("quant_dy1_cols", lambda: P.mxfp8_quantize(self.dy1, True, out=self.dy1_t)),
+            # both orientations of each gradient in one pass (rowwise for dH / dX,
+            # transposed for the weight gradients)
+            ("quant_dy", lambda: P.mxfp8_quantize_both(self.dy, out=self.dy_r, out_t=self.dy_t)),
+            ("quant_dy1", lambda: P.mxfp8_quantize_both(self.dy1, out=self.dy1_r, out_t=self.dy1_t)),
             ("gemm_dh_mxfp8", lambda: P.gemm_mxfp8(self.dy_r[0], self.dy_r[1], self.w2t[0], self.w2t[1],
                                                    self.offsets, P.GROUP_M, torch.bfloat16, out=self.dh)),
             ("gemm_dw2_mxfp8", lambda: P.gemm_mxfp8(self.dy_t[0], self.dy_t[1], self.ht[0][0], self.ht[1][0],
@@ -255,8 +255,8 @@ def decode_algorithmic(counts, d_model, d_ff):
 # quantiser is a memset, not a kernel of the library)
 LAUNCHES = {"gemm1_swiglu_nvfp4": 2}  # the GEMM with the SwiGLU epilogue, then the NVFP4 coding of h
 STEP_CALLS = ["quant_w1", "quant_w2", "quant_x", "gemm1_swiglu_nvfp4", "gemm2_nvfp4_rht_s2f6",
-              "requant_x", "requant_h", "requant_w1", "requant_w2", "quant_dy_rows", "quant_dy_cols",
-              "quant_dy1_rows", "quant_dy1_cols", "gemm_dh_mxfp8", "gemm_dw2_mxfp8", "gemm_dx_mxfp8",
+              "requant_x", "requant_h", "requant_w1", "requant_w2", "quant_dy", "quant_dy1",
+              "gemm_dh_mxfp8", "gemm_dw2_mxfp8", "gemm_dx_mxfp8",
               "gemm_dw1_mxfp8"]
 
 
@@ -282,10 +282,8 @@ def algorithmic(shape: LayerShape):
         "requant_h": (0, R * F * (nv + mx)),
         "requant_w1": (0, w1n * (nv + mx)),
         "requant_w2": (0, w2n * (nv + mx)),
-        "quant_dy_rows": (0, R * D * (2 + mx)),
-        "quant_dy_cols": (0, R * D * (2 + mx)),
-        "quant_dy1_rows": (0, R * F2 * (2 + mx)),
-        "quant_dy1_cols": (0, R * F2 * (2 + mx)),
+        "quant_dy": (0, R * D * (2 + 2 * mx)),      # bf16 read once, both MXFP8 orientations written
+        "quant_dy1": (0, R * F2 * (2 + 2 * mx)),
         "gemm_dh_mxfp8": (2.0 * R * D * F, (R * D + w2n) * mx + R * F * 2),
         "gemm_dw2_mxfp8": (2.0 * R * D * F, (R * D + R * F) * mx + w2n * 4),
         "gemm_dx_mxfp8": (2.0 * R * F2 * D, (R * F2 + w1n) * mx + R * D * 2),

@@ -39,6 +39,7 @@ SIGNATURES = {
     "pmn_nvfp4_quantize_workspace_bytes": ([_I, _I64, _I64], _I64),
     "pmn_nvfp4_quantize_per_group_noalloc": ([_P, _I64, _I64, _I64, _I, _P, _P, _P, _P], _I),
     "pmn_requant_transpose_sr_mxfp8": ([_P, _P, _P, _I, _I64, _I64, _I64, _U64, _U32, _I, _P, _P, _P], _I),
+    "pmn_mxfp8_quantize_both": ([_P, _I64, _I64, _P, _P, _P, _P, _P], _I),
     "pmn_requant_transpose_sr_nvfp4": ([_P, _P, _P, _I, _I64, _I64, _I64, _U64, _U32, _I, _P, _P, _P, _P], _I),
     "pmn_mxfp8_quantize": ([_P, _I64, _I64, _I, _P, _P, _P], _I),
     "pmn_mxfp8_quantize_swiglu": ([_P, _I64, _I64, _P, _P, _P, _P], _I),
@@ -227,6 +228,24 @@ def mxfp8_quantize(x, transpose=False, out=None, stream=None):
     _check(lib().pmn_mxfp8_quantize(_ptr(x), rows, cols, int(transpose), _ptr(q), _ptr(sc), _stream(stream)),
            "mxfp8_quantize")
     return q, sc
+
+
+def mxfp8_quantize_both(x, out=None, out_t=None, stream=None):
+    """bf16 [rows, cols] -> (MXFP8 rowwise (u8 [rows, cols], u8 [rows, cols/32]),
+    MXFP8 of the transpose (u8 [cols, rows], u8 [cols, rows/32])) in one pass."""
+    _dev(x, torch.bfloat16)
+    rows, cols = x.shape
+    dev = x.device
+    if out is None:
+        out = (torch.empty((rows, cols), dtype=torch.uint8, device=dev),
+               torch.empty((rows, cols // 32), dtype=torch.uint8, device=dev))
+    if out_t is None:
+        out_t = (torch.empty((cols, rows), dtype=torch.uint8, device=dev),
+                 torch.empty((cols, rows // 32), dtype=torch.uint8, device=dev))
+    st = lib().pmn_mxfp8_quantize_both(_ptr(x), rows, cols, _ptr(out[0]), _ptr(out[1]), _ptr(out_t[0]),
+                                       _ptr(out_t[1]), _stream(stream))
+    _check(st, "mxfp8_quantize_both")
+    return out, out_t
 
 
 def mxfp8_quantize_swiglu(y, want_h=False, out=None, stream=None):

@@ -53,6 +53,12 @@ def test_host_argument_checks_need_no_gpu(libpath):
     assert L.pmn_nvfp4_quantize(null, 4, 24, 24, 0, 0, 0, 0, null, null, null, null, null, 0,
                                 null) == pmn.ERR_INVALID_ARG
     assert L.pmn_mxfp8_quantize(null, 40, 64, 1, null, null, null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_mxfp8_quantize_both(null, 64, 64, null, null, null, null, null) == pmn.ERR_INVALID_ARG
+    assert L.pmn_mxfp8_quantize_both(1 << 20, 48, 64, 1 << 20, 1 << 20, 1 << 20, 1 << 20, null) == pmn.ERR_INVALID_ARG
+    # more than 65535 rows of 128-row CTAs: refused before anything is enqueued
+    big = 65536 * 128
+    assert L.pmn_mxfp8_quantize_both(1 << 20, big, 32, 1 << 20, 1 << 20, 1 << 20, 1 << 20, null) == pmn.ERR_UNSUPPORTED
+    assert L.pmn_mxfp8_quantize(1 << 20, big, 32, 1, 1 << 20, 1 << 20, null) == pmn.ERR_UNSUPPORTED
     assert L.pmn_requant_transpose_sr_mxfp8(null, null, null, 0, 1, 32, 32, 0, 1, 0, null, null,
                                             null) == pmn.ERR_INVALID_ARG
     assert L.pmn_grouped_gemm_nvfp4(null, null, null, null, null, null, null, 0, 0, 128, 256, 0, null,

@@ -173,6 +173,29 @@ def test_mxfp8_quantize_transposed(pmn, shape):
     assert_same(q, rq, "values")
 
 
+@pytest.mark.parametrize("shape", [(32, 32), (256, 256), (160, 1536), (224, 96), (96, 4096), (384, 3072)])
+def test_mxfp8_quantize_both(pmn, shape):
+    """both orientations in one pass: the bytes of the oracle's rowwise and
+    transposed MXFP8, and of the two separate library calls (partial tiles in
+    both directions included)"""
+    rng = np.random.default_rng(shape[0] + shape[1])
+    x = W.normal_bf16_host(rng, shape, 1e-3, 0.01, 50.0)
+    x[3, :] = 0  # an all-zero row and column block
+    x[:, 5] = 0
+    xd = to_dev_bf16(x)
+    (q, sc), (qt, sct) = pmn.mxfp8_quantize_both(xd)
+    rq, rsc = oracle.mxfp8_quantize(x, transpose=False)
+    rqt, rsct = oracle.mxfp8_quantize(x, transpose=True)
+    assert_same(sc, rsc, "row scales")
+    assert_same(q, rq, "row values")
+    assert_same(sct, rsct, "column scales")
+    assert_same(qt, rqt, "column values")
+    q2, sc2 = pmn.mxfp8_quantize(xd, transpose=False)
+    qt2, sct2 = pmn.mxfp8_quantize(xd, transpose=True)
+    for a, b in [(q, q2), (sc, sc2), (qt, qt2), (sct, sct2)]:
+        assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("stochastic", [True, False])
 @pytest.mark.parametrize("batch,rows,cols,per_row", [(1, 32, 64, True), (1, 256, 256, True), (1, 160, 1536, True),
                                                      (3, 96, 128, False), (2, 512, 192, False)])
