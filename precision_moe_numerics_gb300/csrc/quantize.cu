@@ -1016,25 +1016,64 @@ __global__ void __launch_bounds__(128, PER_ROW ? 1 : 5) requant_transpose_kernel
 // (the rule and bit layout of the MXFP8 requantisation), or nearest even.
 
 // Largest dec(S) * g of each entry, as float bits (non-negative floats order
-// as integers, so atomicMax is order-independent).  Thread = one 4-byte word
-// of scales; grid (ceil(rows * spr / 4 / 256), batch).
+// as integers, so atomicMax is order-independent).  A CTA reduces 32 KB of one
+// entry's scales with 16-byte loads and takes one atomic (grid
+// (ceil(words / 8192), batch)): the atomics of an entry are few enough not to
+// serialise on its one address.  Over the codes with the sign bit clear, dec
+// is non-decreasing in the byte (0x7F decodes as 480); the others decode to
+// <= 0 and never raise the maximum; and RN(x g) is non-decreasing in x for
+// g >= 0.  So the largest product of a set of bytes that share g is
+// RN(dec(their largest sign-clear byte) * g): bytes are compared as unsigned
+// integers and decoded once per word (per-row outer: a word's four scales lie
+// in one row) or once per thread (one outer per entry).
+constexpr int SMX_PIECES = 8;  // 16-byte pieces per thread
 __global__ void __launch_bounds__(256) nvfp4_scale_max_kernel(const uint8_t *__restrict__ scales,
                                                               const float *__restrict__ outer, int per_row,
                                                               uint32_t rows, uint32_t wpr,
                                                               uint32_t *__restrict__ gmax)
 {
+    __shared__ float red[8];
     const int64_t b = blockIdx.y;
-    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t nw = rows * wpr;  // rows % 32 == 0: every entry starts 16-byte aligned, nw % 4 == 0
+    const uint4 *sp = reinterpret_cast<const uint4 *>(scales + (uint64_t)b * nw * 4u);
     float m = 0.0f;
-    if (i < rows * wpr) {
-        const uint32_t r = i / wpr;
-        const float g = per_row ? __ldg(outer + b * rows + r) : __ldg(outer + b);
-        const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(scales) + (b * rows) * wpr + i);
+    uint32_t acc = 0u;  // per-byte maximum of the sign-clear bytes (one outer per entry)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) m = fmaxf(m, __fmul_rn(e4m3_to_f32((w >> (8 * k)) & 0xFFu), g));
+    for (int it = 0; it < SMX_PIECES; ++it) {
+        const uint32_t p = blockIdx.x * (256u * SMX_PIECES) + it * 256u + threadIdx.x;
+        if (p < nw / 4u) {
+            const uint4 v = __ldg(sp + p);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            if (per_row) {
+                uint32_t r = (4u * p) / wpr, k = 4u * p - r * wpr;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t x = w4[kk] & __vcmpltu4(w4[kk], 0x80808080u);
+                    uint32_t t = __vmaxu4(x, x >> 16);
+                    t = __vmaxu4(t, t >> 8);
+                    m = fmaxf(m, __fmul_rn(e4m3_to_f32(t & 0xFFu), __ldg(outer + b * rows + r)));
+                    if (++k == wpr) { k = 0u; ++r; }
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) acc = __vmaxu4(acc, w4[kk] & __vcmpltu4(w4[kk], 0x80808080u));
+            }
+        }
+    }
+    if (!per_row) {
+        uint32_t t = __vmaxu4(acc, acc >> 16);
+        t = __vmaxu4(t, t >> 8);
+        m = __fmul_rn(e4m3_to_f32(t & 0xFFu), __ldg(outer + b));
     }
     m = warp_max(m);
-    if ((threadIdx.x & 31) == 0 && m > 0.0f) atomicMax(gmax + b, __float_as_uint(m));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float mm = red[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) mm = fmaxf(mm, red[i]);
+        if (mm > 0.0f) atomicMax(gmax + b, __float_as_uint(mm));
+    }
 }
 
 __device__ __forceinline__ float nvfp4_outer_from_max(uint32_t bits)
@@ -1718,8 +1757,9 @@ extern "C" pmn_status pmn_requant_transpose_sr_nvfp4(const uint8_t *codes, const
     const bool per_row = outer_mode == PMN_OUTER_PER_ROW;
     if (rows > 0 && cols > 0) {
         const uint32_t wpr = (uint32_t)(cols / 64), nw = (uint32_t)rows * wpr;
-        nvfp4_scale_max_kernel<<<dim3((nw + 255) / 256, (unsigned)batch), 256, 0, s>>>(scales, outer, per_row,
-                                                                                        (uint32_t)rows, wpr, gmax);
+        const uint32_t per_cta = 256u * SMX_PIECES;  // 16-byte pieces per CTA
+        nvfp4_scale_max_kernel<<<dim3((nw / 4u + per_cta - 1u) / per_cta, (unsigned)batch), 256, 0, s>>>(
+            scales, outer, per_row, (uint32_t)rows, wpr, gmax);
         dim3 grid((unsigned)((cols + 127) / 128), (unsigned)((rows + 127) / 128), (unsigned)batch);
         const int sr = rounding == PMN_ROUND_SR;
         if (per_row)

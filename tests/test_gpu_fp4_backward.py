@@ -65,3 +65,23 @@ def test_requant_nvfp4_deterministic_and_arguments(P):
         assert torch.equal(u, v)
     with pytest.raises(P.PmnError):            # rows % 32 != 0
         P.requant_transpose_sr_nvfp4(dev(c[:112]), dev(s[:112]), dev(g[:112]), True, 1, 112, 128, 9, 1)
+
+
+@pytest.mark.parametrize("hot_row", [0, 37, 63])
+def test_requant_nvfp4_outer_from_planted_row(P, hot_row):
+    """The new outer scale is the largest dec(S) * g of the entry: one row
+    carries a value far above the rest, so the maximum sits in that row and
+    pairing a scale with its neighbour row's outer scale would change it.
+    Five scale words per row, so 16-byte pieces of the scales cross rows."""
+    rows, cols = 96, 320
+    rng = np.random.default_rng(hot_row)
+    x = W.normal_bf16_host(rng, (rows, cols), 1.0, 0.002, 40.0)
+    x[rows - 32:] = 0
+    x[hot_row, (7 * hot_row) % cols] = 0x4461   # bf16 bits of 900.0
+    c, s, g = oracle.nvfp4_quantize(x, oracle.OUTER_PER_ROW, four_over_six=True)
+    got = P.requant_transpose_sr_nvfp4(dev(c), dev(s), dev(g), True, 1, rows, cols, 77, 2)
+    torch.cuda.synchronize()
+    want = oracle.requant_transpose_nvfp4(c, s, g, True, 1, rows, cols, 77, 2, stochastic=True)
+    assert got[2].cpu().numpy().view(np.uint32)[0] == want[2].view(np.uint32)[0]
+    for a, b in zip(got[:2], want[:2]):
+        assert np.array_equal(a.cpu().numpy().reshape(b.shape), b)
