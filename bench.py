@@ -214,6 +214,9 @@ def main():
                     "FP4-requant and single-expert measurements")
     ap.add_argument("--single-expert-only", action="store_true",
                     help="profiling: only the single-expert forward (T = 4096), printed as one JSON object")
+    ap.add_argument("--fp4-requant-only", action="store_true",
+                    help="profiling: the step once, then only the FP4-backward requantisations (--steps passes), "
+                    "printed as one JSON object")
     args = ap.parse_args()
     rank, world, local = dist_env()
 
@@ -262,6 +265,13 @@ def main():
                               seed=args.seed)
     calls = L.kernel_calls()
     alg = layer.algorithmic(L.shape)
+    if args.fp4_requant_only:  # profiling: the step once (the saved NVFP4 tensors), then the FP4 requantisations
+        for _, f in calls:
+            f()
+        res = run_fp4_requant(L, args, pmn, reps=args.steps)
+        if rank == 0:
+            print(json.dumps({"fp4_backward_requant": res}))
+        return
     if args.only:
         for name, f in calls:  # the step once, so every operand of the chosen call exists
             f()

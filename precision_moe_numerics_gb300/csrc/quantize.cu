@@ -1143,9 +1143,13 @@ __device__ __forceinline__ uint32_t sr_bits_of(const uint4 &wd, int e)
 // XOR bits 3..5 of the row) and written as 16-byte pieces, four lanes per
 // output row.
 // Register targets (measured): 5 resident CTAs per SM for the per-group form
-// (W1 4.10 -> 3.99 ms), 4 for the per-row form, which would spill at 5.
+// (faster than 4 by 3 %; 6 spills and is 6 % slower), 4 for the per-row
+// form, which would spill at 5.
+#ifndef PMN_FP4RQ_MIN_BLOCKS
+#define PMN_FP4RQ_MIN_BLOCKS 5
+#endif
 template <bool PER_ROW>
-__global__ void __launch_bounds__(128, PER_ROW ? 4 : 5) requant_transpose_nvfp4_kernel(
+__global__ void __launch_bounds__(128, PER_ROW ? 4 : PMN_FP4RQ_MIN_BLOCKS) requant_transpose_nvfp4_kernel(
     const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, const float *__restrict__ outer,
     int64_t rows, int64_t cols, uint64_t seed, uint32_t tag, int stochastic, const uint32_t *__restrict__ gmax,
     uint8_t *__restrict__ out, uint8_t *__restrict__ out_sc)
