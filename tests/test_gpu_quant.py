@@ -196,6 +196,46 @@ def test_mxfp8_quantize_both(pmn, shape):
         assert torch.equal(a, b)
 
 
+def test_mxfp8_extreme_blocks(pmn):
+    """MXFP8 at the ends of the bf16 range, in both orientations and through
+    the one-pass call: blocks of bf16 subnormals (the E8M0 exponent clamps at
+    -127), blocks near the largest bf16, blocks whose amax is exactly
+    448 * 2^k (scale 2^k) or one bf16 step above it (2^(k+1)), one huge value
+    among tiny ones of both signs (negative values that round to zero keep
+    their sign bit), and a column block of subnormals."""
+    rng = np.random.default_rng(11)
+    rows, cols = 96, 256
+    x = W.normal_bf16_host(rng, (rows, cols), 1.0, 0.01, 20.0)
+    sign = lambda n: (rng.integers(0, 2, n, dtype=np.uint16) << 15)
+    x[0] = rng.integers(1, 0x80, cols, dtype=np.uint16) | sign(cols)          # subnormals
+    x[1] = rng.integers(0x7F00, 0x7F80, cols, dtype=np.uint16) | sign(cols)   # near the largest bf16
+    ks = []
+    for b in range(cols // 32):                                               # amax at 448 * 2^k, or just above
+        k = int(rng.integers(-20, 20))
+        ks.append(k)
+        top = np.float32(448.0 * 2.0 ** k).view(np.uint32) >> 16
+        x[2, 32 * b:32 * b + 32] = (top - rng.integers(0x80, 0x800, 32)).astype(np.uint16) | sign(32)  # below top
+        x[2, 32 * b + int(rng.integers(0, 32))] = np.uint16(top + (b & 1)) | np.uint16(0x8000 * (b >> 2 & 1))
+    x[3] = rng.integers(0x0080, 0x0400, cols, dtype=np.uint16) | sign(cols)   # tiny normals ...
+    x[3, ::32] = 0x7E00                                                       # ... under a huge value
+    x[32:64, 64:96] = rng.integers(1, 0x80, (32, 32), dtype=np.uint16) | (
+        rng.integers(0, 2, (32, 32), dtype=np.uint16) << 15)                  # a column block of subnormals
+    xd = to_dev_bf16(x)
+    rq, rsc = oracle.mxfp8_quantize(x, transpose=False)
+    rqt, rsct = oracle.mxfp8_quantize(x, transpose=True)
+    # the clamp, the planted block maxima and the negative zeros are exercised
+    assert rsc[0].max() == 0 and (rq[3] == 0x80).any()
+    assert np.array_equal(rsc[2].astype(int) - 127, [k + (b & 1) for b, k in enumerate(ks)])
+    (q, sc), (qt, sct) = pmn.mxfp8_quantize_both(xd)
+    q1, sc1 = pmn.mxfp8_quantize(xd, transpose=False)
+    qt1, sct1 = pmn.mxfp8_quantize(xd, transpose=True)
+    for got, want, what in [(q, rq, "row values"), (sc, rsc, "row scales"), (qt, rqt, "column values"),
+                            (sct, rsct, "column scales"), (q1, rq, "rowwise call values"),
+                            (sc1, rsc, "rowwise call scales"), (qt1, rqt, "transposed call values"),
+                            (sct1, rsct, "transposed call scales")]:
+        assert_same(got, want, what)
+
+
 @pytest.mark.parametrize("stochastic", [True, False])
 @pytest.mark.parametrize("batch,rows,cols,per_row", [(1, 32, 64, True), (1, 256, 256, True), (1, 160, 1536, True),
                                                      (3, 96, 128, False), (2, 512, 192, False)])
