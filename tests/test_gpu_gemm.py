@@ -194,16 +194,21 @@ def check_mx(got, ref, absab, what):
     check_f32(got, ref, absab, what)
 
 
-def test_gemm_mxfp8_mgrouped(pmn):
-    rng = np.random.default_rng(21)
-    K, N = 1024, 256
+@pytest.mark.parametrize("K,N,out_dtype", [(1024, 256, torch.float32), (3072, 512, torch.bfloat16),
+                                           (512, 256, torch.bfloat16), (1536, 128, torch.float32)])
+def test_gemm_mxfp8_mgrouped(pmn, K, N, out_dtype):
+    """M-grouped MXFP8 (the dX / dH form) against the oracle: ragged, empty
+    and one-row segments; one to six groups of four 128-wide K steps (the
+    256-wide tiles' scale rows cover four steps each); one or two 256-wide
+    column tiles, or 128-wide tiles; fp32 and bf16 outputs."""
+    rng = np.random.default_rng(21 + K + N)
     counts = [64, 0, 200, 32, 1]
     offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     G, M = len(counts), int(offs[-1])
     a, asc = mx_case(rng, M, K)
     b, bsc = mx_case(rng, G * N, K, 0.02)
     b, bsc = b.reshape(G, N, K), bsc.reshape(G, N, K // 32)
-    out = pmn.gemm_mxfp8(dev(a), dev(asc), dev(b), dev(bsc), dev(offs), pmn.GROUP_M, torch.float32)
+    out = pmn.gemm_mxfp8(dev(a), dev(asc), dev(b), dev(bsc), dev(offs), pmn.GROUP_M, out_dtype)
     ref = oracle.gemm_mxfp8_mgrouped(a, asc, b, bsc, offs)
     absab = np.zeros_like(ref)
     for g in range(G):
@@ -211,7 +216,10 @@ def test_gemm_mxfp8_mgrouped(pmn):
         if hi > lo:
             absab[lo:hi] = np.abs(oracle.mxfp8_dequant_f64(a[lo:hi], asc[lo:hi])) @ np.abs(
                 oracle.mxfp8_dequant_f64(b[g], bsc[g])).T
-    check_mx(out.cpu().numpy(), ref, absab, "mxfp8 M-grouped")
+    if out_dtype == torch.float32:
+        check_mx(out.cpu().numpy(), ref, absab, "mxfp8 M-grouped")
+    else:
+        check_bf16(out.view(torch.int16).cpu().numpy(), ref, absab, "mxfp8 M-grouped bf16")
 
 
 def test_gemm_mxfp8_kgrouped(pmn):
