@@ -183,8 +183,7 @@ def oracle_sample(inputs, experts, seed=0):
         oracle.gemm_mxfp8_kgrouped(dy1t[0], dy1t[1], xt[0][0], xt[1][0], [0, n])
         flops += 3 * (2.0 * real * D * F2 + 2.0 * real * F * D)
     dt = time.perf_counter() - t0
-    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return flops, dt, threads
+    return flops, dt, oracle.max_threads()
 
 
 def pick_sample_experts(r, k):
@@ -762,10 +761,21 @@ def cpu_baseline(inp, args, budget_s=12.0):
     k = max(1, min(48, int(budget_s / max(per, 1e-3))))
     experts = pick_sample_experts(r, k)
     flops, dt, threads = oracle_sample(inp, experts, args.seed)
+    # the same step on one thread, over one expert
+    import oracle
+    one = pick_sample_experts(r, 1)
+    oracle.set_num_threads(1)
+    try:
+        f1, t1, _ = oracle_sample(inp, one, args.seed)
+    finally:
+        oracle.set_num_threads(threads)
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": "the full step (quantise, GEMMs in binary64, SwiGLU, RHT+S2F6, SR requant, dY quant, "
-                      "gradient GEMMs) for %d of 384 experts (%d routed rows), %.1f s" % (
-                          len(experts), int(sum(r.counts[e] for e in experts)), dt)}
+                      "gradient GEMMs) for %d of %d experts (%d routed rows), %.1f s" % (
+                          len(experts), len(r.counts), int(sum(r.counts[e] for e in experts)), dt),
+            "single_thread": {"value": round(f1 / t1 / 1e12, 6), "cores": 1,
+                              "sample": "the same step for 1 expert (%d routed rows), %.1f s" % (
+                                  int(r.counts[one[0]]), t1)}}
 
 
 def run_reference(args):

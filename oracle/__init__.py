@@ -41,6 +41,9 @@ def lib():
         P = ctypes.c_void_p
         i64, u64, u32, i32 = ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int
         L.orc_philox4x32_10.argtypes = [P, P, P]
+        L.orc_set_num_threads.argtypes = [i32]
+        L.orc_set_num_threads.restype = None
+        L.orc_max_threads.restype = i32
         L.orc_sr_bits16.argtypes = [u64, u32, u64]
         L.orc_sr_bits16.restype = u32
         for n in ("orc_e2m1_value", "orc_e4m3_value", "orc_e8m0_value"):
@@ -139,6 +142,15 @@ def e2m1_sr(y, rb16):
 
 def bf16_rne(v):
     return lib().orc_bf16_rne(float(v))
+
+
+def set_num_threads(n):
+    """Threads of the oracle's OpenMP loops (timing only; results do not depend on it)."""
+    lib().orc_set_num_threads(int(n))
+
+
+def max_threads():
+    return int(lib().orc_max_threads())
 
 
 def e8m0_exponent(amax, top=448.0):

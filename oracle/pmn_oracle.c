@@ -33,6 +33,7 @@
 #include <stdlib.h>
 #include <stdint.h>
 #include <string.h>
+#include <omp.h>
 
 #define ORC_API __attribute__((visibility("default")))
 
@@ -720,3 +721,8 @@ ORC_API void orc_bf16_rne_array(const double *v, int64_t n, uint16_t *out)
     #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) out[i] = (uint16_t)orc_bf16_rne(v[i]);
 }
+
+/* Threads of the oracle's OpenMP loops (the CPU baseline times all host
+ * cores and one thread); no effect on any result. */
+ORC_API void orc_set_num_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
+ORC_API int orc_max_threads(void) { return omp_get_max_threads(); }

@@ -2,7 +2,7 @@
 samples taken inside the timed region and reports throttle reasons; the DRAM
 traffic table counts an entry only while the kernel source is unchanged; the
 decode forward's algorithmic bytes are the hit experts' weights plus the
-activations."""
+activations; the oracle's CPU baseline reports all threads and one."""
 import datetime
 import importlib.util
 import os
@@ -110,3 +110,19 @@ def test_result_line_carries_the_contract_keys():
     assert line["data"] == "synthetic" and line["gpu_launches"] == 540 and "workload" in line["config"]
     assert set(roof) <= set(line["roofline"]) and line["cpu_baseline"]["kind"] == "oracle"
     assert "decode" in line and "components" in line
+
+
+def test_cpu_baseline_reports_all_threads_and_one():
+    """The oracle's CPU baseline on a small layer: the all-threads figure with
+    the thread count OpenMP really uses, a one-thread figure beside it, and the
+    thread count restored afterwards."""
+    import types
+    import oracle
+    from precision_moe_numerics_gb300 import workloads as W
+    inp = W.moe_device(0, device="cpu", experts=4, tokens=64, d=256, f=128)
+    before = oracle.max_threads()
+    res = load_bench().cpu_baseline(inp, types.SimpleNamespace(seed=0), budget_s=0.0)
+    assert res["kind"] == "oracle" and res["cores"] == before and res["value"] > 0
+    assert res["single_thread"]["cores"] == 1 and res["single_thread"]["value"] > 0
+    assert "of 4 experts" in res["sample"]
+    assert oracle.max_threads() == before
