@@ -902,6 +902,33 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW, SHORT>::THREADS, 1)
                     for (int j = 0; j < NCH; ++j) reinterpret_cast<uint4 *>(o8)[j] = o[j];
                 }
             };
+            // The warp's accumulator slice rounded to bf16 (y = acc * scale * gb
+            // for NVFP4), read 16 columns at a time and software-pipelined: the
+            // next 16 columns load while the current ones convert, so the
+            // read-out before the accumulator's release costs about one load
+            // latency per read instead of a load and its wait per chunk.
+            auto read_bf16 = [&](uint32_t (&yb)[NC][16]) {
+                uint32_t ra[16], rb[16];
+                tmem_ld_32x32b_x16(tbase, ra);
+                tmem_ld_wait();
+#pragma unroll
+                for (int h = 0; h < 2 * NC; ++h) {
+                    uint32_t(&cur)[16] = (h & 1) ? rb : ra;
+                    uint32_t(&nxt)[16] = (h & 1) ? ra : rb;
+                    if (h + 1 < 2 * NC) tmem_ld_32x32b_x16(tbase + 16 * (h + 1), nxt);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float v0 = __uint_as_float(cur[2 * j]), v1 = __uint_as_float(cur[2 * j + 1]);
+                        if constexpr (KIND == KIND_NVFP4) {  // packed products feed only the conversion
+                            mul2(v0, v1, scale, scale, v0, v1);
+                            mul2(v0, v1, gb, gb, v0, v1);
+                        }
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
+                        yb[h >> 1][8 * (h & 1) + j] = *reinterpret_cast<uint32_t *>(&b2);
+                    }
+                    if (h + 1 < 2 * NC) tmem_ld_wait();
+                }
+            };
             if constexpr (SWI) {
                 // accumulator columns 0..127 hold the gate values, 128..255 the up
                 // values of the same 128 h columns.  y = acc * g_t * g_e is rounded
@@ -911,20 +938,7 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW, SHORT>::THREADS, 1)
                 // MMAs run -- the same arithmetic as the SwiGLU input mode of the
                 // row quantiser, so h equals the unfused path's bit for bit.
                 uint32_t yb[NC][16];
-#pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tbase + 32 * c, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {  // packed products feed only the bf16 conversion
-                        float v0, v1;
-                        mul2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]), scale, scale, v0, v1);
-                        mul2(v0, v1, gb, gb, v0, v1);
-                        __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
-                        yb[c][j] = *reinterpret_cast<uint32_t *>(&b2);
-                    }
-                }
+                read_bf16(yb);
                 release();
                 if (slice_any) {
 #pragma unroll
@@ -962,14 +976,14 @@ __global__ void __launch_bounds__(Cfg<KIND, TBN, EW, SHORT>::THREADS, 1)
                         for (int c = 0; c < NC; ++c) convert(reinterpret_cast<uint32_t (&)[32]>(ch[c]), c, ch[c]);
                     }
                 } else {
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(tbase + 32 * c, r);
-                        tmem_ld_wait();
-                        convert(r, c, ch[c]);
-                    }
+                    uint32_t yb[NC][16];  // bf16: the packed tile
+                    read_bf16(yb);
                     release();
+#pragma unroll
+                    for (int c = 0; c < NC; ++c)
+#pragma unroll
+                        for (int k = 0; k < NCH; ++k)
+                            ch[c][k] = make_uint4(yb[c][4 * k], yb[c][4 * k + 1], yb[c][4 * k + 2], yb[c][4 * k + 3]);
                 }
                 if (slice_any) {
 #pragma unroll
