@@ -1523,13 +1523,21 @@ pmn_status launch_quant_groups(const uint16_t *x, int64_t groups, int64_t blocks
     if (quant_groups_grid(&grid) != PMN_OK) return PMN_ERR_CUDA;
     if (cudaMemsetAsync(scratch, 0, quant_groups_scratch_bytes(groups), s) != cudaSuccess) return PMN_ERR_CUDA;
     const int64_t nch = (blocks_per_group + QG_CHUNK - 1) / QG_CHUNK;
-    // one group plus three quarters of an item per CTA: measured best with
-    // the L2 priorities above (a longer lead pushes re-reads out of L2, a
-    // shorter one makes coding items wait)
+    // Amax items lead the coding items of the same chunks by one group plus
+    // three quarters of an item per CTA, capped at 45 MB of chunks (about a
+    // third of L2) and never below one group: the chunks read for their amax
+    // wait in L2 for their coding, so a longer lead pushes them out and a
+    // shorter one makes coding items wait.  Measured (full-size step):
+    // uncapped, quant_w1 2.536 ms; capped at 600 / 690 / 780 items of 64 KB,
+    // 2.525 / 2.473 / 2.478 ms; quant_w2 (648 items) unchanged.
 #ifndef PMN_QG_LEAD_Q  // the lead beyond one group, in quarters of an item per CTA
 #define PMN_QG_LEAD_Q 3
 #endif
-    const int64_t lead = std::min(groups * nch, nch + (int64_t)grid * PMN_QG_LEAD_Q / 4);
+#ifndef PMN_QG_LEAD_CAP_MB
+#define PMN_QG_LEAD_CAP_MB 45
+#endif
+    const int64_t cap = ((int64_t)PMN_QG_LEAD_CAP_MB << 20) / ((int64_t)QG_CHUNK * 32);
+    const int64_t lead = std::min(groups * nch, std::max(nch, std::min(nch + (int64_t)grid * PMN_QG_LEAD_Q / 4, cap)));
     nvfp4_quant_groups_kernel<<<(unsigned)grid, QG_THREADS, 0, s>>>(x, groups, blocks_per_group, nch, lead,
                                                                      four_over_six, codes, scales, outer, scratch,
                                                                      pmn_wait_limit_ns());
